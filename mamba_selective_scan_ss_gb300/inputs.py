@@ -1,0 +1,122 @@
+"""Seeded synthetic inputs for the selective-scan forward workloads.
+
+This module only draws random tensors in the layouts of the C ABI; it holds
+none of the scan's arithmetic.  Both the CUDA path and the CPU oracle are fed
+from here, so that they see bit-identical inputs.
+
+Workload shapes (batch, dim, dstate, seqlen) and value distributions:
+  * u, delta_raw, z ~ N(0, 1), layout [batch, dim, seqlen]
+  * per-channel step size dt ~ LogUniform[lo, hi] and delta_bias = log(expm1(dt)),
+    i.e. the inverse of softplus, so softplus(0 + delta_bias) = dt
+  * A[d, n] = -(n + 1)                       (the real diagonal init of Mamba)
+  * B, C ~ N(0, 1), layout [batch, dstate, seqlen], shared by all channels
+  * D ~ N(0, 1), layout [dim]
+Draw order is u, delta_raw, dt, B, C, D, z from one torch CPU generator seeded
+with the workload's seed.  For bf16 workloads u, delta_raw, B, C and z are
+rounded to bf16 (round to nearest even) before either side sees them; A, D,
+delta_bias stay fp32.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, replace
+
+import torch
+
+
+@dataclass(frozen=True)
+class ScanWorkload:
+    name: str
+    batch: int
+    dim: int
+    dstate: int
+    seqlen: int
+    dtype: str = "f32"            # "f32" or "bf16": type of u, delta, B, C, z, y
+    has_z: bool = True
+    has_D: bool = True
+    has_bias: bool = True
+    softplus: bool = True
+    dt_lo: float = 1e-3
+    dt_hi: float = 1e-1
+    seed: int = 0
+
+    @property
+    def updates(self) -> int:
+        """State updates of one forward pass: batch * dim * seqlen * dstate."""
+        return self.batch * self.dim * self.seqlen * self.dstate
+
+    @property
+    def elt(self) -> int:
+        return 4 if self.dtype == "f32" else 2
+
+    def algorithmic_bytes(self) -> int:
+        """Bytes one forward pass must move at least once through HBM.
+
+        u, delta, (z) in and y out are [b, d, L]; B and C are [b, N, L];
+        A is [d, N]; D and delta_bias [d]; last_state [b, d, N] fp32 out.
+        """
+        bdl = self.batch * self.dim * self.seqlen
+        streams = 3 + (1 if self.has_z else 0)          # u, delta, y (+ z)
+        b = streams * bdl * self.elt
+        b += 2 * self.batch * self.dstate * self.seqlen * self.elt
+        b += 4 * self.dim * self.dstate
+        b += 4 * self.dim * (int(self.has_D) + int(self.has_bias))
+        b += 4 * self.batch * self.dim * self.dstate
+        return b
+
+    def with_(self, **kw) -> "ScanWorkload":
+        return replace(self, **kw)
+
+
+def _cfg4(L: int) -> ScanWorkload:
+    return ScanWorkload(f"seqlen-sweep-b16-d1536-n16-L{L}-f32", 16, 1536, 16, L, "f32",
+                        has_z=True, seed=4)
+
+
+WORKLOADS = {
+    "0": ScanWorkload("tiny-b2-d16-n16-L128-f32", 2, 16, 16, 128, "f32",
+                      has_z=False, seed=0),
+    "1": ScanWorkload("mamba130m-layer-b2-d1536-n16-L2048-f32", 2, 1536, 16, 2048, "f32",
+                      has_z=True, seed=1),
+    "2": ScanWorkload("mamba2.8b-layer-b8-d5120-n16-L2048-bf16", 8, 5120, 16, 2048, "bf16",
+                      has_z=True, seed=2),
+    "3": ScanWorkload("long-seq-b1-d2048-n16-L65536-bf16", 1, 2048, 16, 65536, "bf16",
+                      has_z=True, dt_lo=1e-4, dt_hi=1e-2, seed=3),
+    "4_256": _cfg4(256),
+    "4_1024": _cfg4(1024),
+    "4_4096": _cfg4(4096),
+    "4_16384": _cfg4(16384),
+}
+
+
+def make_inputs(w: ScanWorkload) -> dict:
+    """Draw one workload's inputs on the CPU (torch tensors, ABI layout)."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(w.seed)
+    b, d, n, L = w.batch, w.dim, w.dstate, w.seqlen
+    io = torch.float32 if w.dtype == "f32" else torch.bfloat16
+
+    u = torch.randn((b, d, L), generator=g, dtype=torch.float32)
+    delta = torch.randn((b, d, L), generator=g, dtype=torch.float32)
+    lo, hi = math.log(w.dt_lo), math.log(w.dt_hi)
+    dt = torch.exp(torch.rand((d,), generator=g, dtype=torch.float64) * (hi - lo) + lo)
+    Bm = torch.randn((b, n, L), generator=g, dtype=torch.float32)
+    Cm = torch.randn((b, n, L), generator=g, dtype=torch.float32)
+    D = torch.randn((d,), generator=g, dtype=torch.float32)
+    z = torch.randn((b, d, L), generator=g, dtype=torch.float32) if w.has_z else None
+
+    A = -torch.arange(1, n + 1, dtype=torch.float32).repeat(d, 1).contiguous()
+    bias = torch.log(torch.expm1(dt)).to(torch.float32)
+
+    out = {
+        "u": u.to(io).contiguous(),
+        "delta": delta.to(io).contiguous(),
+        "A": A,
+        "B": Bm.to(io).contiguous(),
+        "C": Cm.to(io).contiguous(),
+        "D": D if w.has_D else None,
+        "z": z.to(io).contiguous() if z is not None else None,
+        "delta_bias": bias if w.has_bias else None,
+        "delta_softplus": bool(w.softplus),
+    }
+    return out

@@ -1,0 +1,67 @@
+"""Each plausible mistake planted in a copy of the oracle fails at least one pin.
+
+The mutants are textual edits of ``oracle/ss_oracle.c`` compiled into a
+temporary library (CPU only).  A mutant that survives every pin would mean
+the pins cannot tell that mistake from the right answer.
+"""
+import pytest
+
+import oracle
+import oracle_pins
+
+MUTANTS = {
+    "dropped_u_in_input_term": ("h[n] = a_bar * h[n] + b_bar * u;",
+                                "h[n] = a_bar * h[n] + b_bar;"),
+    "sign_of_A": ("exp(dt * (double)j->A[d * N + n])",
+                  "exp(-dt * (double)j->A[d * N + n])"),
+    "missing_dt_in_decay": ("exp(dt * (double)j->A[d * N + n])",
+                            "exp((double)j->A[d * N + n])"),
+    "missing_dt_in_input": ("const double b_bar = dt * load_elem(",
+                            "const double b_bar = load_elem("),
+    "A_transposed": ("j->A[d * N + n]", "j->A[n * dim + d]"),
+    "dropped_D_skip": ("      y += Dd * u;\n", "\n"),
+    "D_indexed_by_batch": ("const double Dd = j->D ? (double)j->D[d] : 0.0;",
+                           "const double Dd = j->D ? (double)j->D[b] : 0.0;"),
+    "gate_before_skip": ("      y += Dd * u;\n      if (j->z) y *= silu(load_elem(j->z, x_idx, j->dtype));\n",
+                         "      if (j->z) y *= silu(load_elem(j->z, x_idx, j->dtype));\n      y += Dd * u;\n"),
+    "silu_sign": ("return z / (1.0 + exp(-z));", "return z / (1.0 + exp(z));"),
+    "softplus_dropped_log1p": ("return (x > 0.0 ? x : 0.0) + log1p(exp(-fabs(x)));",
+                               "return (x > 0.0 ? x : 0.0);"),
+    "softplus_missing_abs": ("log1p(exp(-fabs(x)))", "log1p(exp(-x))"),
+    "bias_ignored": ("load_elem(j->delta, x_idx, j->dtype) + bias;",
+                     "load_elem(j->delta, x_idx, j->dtype);"),
+    "B_layout_b_L_N": ("load_elem(j->B, (b * N + n) * L + t, j->dtype)",
+                       "load_elem(j->B, (b * L + t) * N + n, j->dtype)"),
+    "C_time_reversed": ("load_elem(j->C, (b * N + n) * L + t, j->dtype)",
+                        "load_elem(j->C, (b * N + n) * L + (L - 1 - t), j->dtype)"),
+    "readout_before_update": (
+        "        h[n] = a_bar * h[n] + b_bar * u;\n        y += load_elem(j->C, (b * N + n) * L + t, j->dtype) * h[n];\n",
+        "        y += load_elem(j->C, (b * N + n) * L + t, j->dtype) * h[n];\n        h[n] = a_bar * h[n] + b_bar * u;\n"),
+    "h0_ignored": ("h[n] = j->h0 ? j->h0[row * N + n] : 0.0;", "h[n] = 0.0;"),
+    "channel_from_wrong_axis": ("const int64_t b = row / dim, d = row % dim;",
+                                "const int64_t b = row % j->batch, d = row / j->batch;"),
+    "bf16_widening_truncated": ("(uint32_t)((const uint16_t*)p)[i] << 16",
+                                "((uint32_t)((const uint16_t*)p)[i] << 16) & 0xFFFF0000u & ~0x10000u"),
+    "combine_swapped_factor": ("const double v = a2[i] * v1[i] + c2[i];",
+                               "const double v = a1[i] * v1[i] + c2[i];"),
+    "combine_product_wrong": ("const double a = a2[i] * a1[i];",
+                              "const double a = a2[i] + a1[i] - 1.0;"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name, tmp_path):
+    old, new = MUTANTS[name]
+    src = oracle.SOURCE.read_text()
+    assert src.count(old) == 1, f"mutation {name} does not apply exactly once"
+    mutant_src = tmp_path / "ss_oracle_mutant.c"
+    mutant_src.write_text(src.replace(old, new))
+    lib = oracle.build(mutant_src, tmp_path / "libmutant.so", force=True)
+    orc = oracle.Oracle(lib)
+    failed = []
+    for pin in oracle_pins.ALL_PINS:
+        try:
+            pin(orc)
+        except AssertionError:
+            failed.append(pin.__name__)
+    assert failed, f"mutant {name} passes every pin"
