@@ -1,0 +1,121 @@
+/*
+ * ss_selective_scan.h -- C ABI of the GB300 (sm_103a) selective-scan forward.
+ *
+ * The operation is the forward pass of the Mamba selective scan, the
+ * input-dependent diagonal linear recurrence defined by
+ *   - "ТЕХНИЧЕСКОЕ ЗАДАНИЕ: Реализовать selective scan (Mamba)", Этап 1,
+ *     steps 3-4 (discretisation A_bar = exp(delta*A), B_bar = delta*B,
+ *     delta = softplus(.), read-out C*state + D*u, silu(z) gate);
+ *   - "Mamba CUDA 实现解析" (mamba-code-explained), eq (4)-(7): channels are
+ *     independent, A is a length-N vector per channel, and every state
+ *     element follows v_k = a_k v_{k-1} + b_k u_k;
+ *   - the same page, eq (10)-(12): the recurrence is a prefix scan under the
+ *     associative operator (a1, v1) (+) (a2, c2) = (a2 a1, a2 v1 + c2), which
+ *     is how the library evaluates it in parallel over time.
+ *
+ * For every batch b, channel d, state n and step t (state zero at t = 0):
+ *   dt = delta[b,d,t] + delta_bias[d];  if (delta_softplus) dt = log(1 + e^dt)
+ *   h[n] = exp(dt * A[d,n]) * h[n] + dt * B[b,n,t] * u[b,d,t]
+ *   y[b,d,t] = (sum_n C[b,n,t] * h[n] + D[d] * u[b,d,t]) * silu(z[b,d,t])
+ *   last_state[b,d,n] = h[n] after the last step
+ * where the silu factor is 1 when z is NULL, D NULL means D = 0 and
+ * delta_bias NULL means a zero bias.
+ *
+ * Threading and lifetime: the library keeps no pointer after a call returns
+ * and holds no global state besides a per-device error word (see
+ * ss_selective_scan_check).  Calls on different streams may run concurrently.
+ */
+#ifndef SS_SELECTIVE_SCAN_H_
+#define SS_SELECTIVE_SCAN_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(SS_BUILDING_LIBRARY)
+#define SS_API __attribute__((visibility("default")))
+#else
+#define SS_API
+#endif
+
+/* Element type of u, delta, B, C, z and y.  A, D, delta_bias, last_state and
+ * the internal state are always float32. */
+typedef enum {
+  SS_F32 = 0,  /* IEEE float32 */
+  SS_BF16 = 1  /* bfloat16; y is rounded to nearest even */
+} ss_dtype_t;
+
+typedef enum {
+  SS_OK = 0,
+  SS_ERR_INVALID_ARGUMENT = 1, /* null required pointer, size <= 0, overlap of
+                                  an output with an input, misaligned pointer */
+  SS_ERR_UNSUPPORTED = 2,      /* unknown dtype, dstate outside 1..256, or a
+                                  size that overflows 64-bit indexing */
+  SS_ERR_CUDA = 3,             /* a CUDA runtime call or a launch failed */
+  SS_ERR_TIMEOUT = 4           /* a device-side wait gave up (reported by
+                                  ss_selective_scan_check only) */
+} ss_status_t;
+
+/*
+ * ss_selective_scan_fwd -- enqueue one selective-scan forward on `stream`.
+ *
+ * Arguments (all pointers are DEVICE pointers owned by the caller; all
+ * arrays are dense, row-major, with the last index contiguous):
+ *   u          [batch, dim, seqlen]      dtype      input sequence
+ *   delta      [batch, dim, seqlen]      dtype      raw step size (before bias/softplus)
+ *   A          [dim, dstate]             float32    diagonal state matrix (normally < 0)
+ *   B          [batch, dstate, seqlen]   dtype      input projection, shared by all channels
+ *   C          [batch, dstate, seqlen]   dtype      output projection, shared by all channels
+ *   D          [dim]                     float32    skip weight, or NULL (D = 0)
+ *   z          [batch, dim, seqlen]      dtype      gate input, or NULL (no gate)
+ *   delta_bias [dim]                     float32    step-size bias, or NULL (0)
+ *   delta_softplus                       nonzero: dt = softplus(delta + bias)
+ *                                        zero:    dt = delta + bias
+ *   y          [batch, dim, seqlen]      dtype      output (written, never read)
+ *   last_state [batch, dim, dstate]      float32    final state, or NULL (not written)
+ *   batch, dim, dstate, seqlen           sizes; each must be >= 1
+ *   dtype                                SS_F32 or SS_BF16
+ *   stream                               a cudaStream_t (NULL = legacy default stream)
+ *
+ * Alignment: every pointer must be aligned to its element size (4 bytes for
+ * float32 arrays, 2 bytes for bf16 arrays).  Rows whose start is also
+ * 16-byte aligned take the vectorised path; others take a scalar path.
+ *
+ * Behaviour: arguments are validated on the host first; on any error the
+ * function returns that status, launches nothing and writes nothing.  On
+ * success the work is enqueued on `stream` and the call returns without
+ * synchronising; y and last_state are complete when the stream reaches that
+ * point.  Long sequences use stream-ordered scratch memory
+ * (cudaMallocAsync/cudaFreeAsync on `stream`) for the carries between
+ * sequence chunks.  A device-side wait that gives up sets a per-device error
+ * word that ss_selective_scan_check reports; no call traps.
+ *
+ * Limits: dstate in 1..256 (tuned for 16); seqlen and batch*dim*seqlen are
+ * limited only by 64-bit indexing.  y must not overlap any input.
+ */
+SS_API ss_status_t ss_selective_scan_fwd(
+    const void* u, const void* delta, const float* A, const void* B, const void* C,
+    const float* D, const void* z, const float* delta_bias, int delta_softplus,
+    void* y, float* last_state,
+    int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
+    ss_dtype_t dtype, void* stream);
+
+/* Human-readable name of a status code (static storage, never NULL). */
+SS_API const char* ss_status_string(ss_status_t status);
+
+/*
+ * ss_selective_scan_check -- synchronise `stream`, then report and clear the
+ * device-side error word of the current device.  Returns SS_OK when every
+ * call enqueued so far completed normally, SS_ERR_TIMEOUT when a bounded
+ * device-side wait gave up, and SS_ERR_CUDA when the stream reports a CUDA
+ * error.
+ */
+SS_API ss_status_t ss_selective_scan_check(void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SS_SELECTIVE_SCAN_H_ */

@@ -1,0 +1,133 @@
+"""GB300-native Mamba selective-scan forward: Python binding of the C ABI.
+
+This module only marshals arguments to ``libss_selective_scan.so`` (see
+``include/ss_selective_scan.h``); every step of the computation runs in the
+library's CUDA kernels.  If the library has not been built, the functions
+raise: there is no fallback implementation.
+
+Low-level names mirror the C ABI exactly (raw device pointers as ints):
+    ss_selective_scan_fwd, ss_status_string, ss_selective_scan_check
+plus a convenience wrapper for torch CUDA tensors:
+    selective_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None,
+                       delta_softplus=True, ...)
+"""
+from __future__ import annotations
+
+import ctypes
+from pathlib import Path
+
+__all__ = [
+    "SS_F32", "SS_BF16", "SS_OK", "SS_ERR_INVALID_ARGUMENT", "SS_ERR_UNSUPPORTED",
+    "SS_ERR_CUDA", "SS_ERR_TIMEOUT", "SelectiveScanError", "library_path", "load_library",
+    "ss_selective_scan_fwd", "ss_status_string", "ss_selective_scan_check",
+    "selective_scan_fwd",
+]
+
+SS_F32, SS_BF16 = 0, 1
+SS_OK, SS_ERR_INVALID_ARGUMENT, SS_ERR_UNSUPPORTED, SS_ERR_CUDA, SS_ERR_TIMEOUT = range(5)
+
+_PKG = Path(__file__).resolve().parent
+_LIB = None
+
+
+class SelectiveScanError(RuntimeError):
+    def __init__(self, status: int, what: str = "ss_selective_scan_fwd"):
+        self.status = status
+        super().__init__(f"{what} failed: {ss_status_string(status)}")
+
+
+def library_path() -> Path:
+    return _PKG / "libss_selective_scan.so"
+
+
+def load_library():
+    """Load the native library (raises if it was not built)."""
+    global _LIB
+    if _LIB is None:
+        path = library_path()
+        if not path.exists():
+            raise RuntimeError(
+                f"{path.name} is missing: build it with __graft_entry__.build() "
+                "(the selective scan has no non-CUDA implementation)")
+        lib = ctypes.CDLL(str(path))
+        vp, i64 = ctypes.c_void_p, ctypes.c_int64
+        lib.ss_selective_scan_fwd.restype = ctypes.c_int
+        lib.ss_selective_scan_fwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_int,
+                                              vp, vp, i64, i64, i64, i64, ctypes.c_int, vp]
+        lib.ss_status_string.restype = ctypes.c_char_p
+        lib.ss_status_string.argtypes = [ctypes.c_int]
+        lib.ss_selective_scan_check.restype = ctypes.c_int
+        lib.ss_selective_scan_check.argtypes = [vp]
+        _LIB = lib
+    return _LIB
+
+
+def ss_selective_scan_fwd(u, delta, A, B, C, D, z, delta_bias, delta_softplus, y, last_state,
+                          batch, dim, dstate, seqlen, dtype, stream) -> int:
+    """Direct call of the C entry point; pointers are ints (0/None = NULL)."""
+    return load_library().ss_selective_scan_fwd(
+        u, delta, A, B, C, D, z, delta_bias, int(delta_softplus), y, last_state,
+        batch, dim, dstate, seqlen, int(dtype), stream)
+
+
+def ss_status_string(status: int) -> str:
+    return load_library().ss_status_string(int(status)).decode()
+
+
+def ss_selective_scan_check(stream=None) -> int:
+    return load_library().ss_selective_scan_check(stream)
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def selective_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None,
+                       delta_softplus: bool = True, return_last_state: bool = True,
+                       y=None, last_state=None, stream=None):
+    """Run the forward on torch CUDA tensors in the ABI layouts.
+
+    u, delta, z: [batch, dim, seqlen]; B, C: [batch, dstate, seqlen]; A:
+    [dim, dstate] fp32; D, delta_bias: [dim] fp32.  u, delta, B, C, z share one
+    dtype (float32 or bfloat16), which is also y's dtype.  Returns y, or
+    (y, last_state) with last_state [batch, dim, dstate] fp32.  Outputs are
+    allocated with torch unless given.  Runs on ``stream`` (a torch.cuda.Stream
+    or a raw cudaStream_t int), default torch's current stream.
+    """
+    import torch
+
+    if u.dtype == torch.float32:
+        dt = SS_F32
+    elif u.dtype == torch.bfloat16:
+        dt = SS_BF16
+    else:
+        raise TypeError(f"unsupported dtype {u.dtype}")
+    for name, t in (("delta", delta), ("B", B), ("C", C), ("z", z)):
+        if t is not None and t.dtype != u.dtype:
+            raise TypeError(f"{name} must have dtype {u.dtype}")
+    for name, t in (("A", A), ("D", D), ("delta_bias", delta_bias)):
+        if t is not None and t.dtype != torch.float32:
+            raise TypeError(f"{name} must be float32")
+    tensors = [u, delta, A, B, C, D, z, delta_bias]
+    for t in tensors:
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError("all tensors must be contiguous CUDA tensors")
+    batch, dim, seqlen = u.shape
+    dstate = A.shape[1]
+    if y is None:
+        y = torch.empty_like(u)
+    if last_state is None and return_last_state:
+        last_state = torch.empty((batch, dim, dstate), device=u.device, dtype=torch.float32)
+    if stream is None:
+        s = torch.cuda.current_stream(u.device).cuda_stream
+    elif isinstance(stream, int):
+        s = stream
+    else:
+        s = stream.cuda_stream
+    status = ss_selective_scan_fwd(
+        _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias),
+        delta_softplus, _ptr(y), _ptr(last_state) if return_last_state else None,
+        batch, dim, dstate, seqlen, dt, s)
+    if status != SS_OK:
+        raise SelectiveScanError(status)
+    return (y, last_state) if return_last_state else y

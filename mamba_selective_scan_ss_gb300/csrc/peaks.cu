@@ -1,0 +1,308 @@
+// Unit-throughput microbenchmarks for the roofline of the selective-scan
+// forward kernel.
+//
+// The selective-scan update is bound by arithmetic issue rather than by a
+// dense contraction, so the roofline needs three per-SM unit rates that the
+// public specifications do not state for this part:
+//   * MUFU ex2 results per clock per SM   (the decay exp(dt*A) of every update)
+//   * FP32 FMA lane-ops per clock per SM  (scalar FFMA)
+//   * FP32 FMA lane-ops per clock per SM  (packed f32x2 FFMA, sm_100 family)
+// plus one probe of the update body itself with all operands on chip, which
+// bounds what any kernel built around that body can reach.
+//
+// Each probe keeps several independent dependency chains per thread so that
+// latency is hidden and the unit, not the chain, is the limit.  Clocks are
+// measured inside the kernel (clock64 against globaltimer) so the per-clock
+// figures are independent of whatever SM clock the part runs at.
+//
+// This file is built into its own shared library (libss_peaks.so); the
+// selective-scan library does not link it.
+
+#include <cuda_runtime.h>
+#include <cstdint>
+#include <cstdio>
+
+namespace {
+
+constexpr int kChains = 8;
+
+struct ClockRec {
+  unsigned long long clk0, clk1, ns0, ns1;
+};
+
+__device__ __forceinline__ unsigned long long globaltimer_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ void record_start(ClockRec* rec) {
+  if (threadIdx.x == 0) {
+    rec[blockIdx.x].clk0 = clock64();
+    rec[blockIdx.x].ns0 = globaltimer_ns();
+  }
+}
+__device__ __forceinline__ void record_end(ClockRec* rec) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    rec[blockIdx.x].clk1 = clock64();
+    rec[blockIdx.x].ns1 = globaltimer_ns();
+  }
+}
+
+// x <- 2^(-x) stays inside [0.5, 1] for x in [0, 1]: no overflow, no denormals.
+__global__ void k_ex2(float* out, int iters, ClockRec* rec) {
+  float x[kChains];
+#pragma unroll
+  for (int j = 0; j < kChains; ++j) x[j] = 1e-3f * (threadIdx.x + 7 * j);
+  __syncthreads();
+  record_start(rec);
+  for (int i = 0; i < iters; ++i) {
+#pragma unroll
+    for (int j = 0; j < kChains; ++j) x[j] = ex2_approx(-x[j]);
+  }
+  float s = 0.f;
+#pragma unroll
+  for (int j = 0; j < kChains; ++j) s += x[j];
+  record_end(rec);
+  out[blockIdx.x * blockDim.x + threadIdx.x] = s;
+}
+
+// x <- x*a + b with |a| < 1 converges: the chains stay finite.
+__global__ void k_ffma(float* out, int iters, float a, float b, ClockRec* rec) {
+  float x[kChains];
+#pragma unroll
+  for (int j = 0; j < kChains; ++j) x[j] = 1e-3f * (threadIdx.x + 7 * j);
+  __syncthreads();
+  record_start(rec);
+  for (int i = 0; i < iters; ++i) {
+#pragma unroll
+    for (int j = 0; j < kChains; ++j) x[j] = fmaf(x[j], a, b);
+  }
+  float s = 0.f;
+#pragma unroll
+  for (int j = 0; j < kChains; ++j) s += x[j];
+  record_end(rec);
+  out[blockIdx.x * blockDim.x + threadIdx.x] = s;
+}
+
+__device__ __forceinline__ unsigned long long pack2(float lo, float hi) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1,%2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void unpack2(unsigned long long v, float& lo, float& hi) {
+  asm("mov.b64 {%0,%1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
+// Same chains as k_ffma, two lanes-ops per instruction (fma.rn.f32x2).
+__global__ void k_ffma2(float* out, int iters, float a, float b, ClockRec* rec) {
+  unsigned long long x[kChains];
+#pragma unroll
+  for (int j = 0; j < kChains; ++j)
+    x[j] = pack2(1e-3f * (threadIdx.x + 7 * j), 2e-3f * (threadIdx.x + 5 * j));
+  const unsigned long long A = pack2(a, a), B = pack2(b, b);
+  __syncthreads();
+  record_start(rec);
+  for (int i = 0; i < iters; ++i) {
+#pragma unroll
+    for (int j = 0; j < kChains; ++j)
+      asm("fma.rn.f32x2 %0, %0, %1, %2;" : "+l"(x[j]) : "l"(A), "l"(B));
+  }
+  float s = 0.f;
+#pragma unroll
+  for (int j = 0; j < kChains; ++j) {
+    float lo, hi;
+    unpack2(x[j], lo, hi);
+    s += lo + hi;
+  }
+  record_end(rec);
+  out[blockIdx.x * blockDim.x + threadIdx.x] = s;
+}
+
+// The selective-scan update body with every operand on chip.  Per time step a
+// thread owning one channel row and all 16 states does, for each state n,
+//   a = 2^(dt*A2[n]); h[n] = a*h[n] + du*B[n]; y += C[n]*h[n]
+// with dt, du and the B/C rows read from shared memory as the real kernel
+// does.  kPacked selects the scalar or the packed f32x2 form of the FP32 work.
+template <bool kPacked>
+__global__ void k_update(float* out, int steps, ClockRec* rec) {
+  constexpr int N = 16;
+  constexpr int T = 64;
+  __shared__ __align__(16) float sB[T][N];
+  __shared__ __align__(16) float sC[T][N];
+  __shared__ __align__(16) float sDt[T][32];
+  __shared__ __align__(16) float sDu[T][32];
+  for (int i = threadIdx.x; i < T * N; i += blockDim.x) {
+    (&sB[0][0])[i] = 0.01f * ((i * 37) % 101) - 0.5f;
+    (&sC[0][0])[i] = 0.01f * ((i * 53) % 97) - 0.5f;
+  }
+  for (int i = threadIdx.x; i < T * 32; i += blockDim.x) {
+    (&sDt[0][0])[i] = 1e-3f + 1e-4f * (i % 89);
+    (&sDu[0][0])[i] = 0.01f * ((i * 29) % 83) - 0.4f;
+  }
+  float A2[N];
+#pragma unroll
+  for (int n = 0; n < N; ++n) A2[n] = -1.4426950f * (n + 1);
+  __syncthreads();
+  record_start(rec);
+  const int lane = threadIdx.x & 31;
+  float ysum = 0.f;
+  if (!kPacked) {
+    float h[N];
+#pragma unroll
+    for (int n = 0; n < N; ++n) h[n] = 0.f;
+    for (int s = 0; s < steps; ++s) {
+      const int t = s & (T - 1);
+      const float dt = sDt[t][lane];
+      const float du = sDu[t][lane];
+      float y = 0.f;
+#pragma unroll
+      for (int q = 0; q < N / 4; ++q) {
+        const float4 b4 = *reinterpret_cast<const float4*>(&sB[t][4 * q]);
+        const float4 c4 = *reinterpret_cast<const float4*>(&sC[t][4 * q]);
+        const float bb[4] = {b4.x, b4.y, b4.z, b4.w};
+        const float cc[4] = {c4.x, c4.y, c4.z, c4.w};
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const int n = 4 * q + r;
+          const float a = ex2_approx(dt * A2[n]);
+          h[n] = fmaf(a, h[n], du * bb[r]);
+          y = fmaf(cc[r], h[n], y);
+        }
+      }
+      ysum += y;
+    }
+#pragma unroll
+    for (int n = 0; n < N; ++n) ysum += h[n];
+  } else {
+    unsigned long long h[N / 2], A2p[N / 2];
+#pragma unroll
+    for (int p = 0; p < N / 2; ++p) {
+      h[p] = 0ull;
+      A2p[p] = pack2(A2[2 * p], A2[2 * p + 1]);
+    }
+    for (int s = 0; s < steps; ++s) {
+      const int t = s & (T - 1);
+      const float dt = sDt[t][lane];
+      const float du = sDu[t][lane];
+      const unsigned long long dt2 = pack2(dt, dt), du2 = pack2(du, du);
+      unsigned long long y2 = 0ull;
+#pragma unroll
+      for (int q = 0; q < N / 4; ++q) {
+        const ulonglong2 b4 = *reinterpret_cast<const ulonglong2*>(&sB[t][4 * q]);
+        const ulonglong2 c4 = *reinterpret_cast<const ulonglong2*>(&sC[t][4 * q]);
+        const unsigned long long bb[2] = {b4.x, b4.y};
+        const unsigned long long cc[2] = {c4.x, c4.y};
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          const int p = 2 * q + r;
+          unsigned long long x2, c2;
+          asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(x2) : "l"(dt2), "l"(A2p[p]));
+          float x0, x1;
+          unpack2(x2, x0, x1);
+          const unsigned long long a2 = pack2(ex2_approx(x0), ex2_approx(x1));
+          asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(c2) : "l"(du2), "l"(bb[r]));
+          asm("fma.rn.f32x2 %0, %1, %0, %2;" : "+l"(h[p]) : "l"(a2), "l"(c2));
+          asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(y2) : "l"(cc[r]), "l"(h[p]));
+        }
+      }
+      float lo, hi;
+      unpack2(y2, lo, hi);
+      ysum += lo + hi;
+    }
+#pragma unroll
+    for (int p = 0; p < N / 2; ++p) {
+      float lo, hi;
+      unpack2(h[p], lo, hi);
+      ysum += lo + hi;
+    }
+  }
+  record_end(rec);
+  out[blockIdx.x * blockDim.x + threadIdx.x] = ysum;
+}
+
+}  // namespace
+
+// which: 0 = ex2, 1 = ffma, 2 = ffma2 (packed), 3 = update body scalar,
+//        4 = update body packed.
+// result[0] = lane-ops (or state updates) per second over the whole GPU
+// result[1] = lane-ops (or updates) per clock per SM
+// result[2] = mean SM clock during the run, MHz
+// result[3] = number of SMs
+// result[4] = elapsed milliseconds
+// Returns 0 on success, a cudaError_t value otherwise.
+extern "C" __attribute__((visibility("default"))) int ss_peaks_measure(int which, int iters, int blocks_per_sm, int threads,
+                                double* result) {
+  cudaDeviceProp prop;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return (int)e;
+  e = cudaGetDeviceProperties(&prop, dev);
+  if (e != cudaSuccess) return (int)e;
+  const int sms = prop.multiProcessorCount;
+  const int blocks = sms * blocks_per_sm;
+  float* out = nullptr;
+  ClockRec* rec = nullptr;
+  e = cudaMalloc(&out, sizeof(float) * (size_t)blocks * threads);
+  if (e != cudaSuccess) return (int)e;
+  e = cudaMalloc(&rec, sizeof(ClockRec) * blocks);
+  if (e != cudaSuccess) { cudaFree(out); return (int)e; }
+  cudaEvent_t ev0, ev1;
+  cudaEventCreate(&ev0);
+  cudaEventCreate(&ev1);
+  auto launch = [&]() {
+    switch (which) {
+      case 0: k_ex2<<<blocks, threads>>>(out, iters, rec); break;
+      case 1: k_ffma<<<blocks, threads>>>(out, iters, 0.999f, 1e-3f, rec); break;
+      case 2: k_ffma2<<<blocks, threads>>>(out, iters, 0.999f, 1e-3f, rec); break;
+      case 3: k_update<false><<<blocks, threads>>>(out, iters, rec); break;
+      case 4: k_update<true><<<blocks, threads>>>(out, iters, rec); break;
+      default: break;
+    }
+  };
+  launch();  // warm-up
+  cudaEventRecord(ev0);
+  launch();
+  cudaEventRecord(ev1);
+  e = cudaEventSynchronize(ev1);
+  if (e == cudaSuccess) e = cudaGetLastError();
+  float ms = 0.f;
+  cudaEventElapsedTime(&ms, ev0, ev1);
+  ClockRec* h = new ClockRec[blocks];
+  if (e == cudaSuccess) e = cudaMemcpy(h, rec, sizeof(ClockRec) * blocks, cudaMemcpyDeviceToHost);
+  double mhz = 0.0;
+  int cnt = 0;
+  for (int i = 0; i < blocks; ++i) {
+    const double dc = (double)(h[i].clk1 - h[i].clk0);
+    const double dn = (double)(h[i].ns1 - h[i].ns0);
+    if (dn > 0) { mhz += 1e3 * dc / dn; ++cnt; }
+  }
+  delete[] h;
+  if (cnt) mhz /= cnt;
+  double per_thread = 0.0;
+  switch (which) {
+    case 0: case 1: per_thread = (double)iters * kChains; break;
+    case 2: per_thread = 2.0 * iters * kChains; break;
+    case 3: case 4: per_thread = 16.0 * iters; break;
+    default: break;
+  }
+  const double total = per_thread * blocks * threads;
+  const double per_s = total / (ms * 1e-3);
+  result[0] = per_s;
+  result[1] = (mhz > 0) ? per_s / (mhz * 1e6 * sms) : 0.0;
+  result[2] = mhz;
+  result[3] = sms;
+  result[4] = ms;
+  cudaEventDestroy(ev0);
+  cudaEventDestroy(ev1);
+  cudaFree(out);
+  cudaFree(rec);
+  return (int)e;
+}

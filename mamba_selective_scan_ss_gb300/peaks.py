@@ -1,0 +1,50 @@
+"""Loader for the unit-throughput microbenchmarks (libss_peaks.so).
+
+The roofline of the selective-scan forward kernel needs the per-SM rates of
+the MUFU ex2 unit and of the FP32 FMA pipe, which are measured here on the
+device at hand rather than taken from a data sheet.
+"""
+from __future__ import annotations
+
+import ctypes
+from pathlib import Path
+
+_LIB = None
+
+PROBES = {
+    "ex2": 0,             # MUFU ex2 results
+    "ffma": 1,            # scalar FP32 FMA lane-ops
+    "ffma2": 2,           # packed f32x2 FMA lane-ops
+    "update_scalar": 3,   # selective-scan state updates, scalar FP32 body
+    "update_packed": 4,   # selective-scan state updates, f32x2 body
+}
+
+DEFAULT_ITERS = {"ex2": 20000, "ffma": 40000, "ffma2": 20000,
+                 "update_scalar": 4000, "update_packed": 4000}
+
+
+def _lib():
+    global _LIB
+    if _LIB is None:
+        path = Path(__file__).resolve().parent / "libss_peaks.so"
+        if not path.exists():
+            raise RuntimeError(f"{path.name} is not built; run __graft_entry__.build()")
+        lib = ctypes.CDLL(str(path))
+        lib.ss_peaks_measure.restype = ctypes.c_int
+        lib.ss_peaks_measure.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                         ctypes.c_int, ctypes.POINTER(ctypes.c_double)]
+        _LIB = lib
+    return _LIB
+
+
+def measure(probe: str, iters: int | None = None, blocks_per_sm: int = 4,
+            threads: int = 256) -> dict:
+    """Run one probe; returns rates over the GPU and per clock per SM."""
+    res = (ctypes.c_double * 5)()
+    it = iters if iters is not None else DEFAULT_ITERS[probe]
+    rc = _lib().ss_peaks_measure(PROBES[probe], it, blocks_per_sm, threads, res)
+    if rc != 0:
+        raise RuntimeError(f"peaks probe {probe} failed with CUDA error {rc}")
+    return {"probe": probe, "per_s": res[0], "per_clk_per_sm": res[1],
+            "sm_mhz": res[2], "sms": int(res[3]), "ms": res[4],
+            "blocks_per_sm": blocks_per_sm, "threads": threads}

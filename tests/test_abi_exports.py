@@ -1,0 +1,80 @@
+"""The C-ABI library builds, loads and exports every symbol its header declares;
+host-side argument validation rejects bad calls before touching the device.
+CPU only: no call here reaches a kernel or the CUDA runtime."""
+import ctypes
+import re
+import subprocess
+from pathlib import Path
+
+import pytest
+
+from mamba_selective_scan_ss_gb300 import _build
+import mamba_selective_scan_ss_gb300 as ss
+
+HEADER = Path(__file__).resolve().parent.parent / "include" / "ss_selective_scan.h"
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build_all()
+    return ss.load_library()
+
+
+def declared_functions():
+    text = HEADER.read_text()
+    return sorted(set(re.findall(r"SS_API\s+[\w\s\*]+?\b(ss_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    assert declared_functions() == ["ss_selective_scan_check", "ss_selective_scan_fwd",
+                                    "ss_status_string"]
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", str(ss.library_path())],
+                         capture_output=True, text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (ss_\w+)", out))
+    for name in declared_functions():
+        assert name in exported, name
+        assert hasattr(lib, name)
+
+
+def test_status_strings(lib):
+    assert ss.ss_status_string(ss.SS_OK) == "SS_OK"
+    assert ss.ss_status_string(ss.SS_ERR_TIMEOUT) == "SS_ERR_TIMEOUT"
+    assert ss.ss_status_string(99) == "SS_UNKNOWN_STATUS"
+
+
+def _fake_ptrs():
+    # host buffers stand in for device pointers: validation never dereferences them
+    bufs = [ctypes.create_string_buffer(4096) for _ in range(11)]
+    return bufs, [ctypes.addressof(b) for b in bufs]
+
+
+def test_validation_rejects_bad_arguments(lib):
+    bufs, p = _fake_ptrs()
+    u, dl, A, B, C, D, z, bias, y, st, _ = p
+    ok = dict(u=u, delta=dl, A=A, B=B, C=C, D=D, z=z, delta_bias=bias, delta_softplus=1,
+              y=y, last_state=st, batch=1, dim=2, dstate=4, seqlen=8, dtype=ss.SS_F32,
+              stream=None)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return ss.ss_selective_scan_fwd(**a)
+
+    assert call(u=None) == ss.SS_ERR_INVALID_ARGUMENT
+    assert call(B=None) == ss.SS_ERR_INVALID_ARGUMENT
+    assert call(y=None) == ss.SS_ERR_INVALID_ARGUMENT
+    assert call(batch=0) == ss.SS_ERR_INVALID_ARGUMENT       # batch=0: refused, no crash
+    assert call(seqlen=0) == ss.SS_ERR_INVALID_ARGUMENT
+    assert call(dim=-3) == ss.SS_ERR_INVALID_ARGUMENT
+    assert call(dstate=257) == ss.SS_ERR_UNSUPPORTED
+    assert call(dtype=7) == ss.SS_ERR_UNSUPPORTED
+    assert call(batch=1 << 40, dim=1 << 30) == ss.SS_ERR_UNSUPPORTED   # overflows int64
+    assert call(y=u) == ss.SS_ERR_INVALID_ARGUMENT           # output aliases an input
+    assert call(y=u + 16) == ss.SS_ERR_INVALID_ARGUMENT      # partial overlap
+    assert call(last_state=dl) == ss.SS_ERR_INVALID_ARGUMENT
+    assert call(last_state=y) == ss.SS_ERR_INVALID_ARGUMENT
+    assert call(u=u + 1) == ss.SS_ERR_INVALID_ARGUMENT       # misaligned fp32 pointer
+    assert call(A=A + 2) == ss.SS_ERR_INVALID_ARGUMENT
+    assert call(u=u + 1, dtype=ss.SS_BF16) == ss.SS_ERR_INVALID_ARGUMENT  # odd bf16 address
