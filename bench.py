@@ -1,0 +1,470 @@
+"""Benchmark of the selective-scan forward on GB300: state-updates/s and roofline.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload KEY]
+
+A step is one selective-scan forward (one ss_selective_scan_fwd call) over the
+workload's synthetic inputs, already resident in HBM.  The default workload is
+the Mamba-130M-shaped layer (batch 2, dim 1536, dstate 16, seqlen 2048, fp32
+I/O, silu gate).  Its inputs (about 100 MB) fit in the 129 MB L2, so the timed
+steps rotate over enough input sets to exceed twice the L2 size.
+
+Under torchrun each rank runs the same workload on its own GPU (weak scaling,
+no collective on the data path); rank 0 prints one JSON line with the
+whole-job throughput measured over the slowest rank.
+
+--impl reference times the CPU oracle (the plain fp64 C implementation the
+tests check against) on the host cores, on a bounded sample of the same
+workload, and prints the same metric.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+from pathlib import Path
+
+REPO = Path(__file__).resolve().parent
+sys.path.insert(0, str(REPO))
+
+METRIC = "selective-scan fwd state-updates/s (B*D*L*N/s) at 1 GB300; % of roofline"
+L2_BYTES = 129 * 2**20
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=4000)
+    ap.add_argument("--warmup", type=int, default=40)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="1", help="workload key (see inputs.WORKLOADS)")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-baseline-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--reference-seconds", type=float, default=150.0,
+                    help="total CPU time budget of the reference arm's timed steps")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------- distributed
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        import torch
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(value: float, world: int) -> float:
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_id: str, period_ms: int = 50):
+        self.gpu_id = gpu_id
+        self.period_ms = period_ms
+        self.proc = None
+        self.lines: list[str] = []
+
+    def _query(self, extra=()):
+        return ["nvidia-smi", "-i", self.gpu_id, f"--query-gpu={self.FIELDS}",
+                "--format=csv,noheader,nounits", *extra]
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(self._query([f"-lms", str(self.period_ms)]),
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        self._reader = threading.Thread(target=self._read, daemon=True)
+        if self.proc:
+            self._reader.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            if line.strip():
+                self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self._reader.join(timeout=2)
+        samples = list(self.lines)
+        if not samples:  # region shorter than one period: one sample right after
+            try:
+                out = subprocess.run(self._query(), capture_output=True, text=True, timeout=20)
+                samples = [l.strip() for l in out.stdout.splitlines() if l.strip()]
+            except (FileNotFoundError, OSError, subprocess.TimeoutExpired):
+                samples = []
+        sm, smax, power, reasons = [], [], [], set()
+        for line in samples:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+                power.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(self.REASONS, parts[3:7]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_max": max(power) if power else None}
+
+
+def gpu_id_for(device_index: int) -> str:
+    import torch
+    props = torch.cuda.get_device_properties(device_index)
+    uuid = getattr(props, "uuid", None)
+    if uuid is not None:
+        s = str(uuid)
+        return s if s.startswith("GPU-") else f"GPU-{s}"
+    return str(device_index)
+
+
+# ---------------------------------------------------------------- peaks
+def measured_peaks() -> dict:
+    p = REPO / "MEASURED_PEAKS.json"
+    if p.exists():
+        try:
+            d = json.loads(p.read_text())
+            return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+        except (ValueError, KeyError):
+            pass
+    return {"hbm_gbs": FALLBACK_HBM_GBS, "source": "fallback"}
+
+
+def unit_rates() -> dict:
+    """Per-clock per-SM rates of MUFU ex2 and FP32 FMA lane-ops (microbenchmarks)."""
+    from mamba_selective_scan_ss_gb300 import peaks
+    ex2 = peaks.measure("ex2")
+    ffma = peaks.measure("ffma2")
+    return {"ex2_per_clk_sm": ex2["per_clk_per_sm"], "fp32_per_clk_sm": ffma["per_clk_per_sm"],
+            "sms": ex2["sms"], "probe_mhz": ex2["sm_mhz"]}
+
+
+def traffic_record(kernel_sources: list[Path], workload_name: str):
+    """dram bytes per launch from the committed ncu summary, if it matches the source."""
+    import hashlib
+    h = hashlib.sha256()
+    for src in kernel_sources:
+        h.update(src.read_bytes())
+    digest = h.hexdigest()[:16]
+    for f in sorted((REPO / "profiles").glob("*.txt")):
+        kv = {}
+        for line in f.read_text().splitlines():
+            if ":" in line:
+                k, v = line.split(":", 1)
+                kv[k.strip()] = v.strip()
+        if kv.get("workload") == workload_name and kv.get("kernel_source_sha256_16") == digest:
+            try:
+                return float(kv["dram_bytes_per_step"]), f.name
+            except (KeyError, ValueError):
+                pass
+    return None, None
+
+
+# ---------------------------------------------------------------- oracle leg
+def oracle_rate(w, budget_s: float, inp_cpu=None) -> dict:
+    """Time the CPU oracle on a bounded sample of the workload (rows subset)."""
+    import oracle
+    from mamba_selective_scan_ss_gb300.inputs import make_inputs
+    orc = oracle.default()
+    inp = inp_cpu if inp_cpu is not None else make_inputs(w)
+    cores = os.cpu_count() or 1
+
+    def run(ch):
+        sub = {k: v for k, v in inp.items()}
+        sub["u"] = inp["u"][:, :ch].contiguous()
+        sub["delta"] = inp["delta"][:, :ch].contiguous()
+        sub["z"] = inp["z"][:, :ch].contiguous() if inp["z"] is not None else None
+        sub["A"] = inp["A"][:ch].contiguous()
+        sub["D"] = inp["D"][:ch].contiguous() if inp["D"] is not None else None
+        sub["delta_bias"] = inp["delta_bias"][:ch].contiguous() if inp["delta_bias"] is not None else None
+        t0 = time.perf_counter()
+        orc.fwd(sub["u"], sub["delta"], sub["A"], sub["B"], sub["C"], sub["D"], sub["z"],
+                sub["delta_bias"], sub["delta_softplus"], dtype=w.dtype, nthreads=cores)
+        return time.perf_counter() - t0
+
+    probe_ch = min(w.dim, max(1, cores))
+    t_probe = run(probe_ch)
+    per_ch = t_probe / probe_ch
+    ch = int(max(1, min(w.dim, budget_s / max(per_ch, 1e-9))))
+    # whole passes over the chosen channels until the budget is spent
+    reps, dt = 0, 0.0
+    while True:
+        dt += run(ch)
+        reps += 1
+        if dt >= budget_s or (reps >= 1 and dt * (reps + 1) / reps > 2.5 * budget_s):
+            break
+    upd = w.batch * ch * w.seqlen * w.dstate * reps
+    return {"value": upd / dt, "seconds": dt, "channels": ch, "reps": reps, "updates": upd,
+            "cores": cores}
+
+
+def run_reference(args, world, rank):
+    """Reference arm: the CPU oracle as it stands, on the host cores."""
+    from mamba_selective_scan_ss_gb300.inputs import WORKLOADS, make_inputs
+    if rank != 0:
+        return
+    w = WORKLOADS[args.workload]
+    inp = make_inputs(w)
+    import oracle
+    oracle.build()
+    per_step = max(0.2, min(20.0, args.reference_seconds / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        oracle_rate(w, per_step, inp)
+    rates = [oracle_rate(w, per_step, inp) for _ in range(args.steps)]
+    tot_upd = sum(r["updates"] for r in rates)
+    tot_s = sum(r["seconds"] for r in rates)
+    value = tot_upd / tot_s
+    cores = rates[0]["cores"]
+    sample = (f"{rates[0]['reps']} pass(es) over the first {rates[0]['channels']} of {w.dim} "
+              f"channels of every batch row, full seqlen {w.seqlen}, dstate {w.dstate} "
+              f"({rates[0]['updates']} updates) per step")
+    line = {
+        "metric": METRIC, "value": value, "unit": "state-updates/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * tot_s / max(1, len(rates)), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "impl": "reference",
+        "config": {"workload": w.name, "batch": w.batch, "dim": w.dim, "dstate": w.dstate,
+                   "seqlen": w.seqlen, "io_dtype": w.dtype},
+        "cpu_baseline": {"value": value, "unit": "state-updates/s", "cores": cores,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "state-updates/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- our arm
+def run_ours(args, world, rank, local):
+    import torch
+    import mamba_selective_scan_ss_gb300 as ss
+    from mamba_selective_scan_ss_gb300 import _build
+    from mamba_selective_scan_ss_gb300.inputs import WORKLOADS, make_inputs
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py: no CUDA device (the selective scan runs only on the GPU)")
+    if rank == 0:
+        _build.build_all()
+    barrier(world)
+    ss.load_library()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(dev)
+    w = WORKLOADS[args.workload]
+    inp = make_inputs(w)
+    nbytes = w.algorithmic_bytes()
+    nsets = 1 if nbytes >= 2 * L2_BYTES else int(math.ceil(2 * L2_BYTES / nbytes)) + 1
+    sets = []
+    for _ in range(nsets):
+        d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+        y = torch.empty_like(d["u"])
+        st = torch.empty((w.batch, w.dim, w.dstate), device=dev, dtype=torch.float32)
+        sets.append((d, y, st))
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    plan = ss.ss_selective_scan_plan(w.batch, w.dim, w.dstate, w.seqlen,
+                                     ss.SS_F32 if w.dtype == "f32" else ss.SS_BF16, True, sms)
+
+    def step(i):
+        d, y, st = sets[i % nsets]
+        ss.selective_scan_fwd(d["u"], d["delta"], d["A"], d["B"], d["C"], d["D"], d["z"],
+                              d["delta_bias"], d["delta_softplus"], y=y, last_state=st,
+                              stream=stream)
+
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            step(i)
+    torch.cuda.synchronize(dev)
+    status = ss.ss_selective_scan_check(stream.cuda_stream)
+    if status != ss.SS_OK:
+        raise SystemExit(f"device status after warm-up: {ss.ss_status_string(status)}")
+
+    rates = unit_rates() if rank == 0 else None
+    sampler = ClockSampler(gpu_id_for(dev.index))
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    sampler.start()
+    t_wall0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for i in range(args.steps):
+            step(i)
+        ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    t_wall = time.perf_counter() - t_wall0
+    clocks = sampler.stop()
+    barrier(world)
+    ms_total = ev0.elapsed_time(ev1)
+    status = ss.ss_selective_scan_check(stream.cuda_stream)
+    if status != ss.SS_OK:
+        raise SystemExit(f"device status after timing: {ss.ss_status_string(status)}")
+    ms_max = max_over_ranks(ms_total, world)
+    ms_step = ms_max / args.steps
+    total_updates = w.updates * args.steps * world
+    value = total_updates / (ms_max * 1e-3)
+
+    # e2e: pinned host inputs -> device, the call, outputs -> pinned host, every step
+    e2e = None
+    if args.e2e_steps > 0:
+        host = {k: (v.pin_memory() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+        d, y, st = sets[0]
+        y_host = torch.empty(y.shape, dtype=y.dtype).pin_memory()
+        st_host = torch.empty(st.shape, dtype=st.dtype).pin_memory()
+        h2d = sum(v.numel() * v.element_size() for v in host.values()
+                  if isinstance(v, torch.Tensor))
+        d2h = y_host.numel() * y_host.element_size() + st_host.numel() * st_host.element_size()
+
+        def e2e_step():
+            with torch.cuda.stream(stream):
+                for k, v in host.items():
+                    if isinstance(v, torch.Tensor):
+                        d[k].copy_(v, non_blocking=True)
+                ss.selective_scan_fwd(d["u"], d["delta"], d["A"], d["B"], d["C"], d["D"], d["z"],
+                                      d["delta_bias"], d["delta_softplus"], y=y, last_state=st,
+                                      stream=stream)
+                y_host.copy_(y, non_blocking=True)
+                st_host.copy_(st, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        e_ms = max_over_ranks(e0.elapsed_time(e1), world)
+        e2e = {"value": w.updates * args.e2e_steps * world / (e_ms * 1e-3),
+               "unit": "state-updates/s", "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(d2h), "ms_per_step": e_ms / args.e2e_steps}
+
+    if rank != 0:
+        return
+    # roofline of one step (all kernels of one call): slowest of HBM bytes, MUFU
+    # exps and FP32 lane-ops, at the SM clock sampled during the timed region
+    pk = measured_peaks()
+    mhz = clocks["sm_mhz"] or rates["probe_mhz"]
+    r_sfu = rates["ex2_per_clk_sm"] * rates["sms"] * mhz * 1e6         # ex2 / s
+    r_fp32 = rates["fp32_per_clk_sm"] * rates["sms"] * mhz * 1e6       # lane-ops / s
+    t_hbm = nbytes / (pk["hbm_gbs"] * 1e9)
+    t_sfu = w.updates / r_sfu
+    t_fp32 = 4 * w.updates / r_fp32
+    t_step = ms_step * 1e-3 / world * world  # per-rank step time
+    kernel_src = [REPO / "mamba_selective_scan_ss_gb300" / "csrc" / f
+                  for f in ("ss_fwd.cuh", "ss_device.cuh", "ss_api.cu")]
+    traffic, traffic_src = traffic_record(kernel_src, w.name)
+    if t_hbm >= max(t_sfu, t_fp32):
+        achieved = nbytes / t_step / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / pk["hbm_gbs"], "peak_source": pk["source"]}
+    else:
+        alu_peak = min(r_sfu, r_fp32 / 4)
+        achieved = w.updates / t_step
+        roof = {"bound": "alu", "achieved": achieved / 1e9, "peak": alu_peak / 1e9,
+                "unit": "Gupdate/s", "frac": achieved / alu_peak,
+                "peak_source": (f"microbenchmarks: {rates['ex2_per_clk_sm']:.1f} ex2 and "
+                                f"{rates['fp32_per_clk_sm']:.1f} fp32 lane-ops /clk/SM x "
+                                f"{rates['sms']} SMs x {mhz:.0f} MHz sampled")}
+    roof.update({"traffic": traffic, "traffic_source": traffic_src,
+                 "algorithmic_bytes_per_step": nbytes, "updates_per_step": w.updates,
+                 "t_hbm_us": t_hbm * 1e6, "t_sfu_us": t_sfu * 1e6, "t_fp32_us": t_fp32 * 1e6,
+                 "measured_step_us": t_step * 1e6,
+                 "scope": f"one ss_selective_scan_fwd call = {plan['kernel_launches']} kernel(s)"})
+
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        r = oracle_rate(w, args.cpu_baseline_seconds, inp)
+        cpu = {"value": r["value"], "unit": "state-updates/s", "cores": r["cores"],
+               "kind": "oracle",
+               "sample": (f"{r['reps']} pass(es) over the first {r['channels']} of {w.dim} "
+                          f"channels of every batch row, full seqlen {w.seqlen}, dstate "
+                          f"{w.dstate}: {r['updates']} updates in {r['seconds']:.1f} s")}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "state-updates/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": {"workload": w.name, "batch": w.batch, "dim": w.dim, "dstate": w.dstate,
+                   "seqlen": w.seqlen, "io_dtype": w.dtype, "z_gate": w.has_z,
+                   "l2": (f"{nsets} rotating input sets ({nsets * nbytes / 2**20:.0f} MiB > 2x L2)"
+                          if nsets > 1 else "inputs larger than 2x L2"),
+                   "nchunks": plan["nchunks"], "parallelism": f"replicas x{world}"},
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": int(plan["kernel_launches"] * args.steps),
+        "clocks": clocks,
+        "wall_s_timed_region": t_wall,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    world, rank, local = dist_setup(args)
+    try:
+        if args.impl == "reference":
+            run_reference(args, world, rank)
+        else:
+            run_ours(args, world, rank, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -114,6 +114,32 @@ SS_API const char* ss_status_string(ss_status_t status);
  */
 SS_API ss_status_t ss_selective_scan_check(void* stream);
 
+/*
+ * ss_selective_scan_plan -- describe, without any CUDA call, how
+ * ss_selective_scan_fwd would run a problem of these sizes on a device with
+ * `sm_count` SMs.  Long sequences are split into chunks that run in
+ * parallel and are joined by the prefix formulation of "Mamba CUDA 实现解析"
+ * eq (11)-(12); this reports that split so callers can size scratch and
+ * count launches.  `aligned16` states whether every u/delta/z/y/B/C pointer
+ * will be 16-byte aligned.  Returns SS_ERR_INVALID_ARGUMENT for sizes <= 0 or
+ * a NULL `plan`, SS_ERR_UNSUPPORTED as ss_selective_scan_fwd would; fills
+ * `plan` on SS_OK.  Reads the SS_NCHUNKS environment variable as
+ * ss_selective_scan_fwd does (a tuning aid that forces the chunk count).
+ */
+typedef struct {
+  int64_t nchunks;         /* sequence chunks */
+  int64_t chunk_len;       /* steps per chunk (the last one may be shorter) */
+  int64_t state_groups;    /* groups of at most 16 states */
+  int64_t ctas;            /* CTAs of the main kernel */
+  int64_t kernel_launches; /* kernels one call enqueues */
+  int64_t scratch_bytes;   /* stream-ordered scratch one call allocates */
+  int64_t vector_path;     /* 1: 16-byte vector path; 0: scalar path */
+} ss_plan_t;
+
+SS_API ss_status_t ss_selective_scan_plan(int64_t batch, int64_t dim, int64_t dstate,
+                                          int64_t seqlen, ss_dtype_t dtype, int aligned16,
+                                          int sm_count, ss_plan_t* plan);
+
 #ifdef __cplusplus
 }
 #endif

@@ -20,7 +20,7 @@ __all__ = [
     "SS_F32", "SS_BF16", "SS_OK", "SS_ERR_INVALID_ARGUMENT", "SS_ERR_UNSUPPORTED",
     "SS_ERR_CUDA", "SS_ERR_TIMEOUT", "SelectiveScanError", "library_path", "load_library",
     "ss_selective_scan_fwd", "ss_status_string", "ss_selective_scan_check",
-    "selective_scan_fwd",
+    "ss_selective_scan_plan", "selective_scan_fwd",
 ]
 
 SS_F32, SS_BF16 = 0, 1
@@ -58,8 +58,28 @@ def load_library():
         lib.ss_status_string.argtypes = [ctypes.c_int]
         lib.ss_selective_scan_check.restype = ctypes.c_int
         lib.ss_selective_scan_check.argtypes = [vp]
+        lib.ss_selective_scan_plan.restype = ctypes.c_int
+        lib.ss_selective_scan_plan.argtypes = [i64, i64, i64, i64, ctypes.c_int, ctypes.c_int,
+                                               ctypes.c_int, ctypes.POINTER(_Plan)]
         _LIB = lib
     return _LIB
+
+
+class _Plan(ctypes.Structure):
+    _fields_ = [(name, ctypes.c_int64) for name in
+                ("nchunks", "chunk_len", "state_groups", "ctas", "kernel_launches",
+                 "scratch_bytes", "vector_path")]
+
+
+def ss_selective_scan_plan(batch, dim, dstate, seqlen, dtype, aligned16, sm_count) -> dict:
+    """Launch plan of one call (host-only): chunks, launches, scratch bytes."""
+    plan = _Plan()
+    status = load_library().ss_selective_scan_plan(batch, dim, dstate, seqlen, int(dtype),
+                                                   int(bool(aligned16)), sm_count,
+                                                   ctypes.byref(plan))
+    if status != SS_OK:
+        raise SelectiveScanError(status, "ss_selective_scan_plan")
+    return {name: getattr(plan, name) for name, _ in _Plan._fields_}
 
 
 def ss_selective_scan_fwd(u, delta, A, B, C, D, z, delta_bias, delta_softplus, y, last_state,

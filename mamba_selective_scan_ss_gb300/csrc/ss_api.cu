@@ -20,6 +20,7 @@ namespace {
 constexpr int kThreads = 64;  // threads per CTA
 constexpr int kRows = 2;      // channel rows per thread
 constexpr int kMaxChunks = 1024;
+constexpr int kStages = 4;    // depth of the per-thread u/delta/z copy ring
 
 // Error word of the device-side waits (one per device context).
 __device__ unsigned int g_ss_device_error = 0;
@@ -33,6 +34,22 @@ bool range_overlap(const void* a, int64_t a_bytes, const void* b, int64_t b_byte
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 bool mul_ok(int64_t a, int64_t b, int64_t* out) { return !__builtin_mul_overflow(a, b, out); }
+
+struct Sizes {
+  int64_t rows, x_elems, x_bytes, bc_bytes, a_elems, st_elems;
+};
+
+// Byte sizes of the operands; false if any of them overflows int64 (the fp32
+// partial read-out of dstate > 16 is the largest: rows * seqlen * 4).
+bool sizes_ok(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, int64_t elt,
+              Sizes* s) {
+  int64_t tmp, bc_elems;
+  return mul_ok(batch, dim, &s->rows) && mul_ok(s->rows, seqlen, &s->x_elems) &&
+         mul_ok(s->x_elems, elt, &s->x_bytes) && mul_ok(batch, dstate, &tmp) &&
+         mul_ok(tmp, seqlen, &bc_elems) && mul_ok(bc_elems, elt, &s->bc_bytes) &&
+         mul_ok(dim, dstate, &s->a_elems) && mul_ok(s->rows, dstate, &s->st_elems) &&
+         mul_ok(s->x_elems, 4, &tmp) && mul_ok(s->rows, 256 * 1024 * 8, &tmp);
+}
 
 int sm_count() {
   int dev = 0, sms = 0;
@@ -49,6 +66,8 @@ struct LaunchPlan {
   int64_t base_ctas;   // batch * dim_tiles
   int nchunks;
   int64_t chunk_len;
+  int64_t agg_bytes, carry_bytes, part_bytes;  // scratch
+  int launches;
 };
 
 // Number of sequence chunks: enough CTAs to fill the GPU about four CTAs deep,
@@ -66,13 +85,50 @@ int choose_chunks(int64_t base_ctas, int64_t seqlen, int sms) {
   return (int)want;
 }
 
+// Launch plan shared by ss_selective_scan_fwd and ss_selective_scan_plan.
+bool make_plan(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, int64_t elt,
+               bool aligned16, int sms, LaunchPlan* plan) {
+  plan->nt = dstate <= 4 ? 4 : (dstate <= 8 ? 8 : 16);
+  plan->groups = (int)((dstate + plan->nt - 1) / plan->nt);
+  plan->vec = aligned16 && seqlen % (16 / elt) == 0;
+  // rows per CTA: the vector kernel splits the states of a row pair over two
+  // lanes when a group holds 8 or 16 states; the scalar kernel gives each
+  // thread two rows with all their states
+  const int64_t rows_per_cta = (plan->vec && plan->nt >= 8) ? kThreads : kThreads * kRows;
+  plan->dim_tiles = (dim + rows_per_cta - 1) / rows_per_cta;
+  if (plan->dim_tiles > INT_MAX / std::max<int64_t>(batch, 1)) return false;
+  plan->base_ctas = batch * plan->dim_tiles;
+  if (plan->base_ctas > INT_MAX) return false;
+  plan->nchunks = choose_chunks(plan->base_ctas, seqlen, sms);
+  const int64_t per = (seqlen + plan->nchunks - 1) / plan->nchunks;
+  plan->chunk_len = (per + ss::kTileSteps - 1) / ss::kTileSteps * ss::kTileSteps;
+  plan->nchunks = (int)((seqlen + plan->chunk_len - 1) / plan->chunk_len);
+  const int64_t rows = batch * dim;
+  const int64_t ns = (int64_t)plan->groups * plan->nt;
+  plan->agg_bytes = 0;
+  plan->carry_bytes = 0;
+  plan->part_bytes = 0;
+  if (plan->nchunks > 1) {
+    plan->agg_bytes = (int64_t)(plan->nchunks - 1) * rows * ns * 8;
+    plan->carry_bytes = (int64_t)plan->nchunks * rows * ns * 4;
+  }
+  if (plan->groups > 1) plan->part_bytes = rows * seqlen * 4;
+  plan->launches = plan->groups + (plan->nchunks > 1 ? 2 : 0);
+  return true;
+}
+
 template <typename T, int NT, bool VEC>
 cudaError_t enqueue(ss::FwdParams p, const LaunchPlan& plan, cudaStream_t st) {
+  constexpr int kTgs = NT >= 8 ? 2 : 1;  // lanes sharing a row pair
   const dim3 block(kThreads);
   if (plan.nchunks > 1) {
     const dim3 grid_agg((unsigned)plan.base_ctas, (unsigned)(plan.nchunks - 1),
                         (unsigned)plan.groups);
-    ss::ss_chunk_aggregate<T, NT, kRows, kThreads, VEC><<<grid_agg, block, 0, st>>>(p);
+    if constexpr (VEC) {
+      ss::ss_fwd_pipe<T, NT, kTgs, kThreads, kStages, true><<<grid_agg, block, 0, st>>>(p);
+    } else {
+      ss::ss_chunk_aggregate<T, NT, kRows, kThreads, false><<<grid_agg, block, 0, st>>>(p);
+    }
     const int64_t n = p.batch * p.dim * p.ns;
     const unsigned cblocks = (unsigned)((n + 255) / 256);
     ss::ss_chunk_carry<<<cblocks, 256, 0, st>>>(p);
@@ -82,7 +138,11 @@ cudaError_t enqueue(ss::FwdParams p, const LaunchPlan& plan, cudaStream_t st) {
     p.group = g;
     p.accum_in = g > 0;
     p.final_group = g == plan.groups - 1;
-    ss::ss_fwd_main<T, NT, kRows, kThreads, VEC><<<grid, block, 0, st>>>(p);
+    if constexpr (VEC) {
+      ss::ss_fwd_pipe<T, NT, kTgs, kThreads, kStages, false><<<grid, block, 0, st>>>(p);
+    } else {
+      ss::ss_fwd_main<T, NT, kRows, kThreads, false><<<grid, block, 0, st>>>(p);
+    }
   }
   return cudaGetLastError();
 }
@@ -123,13 +183,10 @@ SS_API ss_status_t ss_selective_scan_fwd(
   if (batch <= 0 || dim <= 0 || dstate <= 0 || seqlen <= 0) return SS_ERR_INVALID_ARGUMENT;
   if (dstate > 256) return SS_ERR_UNSUPPORTED;
   const int64_t elt = dtype == SS_F32 ? 4 : 2;
-  int64_t rows, x_elems, x_bytes, bc_elems, bc_bytes, a_elems, st_elems, tmp;
-  if (!mul_ok(batch, dim, &rows) || !mul_ok(rows, seqlen, &x_elems) ||
-      !mul_ok(x_elems, elt, &x_bytes) || !mul_ok(batch, dstate, &tmp) ||
-      !mul_ok(tmp, seqlen, &bc_elems) || !mul_ok(bc_elems, elt, &bc_bytes) ||
-      !mul_ok(dim, dstate, &a_elems) || !mul_ok(rows, dstate, &st_elems) ||
-      !mul_ok(x_elems, 4, &tmp) || x_bytes > INT64_MAX / 4)
-    return SS_ERR_UNSUPPORTED;
+  Sizes sz;
+  if (!sizes_ok(batch, dim, dstate, seqlen, elt, &sz)) return SS_ERR_UNSUPPORTED;
+  const int64_t x_bytes = sz.x_bytes, bc_bytes = sz.bc_bytes, a_elems = sz.a_elems,
+                st_elems = sz.st_elems;
   const uintptr_t ea = (uintptr_t)elt;
   if (!aligned(u, ea) || !aligned(delta, ea) || !aligned(B, ea) || !aligned(C, ea) ||
       !aligned(y, ea) || (z && !aligned(z, ea)) || !aligned(A, 4) || (D && !aligned(D, 4)) ||
@@ -150,19 +207,11 @@ SS_API ss_status_t ss_selective_scan_fwd(
   // ---- launch plan ----
   const int sms = sm_count();
   if (sms <= 0) return SS_ERR_CUDA;
+  const bool aligned16 = aligned(u, 16) && aligned(delta, 16) && aligned(B, 16) &&
+                         aligned(C, 16) && aligned(y, 16) && (!z || aligned(z, 16));
   LaunchPlan plan{};
-  plan.nt = dstate <= 4 ? 4 : (dstate <= 8 ? 8 : 16);
-  plan.groups = (int)((dstate + plan.nt - 1) / plan.nt);
-  const int64_t vlen = 16 / elt;
-  plan.vec = seqlen % vlen == 0 && aligned(u, 16) && aligned(delta, 16) && aligned(B, 16) &&
-             aligned(C, 16) && aligned(y, 16) && (!z || aligned(z, 16));
-  plan.dim_tiles = (dim + kThreads * kRows - 1) / (kThreads * kRows);
-  plan.base_ctas = batch * plan.dim_tiles;
-  if (plan.base_ctas > INT_MAX) return SS_ERR_UNSUPPORTED;
-  plan.nchunks = choose_chunks(plan.base_ctas, seqlen, sms);
-  const int64_t per = (seqlen + plan.nchunks - 1) / plan.nchunks;
-  plan.chunk_len = (per + ss::kTileSteps - 1) / ss::kTileSteps * ss::kTileSteps;
-  plan.nchunks = (int)((seqlen + plan.chunk_len - 1) / plan.chunk_len);
+  if (!make_plan(batch, dim, dstate, seqlen, elt, aligned16, sms, &plan))
+    return SS_ERR_UNSUPPORTED;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   ss::FwdParams p{};
@@ -175,21 +224,16 @@ SS_API ss_status_t ss_selective_scan_fwd(
   p.softplus = delta_softplus ? 1 : 0;
 
   // ---- stream-ordered scratch: chunk aggregates and carries, partial y ----
-  int64_t agg_bytes = 0, carry_bytes = 0, part_bytes = 0;
-  if (plan.nchunks > 1) {
-    agg_bytes = (int64_t)(plan.nchunks - 1) * rows * p.ns * (int64_t)sizeof(float2);
-    carry_bytes = (int64_t)plan.nchunks * rows * p.ns * (int64_t)sizeof(float);
-  }
-  if (plan.groups > 1) part_bytes = x_elems * 4;
-  const int64_t scratch_bytes = agg_bytes + carry_bytes + part_bytes;
+  const int64_t scratch_bytes = plan.agg_bytes + plan.carry_bytes + plan.part_bytes;
   void* scratch = nullptr;
   (void)cudaGetLastError();
   if (scratch_bytes > 0) {
     if (cudaMallocAsync(&scratch, (size_t)scratch_bytes, st) != cudaSuccess) return SS_ERR_CUDA;
     char* base = static_cast<char*>(scratch);
-    if (agg_bytes) p.agg = reinterpret_cast<float2*>(base);
-    if (carry_bytes) p.carry = reinterpret_cast<float*>(base + agg_bytes);
-    if (part_bytes) p.y_partial = reinterpret_cast<float*>(base + agg_bytes + carry_bytes);
+    if (plan.agg_bytes) p.agg = reinterpret_cast<float2*>(base);
+    if (plan.carry_bytes) p.carry = reinterpret_cast<float*>(base + plan.agg_bytes);
+    if (plan.part_bytes)
+      p.y_partial = reinterpret_cast<float*>(base + plan.agg_bytes + plan.carry_bytes);
   }
 
   const cudaError_t err = dtype == SS_F32 ? dispatch<float>(p, plan, st)
@@ -199,6 +243,29 @@ SS_API ss_status_t ss_selective_scan_fwd(
     if (err == cudaSuccess && ferr != cudaSuccess) return SS_ERR_CUDA;
   }
   return err == cudaSuccess ? SS_OK : SS_ERR_CUDA;
+}
+
+SS_API ss_status_t ss_selective_scan_plan(int64_t batch, int64_t dim, int64_t dstate,
+                                          int64_t seqlen, ss_dtype_t dtype, int aligned16,
+                                          int sm_count, ss_plan_t* out) {
+  if (dtype != SS_F32 && dtype != SS_BF16) return SS_ERR_UNSUPPORTED;
+  if (!out || batch <= 0 || dim <= 0 || dstate <= 0 || seqlen <= 0 || sm_count <= 0)
+    return SS_ERR_INVALID_ARGUMENT;
+  if (dstate > 256) return SS_ERR_UNSUPPORTED;
+  const int64_t elt = dtype == SS_F32 ? 4 : 2;
+  Sizes sz;
+  if (!sizes_ok(batch, dim, dstate, seqlen, elt, &sz)) return SS_ERR_UNSUPPORTED;
+  LaunchPlan plan{};
+  if (!make_plan(batch, dim, dstate, seqlen, elt, aligned16 != 0, sm_count, &plan))
+    return SS_ERR_UNSUPPORTED;
+  out->nchunks = plan.nchunks;
+  out->chunk_len = plan.chunk_len;
+  out->state_groups = plan.groups;
+  out->ctas = plan.base_ctas * plan.nchunks;
+  out->kernel_launches = plan.launches;
+  out->scratch_bytes = plan.agg_bytes + plan.carry_bytes + plan.part_bytes;
+  out->vector_path = plan.vec ? 1 : 0;
+  return SS_OK;
 }
 
 SS_API ss_status_t ss_selective_scan_check(void* stream) {

@@ -96,4 +96,17 @@ __device__ __forceinline__ void stg_vec(T* p, const Vec16<T>& v) {
   *reinterpret_cast<uint4*>(p) = *reinterpret_cast<const uint4*>(&v);
 }
 
+// ---- asynchronous global -> shared copies (per-thread, 16 bytes) -------------
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+  const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 }  // namespace ss

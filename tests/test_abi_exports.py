@@ -27,7 +27,7 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     assert declared_functions() == ["ss_selective_scan_check", "ss_selective_scan_fwd",
-                                    "ss_status_string"]
+                                    "ss_selective_scan_plan", "ss_status_string"]
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -78,3 +78,30 @@ def test_validation_rejects_bad_arguments(lib):
     assert call(u=u + 1) == ss.SS_ERR_INVALID_ARGUMENT       # misaligned fp32 pointer
     assert call(A=A + 2) == ss.SS_ERR_INVALID_ARGUMENT
     assert call(u=u + 1, dtype=ss.SS_BF16) == ss.SS_ERR_INVALID_ARGUMENT  # odd bf16 address
+
+
+def test_plan_is_host_only_and_consistent(lib, monkeypatch):
+    monkeypatch.delenv("SS_NCHUNKS", raising=False)
+    # a short sequence with many rows runs as one chunk, one launch, no scratch
+    p = ss.ss_selective_scan_plan(8, 5120, 16, 2048, ss.SS_BF16, True, 152)
+    assert p["nchunks"] >= 1 and p["state_groups"] == 1 and p["vector_path"] == 1
+    if p["nchunks"] == 1:
+        assert p["kernel_launches"] == 1 and p["scratch_bytes"] == 0
+    # few rows and a long sequence are split into chunks joined by carries
+    p = ss.ss_selective_scan_plan(1, 2048, 16, 65536, ss.SS_BF16, True, 152)
+    assert p["nchunks"] > 1 and p["kernel_launches"] == 3
+    assert p["chunk_len"] % 64 == 0 and (p["nchunks"] - 1) * p["chunk_len"] < 65536
+    assert p["scratch_bytes"] == (p["nchunks"] - 1) * 2048 * 16 * 8 + p["nchunks"] * 2048 * 16 * 4
+    # dstate above 16 runs in state groups, one main launch per group
+    p = ss.ss_selective_scan_plan(2, 64, 40, 256, ss.SS_F32, True, 152)
+    assert p["state_groups"] == 3
+    # misaligned pointers or odd lengths take the scalar path
+    assert ss.ss_selective_scan_plan(2, 64, 16, 250, ss.SS_BF16, True, 152)["vector_path"] == 0
+    assert ss.ss_selective_scan_plan(2, 64, 16, 256, ss.SS_BF16, False, 152)["vector_path"] == 0
+    # the tuning override forces the chunk count
+    monkeypatch.setenv("SS_NCHUNKS", "4")
+    assert ss.ss_selective_scan_plan(2, 64, 16, 1024, ss.SS_F32, True, 152)["nchunks"] == 4
+    with pytest.raises(ss.SelectiveScanError):
+        ss.ss_selective_scan_plan(0, 64, 16, 1024, ss.SS_F32, True, 152)
+    with pytest.raises(ss.SelectiveScanError):
+        ss.ss_selective_scan_plan(1, 64, 300, 1024, ss.SS_F32, True, 152)
