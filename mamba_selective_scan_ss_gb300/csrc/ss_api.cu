@@ -12,7 +12,7 @@
 #include <cstring>
 #include <algorithm>
 
-#include "ss_fwd.cuh"
+#include "ss_sched.cuh"
 #include "ss_selective_scan.h"
 
 namespace {
@@ -21,9 +21,7 @@ constexpr int kThreads = 64;  // threads per CTA
 constexpr int kRows = 2;      // channel rows per thread
 constexpr int kMaxChunks = 1024;
 constexpr int kStages = 4;    // depth of the per-thread u/delta/z copy ring
-
-// Error word of the device-side waits (one per device context).
-__device__ unsigned int g_ss_device_error = 0;
+constexpr int kCtasPerSm = 4; // resident CTAs per SM of the scheduled kernel
 
 bool range_overlap(const void* a, int64_t a_bytes, const void* b, int64_t b_bytes) {
   if (!a || !b || a_bytes <= 0 || b_bytes <= 0) return false;
@@ -60,99 +58,162 @@ int sm_count() {
 
 struct LaunchPlan {
   int nt;              // states per thread group (4, 8 or 16)
+  int tgs;             // vector path: lanes sharing a row pair
   int groups;          // state groups
-  bool vec;            // 16-byte vector path
+  bool vec;            // 16-byte vector path (scheduled kernel)
+  int64_t rows_per_cta;
   int64_t dim_tiles;
-  int64_t base_ctas;   // batch * dim_tiles
+  int64_t tiles;       // batch * dim_tiles
   int nchunks;
   int64_t chunk_len;
-  int64_t agg_bytes, carry_bytes, part_bytes;  // scratch
+  int64_t grid;        // CTAs of each main launch
+  bool chained;        // scheduled kernel: chained (true) or decoupled units
+  // scratch (bytes)
+  int64_t sched_bytes_per_group;  // ticket + unit flags (zeroed per call)
+  int64_t sched_bytes, unit_agg_bytes, unit_incl_bytes;     // vector path
+  int64_t agg_bytes, carry_bytes;                           // scalar path
+  int64_t part_bytes;                                       // dstate > 16
   int launches;
 };
 
-// Number of sequence chunks: enough CTAs to fill the GPU about four CTAs deep,
-// each chunk at least one B/C tile long.  SS_NCHUNKS overrides (tuning aid).
-int choose_chunks(int64_t base_ctas, int64_t seqlen, int sms) {
-  const int64_t max_by_len = std::max<int64_t>(1, seqlen / ss::kTileSteps);
-  int64_t want = 1;
-  if (const char* env = std::getenv("SS_NCHUNKS")) {
-    want = std::atoll(env);
-  } else {
-    const int64_t target = (int64_t)std::max(sms, 1) * 4;
-    want = (target + base_ctas - 1) / base_ctas;
-  }
-  want = std::max<int64_t>(1, std::min<int64_t>({want, max_by_len, kMaxChunks}));
-  return (int)want;
+int env_int(const char* name, int fallback) {
+  const char* v = std::getenv(name);
+  return v ? std::atoi(v) : fallback;
 }
 
+int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
+
 // Launch plan shared by ss_selective_scan_fwd and ss_selective_scan_plan.
+//
+// Vector path: one persistent kernel per state group with sms * ctas_per_sm
+// CTAs taking (row tile, chunk) units.  With at least as many row tiles as
+// CTAs, chunks are chained and cost nothing extra; they only give the
+// dynamic balance (about eight units per CTA).  With fewer row tiles than
+// CTAs the split over time is what provides the parallelism (about four
+// units per CTA), at the cost of an aggregate pass in each decoupled unit.
+// Scalar path: aggregate, carry and main kernels over a fixed chunk grid.
+// SS_NCHUNKS and SS_CTAS_PER_SM override the heuristics (tuning aids).
 bool make_plan(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, int64_t elt,
                bool aligned16, int sms, LaunchPlan* plan) {
   plan->nt = dstate <= 4 ? 4 : (dstate <= 8 ? 8 : 16);
   plan->groups = (int)((dstate + plan->nt - 1) / plan->nt);
   plan->vec = aligned16 && seqlen % (16 / elt) == 0;
-  // rows per CTA: the vector kernel splits the states of a row pair over two
-  // lanes when a group holds 8 or 16 states; the scalar kernel gives each
-  // thread two rows with all their states
-  const int64_t rows_per_cta = (plan->vec && plan->nt >= 8) ? kThreads : kThreads * kRows;
-  plan->dim_tiles = (dim + rows_per_cta - 1) / rows_per_cta;
+  // lanes sharing a row pair on the vector path: two for 8 or 16 states, one
+  // for 4 (SS_LANES_PER_PAIR=4 gives four lanes for 16 states: twice the
+  // resident warps for more shuffles and half-vector copies; a tuning aid)
+  plan->tgs = plan->nt >= 8 ? 2 : 1;
+  if (plan->nt == 16 && env_int("SS_LANES_PER_PAIR", 0) == 4) plan->tgs = 4;
+  plan->rows_per_cta = plan->vec ? 2 * kThreads / plan->tgs : kThreads * kRows;
+  plan->dim_tiles = (dim + plan->rows_per_cta - 1) / plan->rows_per_cta;
   if (plan->dim_tiles > INT_MAX / std::max<int64_t>(batch, 1)) return false;
-  plan->base_ctas = batch * plan->dim_tiles;
-  if (plan->base_ctas > INT_MAX) return false;
-  plan->nchunks = choose_chunks(plan->base_ctas, seqlen, sms);
-  const int64_t per = (seqlen + plan->nchunks - 1) / plan->nchunks;
-  plan->chunk_len = (per + ss::kTileSteps - 1) / ss::kTileSteps * ss::kTileSteps;
-  plan->nchunks = (int)((seqlen + plan->chunk_len - 1) / plan->chunk_len);
+  plan->tiles = batch * plan->dim_tiles;
   const int64_t rows = batch * dim;
   const int64_t ns = (int64_t)plan->groups * plan->nt;
-  plan->agg_bytes = 0;
-  plan->carry_bytes = 0;
-  plan->part_bytes = 0;
-  if (plan->nchunks > 1) {
-    plan->agg_bytes = (int64_t)(plan->nchunks - 1) * rows * ns * 8;
-    plan->carry_bytes = (int64_t)plan->nchunks * rows * ns * 4;
+  const int env_chunks = env_int("SS_NCHUNKS", 0);
+  plan->sched_bytes_per_group = plan->sched_bytes = plan->unit_agg_bytes = 0;
+  plan->unit_incl_bytes = plan->agg_bytes = plan->carry_bytes = plan->part_bytes = 0;
+  int64_t want;
+  if (plan->vec) {
+    const int64_t per_sm = std::max(1, env_int("SS_CTAS_PER_SM", kCtasPerSm));
+    const int64_t slots = (int64_t)std::max(sms, 1) * per_sm;
+    if (env_chunks > 0) {
+      want = env_chunks;
+    } else if (plan->tiles >= slots) {
+      want = std::min<int64_t>((8 * slots + plan->tiles - 1) / plan->tiles, seqlen / 256);
+    } else if (2 * plan->tiles >= slots) {
+      want = 1;  // one wave of whole rows costs less than decoupled chunks
+    } else {
+      want = std::min<int64_t>((4 * slots + plan->tiles - 1) / plan->tiles, seqlen / 128);
+    }
+    want = std::max<int64_t>(1, std::min<int64_t>({want, seqlen / ss::kTileSteps, kMaxChunks}));
+    plan->chunk_len = round_up((seqlen + want - 1) / want, ss::kTileSteps);
+    plan->nchunks = (int)((seqlen + plan->chunk_len - 1) / plan->chunk_len);
+    plan->grid = std::min<int64_t>(plan->tiles * plan->nchunks, slots);
+    plan->chained = plan->tiles >= plan->grid;
+    if (plan->grid > INT_MAX) return false;
+    plan->sched_bytes_per_group = round_up(128 + plan->nchunks * plan->tiles * 4, 256);
+    plan->sched_bytes = plan->sched_bytes_per_group * plan->groups;
+    const int64_t rec = (int64_t)plan->nchunks * plan->tiles * plan->rows_per_cta * plan->nt;
+    plan->unit_agg_bytes = round_up(rec * 8, 256);
+    plan->unit_incl_bytes = round_up(rec * 4, 256);
+    plan->launches = plan->groups;
+  } else {
+    if (env_chunks > 0) {
+      want = env_chunks;
+    } else {
+      const int64_t target = (int64_t)std::max(sms, 1) * 4;
+      want = (target + plan->tiles - 1) / plan->tiles;
+    }
+    want = std::max<int64_t>(1, std::min<int64_t>({want, std::max<int64_t>(1, seqlen / ss::kTileSteps),
+                                                   kMaxChunks}));
+    plan->chunk_len = round_up((seqlen + want - 1) / want, ss::kTileSteps);
+    plan->nchunks = (int)((seqlen + plan->chunk_len - 1) / plan->chunk_len);
+    plan->grid = plan->tiles * plan->nchunks;
+    if (plan->nchunks > 1) {
+      plan->agg_bytes = (int64_t)(plan->nchunks - 1) * rows * ns * 8;
+      plan->carry_bytes = (int64_t)plan->nchunks * rows * ns * 4;
+    }
+    plan->launches = plan->groups + (plan->nchunks > 1 ? 2 : 0);
   }
-  if (plan->groups > 1) plan->part_bytes = rows * seqlen * 4;
-  plan->launches = plan->groups + (plan->nchunks > 1 ? 2 : 0);
+  if (plan->groups > 1) plan->part_bytes = round_up(rows * seqlen * 4, 256);
   return true;
 }
 
-template <typename T, int NT, bool VEC>
-cudaError_t enqueue(ss::FwdParams p, const LaunchPlan& plan, cudaStream_t st) {
-  constexpr int kTgs = NT >= 8 ? 2 : 1;  // lanes sharing a row pair
-  const dim3 block(kThreads);
-  if (plan.nchunks > 1) {
-    const dim3 grid_agg((unsigned)plan.base_ctas, (unsigned)(plan.nchunks - 1),
-                        (unsigned)plan.groups);
-    if constexpr (VEC) {
-      ss::ss_fwd_pipe<T, NT, kTgs, kThreads, kStages, true><<<grid_agg, block, 0, st>>>(p);
-    } else {
-      ss::ss_chunk_aggregate<T, NT, kRows, kThreads, false><<<grid_agg, block, 0, st>>>(p);
-    }
-    const int64_t n = p.batch * p.dim * p.ns;
-    const unsigned cblocks = (unsigned)((n + 255) / 256);
-    ss::ss_chunk_carry<<<cblocks, 256, 0, st>>>(p);
-  }
-  const dim3 grid((unsigned)plan.base_ctas, (unsigned)plan.nchunks);
+int64_t scratch_bytes(const LaunchPlan& plan) {
+  return plan.sched_bytes + plan.unit_agg_bytes + plan.unit_incl_bytes + plan.agg_bytes +
+         plan.carry_bytes + plan.part_bytes;
+}
+
+template <typename T, int NT, int TGS>
+cudaError_t enqueue_vec(ss::FwdParams p, const LaunchPlan& plan, cudaStream_t st) {
+  auto kernel = ss::ss_fwd_sched<T, NT, TGS, kThreads, kStages>;
+  char* sched = reinterpret_cast<char*>(p.ticket);
   for (int g = 0; g < plan.groups; ++g) {
     p.group = g;
     p.accum_in = g > 0;
     p.final_group = g == plan.groups - 1;
-    if constexpr (VEC) {
-      ss::ss_fwd_pipe<T, NT, kTgs, kThreads, kStages, false><<<grid, block, 0, st>>>(p);
-    } else {
-      ss::ss_fwd_main<T, NT, kRows, kThreads, false><<<grid, block, 0, st>>>(p);
-    }
+    p.ticket = reinterpret_cast<unsigned*>(sched + g * plan.sched_bytes_per_group);
+    p.flags = p.ticket + 32;
+    kernel<<<(unsigned)plan.grid, kThreads, 0, st>>>(p);
+  }
+  return cudaGetLastError();
+}
+
+template <typename T, int NT>
+cudaError_t enqueue_scalar(ss::FwdParams p, const LaunchPlan& plan, cudaStream_t st) {
+  const dim3 block(kThreads);
+  if (plan.nchunks > 1) {
+    const dim3 grid_agg((unsigned)plan.tiles, (unsigned)(plan.nchunks - 1),
+                        (unsigned)plan.groups);
+    ss::ss_chunk_aggregate<T, NT, kRows, kThreads, false><<<grid_agg, block, 0, st>>>(p);
+    const int64_t n = p.batch * p.dim * p.ns;
+    ss::ss_chunk_carry<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(p);
+  }
+  const dim3 grid((unsigned)plan.tiles, (unsigned)plan.nchunks);
+  for (int g = 0; g < plan.groups; ++g) {
+    p.group = g;
+    p.accum_in = g > 0;
+    p.final_group = g == plan.groups - 1;
+    ss::ss_fwd_main<T, NT, kRows, kThreads, false><<<grid, block, 0, st>>>(p);
   }
   return cudaGetLastError();
 }
 
 template <typename T>
 cudaError_t dispatch(const ss::FwdParams& p, const LaunchPlan& plan, cudaStream_t st) {
+  if (plan.vec) {
+    switch (plan.nt) {
+      case 4: return enqueue_vec<T, 4, 1>(p, plan, st);
+      case 8: return enqueue_vec<T, 8, 2>(p, plan, st);
+      default:
+        return plan.tgs == 2 ? enqueue_vec<T, 16, 2>(p, plan, st)
+                             : enqueue_vec<T, 16, 4>(p, plan, st);
+    }
+  }
   switch (plan.nt) {
-    case 4: return plan.vec ? enqueue<T, 4, true>(p, plan, st) : enqueue<T, 4, false>(p, plan, st);
-    case 8: return plan.vec ? enqueue<T, 8, true>(p, plan, st) : enqueue<T, 8, false>(p, plan, st);
-    default: return plan.vec ? enqueue<T, 16, true>(p, plan, st) : enqueue<T, 16, false>(p, plan, st);
+    case 4: return enqueue_scalar<T, 4>(p, plan, st);
+    case 8: return enqueue_scalar<T, 8>(p, plan, st);
+    default: return enqueue_scalar<T, 16>(p, plan, st);
   }
 }
 
@@ -223,18 +284,37 @@ SS_API ss_status_t ss_selective_scan_fwd(
   p.ns = plan.groups * plan.nt;
   p.softplus = delta_softplus ? 1 : 0;
 
-  // ---- stream-ordered scratch: chunk aggregates and carries, partial y ----
-  const int64_t scratch_bytes = plan.agg_bytes + plan.carry_bytes + plan.part_bytes;
+  // ---- stream-ordered scratch: schedule, unit records or chunk carries, partial y ----
+  const int64_t total_scratch = scratch_bytes(plan);
   void* scratch = nullptr;
   (void)cudaGetLastError();
-  if (scratch_bytes > 0) {
-    if (cudaMallocAsync(&scratch, (size_t)scratch_bytes, st) != cudaSuccess) return SS_ERR_CUDA;
+  if (total_scratch > 0) {
+    if (cudaMallocAsync(&scratch, (size_t)total_scratch, st) != cudaSuccess) return SS_ERR_CUDA;
     char* base = static_cast<char*>(scratch);
-    if (plan.agg_bytes) p.agg = reinterpret_cast<float2*>(base);
-    if (plan.carry_bytes) p.carry = reinterpret_cast<float*>(base + plan.agg_bytes);
-    if (plan.part_bytes)
-      p.y_partial = reinterpret_cast<float*>(base + plan.agg_bytes + plan.carry_bytes);
+    if (plan.sched_bytes) {
+      if (cudaMemsetAsync(base, 0, (size_t)plan.sched_bytes, st) != cudaSuccess) {
+        cudaFreeAsync(scratch, st);
+        return SS_ERR_CUDA;
+      }
+      p.ticket = reinterpret_cast<unsigned*>(base);
+      base += plan.sched_bytes;
+    }
+    if (plan.unit_agg_bytes) {
+      p.unit_agg = reinterpret_cast<float2*>(base);
+      base += plan.unit_agg_bytes;
+      p.unit_incl = reinterpret_cast<float*>(base);
+      base += plan.unit_incl_bytes;
+    }
+    if (plan.agg_bytes) {
+      p.agg = reinterpret_cast<float2*>(base);
+      base += plan.agg_bytes;
+      p.carry = reinterpret_cast<float*>(base);
+      base += plan.carry_bytes;
+    }
+    if (plan.part_bytes) p.y_partial = reinterpret_cast<float*>(base);
   }
+  p.tiles = plan.tiles;
+  p.chained = plan.chained ? 1 : 0;
 
   const cudaError_t err = dtype == SS_F32 ? dispatch<float>(p, plan, st)
                                           : dispatch<__nv_bfloat16>(p, plan, st);
@@ -261,9 +341,9 @@ SS_API ss_status_t ss_selective_scan_plan(int64_t batch, int64_t dim, int64_t ds
   out->nchunks = plan.nchunks;
   out->chunk_len = plan.chunk_len;
   out->state_groups = plan.groups;
-  out->ctas = plan.base_ctas * plan.nchunks;
+  out->ctas = plan.grid;
   out->kernel_launches = plan.launches;
-  out->scratch_bytes = plan.agg_bytes + plan.carry_bytes + plan.part_bytes;
+  out->scratch_bytes = scratch_bytes(plan);
   out->vector_path = plan.vec ? 1 : 0;
   return SS_OK;
 }
@@ -272,11 +352,11 @@ SS_API ss_status_t ss_selective_scan_check(void* stream) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (cudaStreamSynchronize(st) != cudaSuccess) return SS_ERR_CUDA;
   unsigned int word = 0;
-  if (cudaMemcpyFromSymbol(&word, g_ss_device_error, sizeof(word)) != cudaSuccess)
+  if (cudaMemcpyFromSymbol(&word, ss::g_ss_device_error, sizeof(word)) != cudaSuccess)
     return SS_ERR_CUDA;
   if (word != 0) {
     const unsigned int zero = 0;
-    if (cudaMemcpyToSymbol(g_ss_device_error, &zero, sizeof(zero)) != cudaSuccess)
+    if (cudaMemcpyToSymbol(ss::g_ss_device_error, &zero, sizeof(zero)) != cudaSuccess)
       return SS_ERR_CUDA;
     return SS_ERR_TIMEOUT;
   }

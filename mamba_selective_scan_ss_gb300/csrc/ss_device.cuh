@@ -46,7 +46,64 @@ __device__ __forceinline__ f2 ex2x2(f2 x) {
   return pack(ex2(lo), ex2(hi));
 }
 
-// ---- step size and gate -------------------------------------------------------
+__device__ __forceinline__ f2 add2(f2 a, f2 b) {
+  f2 r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r.v) : "l"(a.v), "l"(b.v));
+  return r;
+}
+__device__ __forceinline__ f2 splat(float x) { return pack(x, x); }
+__device__ __forceinline__ float lo_of(f2 p) {
+  float lo, hi;
+  unpack(p, lo, hi);
+  return lo;
+}
+__device__ __forceinline__ float hi_of(f2 p) {
+  float lo, hi;
+  unpack(p, lo, hi);
+  return hi;
+}
+__device__ __forceinline__ float rcp_approx(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// ---- step size and gate, two steps at a time ------------------------------------
+// log1p(e) for e in [0, 1] as e * g(e), g a degree-8 polynomial fitted here by
+// least squares on Chebyshev nodes of [0, 1] to log1p(e)/e (max relative error
+// of the fp32 evaluation 1.9e-7 over (0, 1], tiny e included).
+__device__ __forceinline__ f2 log1p_unit2(f2 e) {
+  f2 g = splat(0.005253458f);
+  g = fma2(g, e, splat(-0.029588507f));
+  g = fma2(g, e, splat(0.07836167f));
+  g = fma2(g, e, splat(-0.1367477f));
+  g = fma2(g, e, splat(0.1911143f));
+  g = fma2(g, e, splat(-0.2484437f));
+  g = fma2(g, e, splat(0.3331927f));
+  g = fma2(g, e, splat(-0.49999502f));
+  g = fma2(g, e, splat(1.0f));
+  return mul2(e, g);
+}
+
+// softplus(x) = max(x, 0) + log1p(e^-|x|) on a pair of steps; e^-|x| is in
+// (0, 1], so nothing overflows and small results keep their relative precision.
+__device__ __forceinline__ f2 softplus2(f2 x) {
+  float x0, x1;
+  unpack(x, x0, x1);
+  const f2 e = pack(ex2(-fabsf(x0) * kLog2e), ex2(-fabsf(x1) * kLog2e));
+  return add2(pack(fmaxf(x0, 0.f), fmaxf(x1, 0.f)), log1p_unit2(e));
+}
+
+// silu(z) = z / (1 + e^-z) on a pair of steps
+__device__ __forceinline__ f2 silu2(f2 z) {
+  const f2 e = ex2x2(mul2(z, splat(-kLog2e)));
+  const f2 d = add2(e, splat(1.f));
+  float d0, d1;
+  unpack(d, d0, d1);
+  return mul2(z, pack(rcp_approx(d0), rcp_approx(d1)));
+}
+
+// ---- step size and gate (scalar path) -------------------------------------------
 // softplus(x) = log(1 + e^x) = max(x, 0) + log1p(e^-|x|); e^-|x| is in (0, 1],
 // so neither term overflows and small results keep full relative precision.
 __device__ __forceinline__ float softplus(float x) {
@@ -76,6 +133,78 @@ struct Elem<__nv_bfloat16> {
   __device__ __forceinline__ static float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
   __device__ __forceinline__ static __nv_bfloat16 from_f32(float x) { return __float2bfloat16_rn(x); }
 };
+
+// NP fp32 pairs (consecutive steps) from 32-bit words of packed elements:
+// two words per pair for float, one word (a bf16x2) per pair for bf16.
+template <typename T, int NP>
+__device__ __forceinline__ void words_to_pairs(const unsigned* w, f2 (&out)[NP]) {
+#pragma unroll
+  for (int i = 0; i < NP; ++i) {
+    if constexpr (sizeof(T) == 4) {
+      out[i] = pack(__uint_as_float(w[2 * i]), __uint_as_float(w[2 * i + 1]));
+    } else {  // low half is the earlier step
+      out[i] = pack(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u));
+    }
+  }
+}
+// ... and back (bf16: round to nearest even); writes NP * 2 * sizeof(T) bytes
+template <typename T, int NP>
+__device__ __forceinline__ void pairs_to_words(const f2 (&in)[NP], unsigned* w) {
+#pragma unroll
+  for (int i = 0; i < NP; ++i) {
+    float lo, hi;
+    unpack(in[i], lo, hi);
+    if constexpr (sizeof(T) == 4) {
+      w[2 * i] = __float_as_uint(lo);
+      w[2 * i + 1] = __float_as_uint(hi);
+    } else {
+      asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(w[i]) : "f"(hi), "f"(lo));
+    }
+  }
+}
+
+__device__ __forceinline__ void cp_async8(void* smem, const void* gmem) {
+  const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(s), "l"(gmem) : "memory");
+}
+
+// A 16-byte vector of V elements as V/2 fp32 pairs (consecutive steps).
+template <typename T>
+__device__ __forceinline__ void to_pairs(const uint4& raw, f2 (&out)[Elem<T>::kVec / 2]);
+template <>
+__device__ __forceinline__ void to_pairs<float>(const uint4& raw, f2 (&out)[2]) {
+  out[0] = pack(__uint_as_float(raw.x), __uint_as_float(raw.y));
+  out[1] = pack(__uint_as_float(raw.z), __uint_as_float(raw.w));
+}
+template <>
+__device__ __forceinline__ void to_pairs<__nv_bfloat16>(const uint4& raw, f2 (&out)[4]) {
+  const unsigned w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i)  // low half is the earlier step
+    out[i] = pack(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u));
+}
+// ... and back (bf16: round to nearest even)
+template <typename T>
+__device__ __forceinline__ uint4 from_pairs(const f2 (&in)[Elem<T>::kVec / 2]);
+template <>
+__device__ __forceinline__ uint4 from_pairs<float>(const f2 (&in)[2]) {
+  float a, b, c, d;
+  unpack(in[0], a, b);
+  unpack(in[1], c, d);
+  return make_uint4(__float_as_uint(a), __float_as_uint(b), __float_as_uint(c),
+                    __float_as_uint(d));
+}
+template <>
+__device__ __forceinline__ uint4 from_pairs<__nv_bfloat16>(const f2 (&in)[4]) {
+  unsigned w[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float lo, hi;
+    unpack(in[i], lo, hi);
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(w[i]) : "f"(hi), "f"(lo));
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
 
 // 16-byte vector of V elements, loaded/stored whole.
 template <typename T>

@@ -1,0 +1,616 @@
+// Vector path of the selective-scan forward: one persistent kernel per call
+// that hands out (row tile, sequence chunk) units in order and joins the
+// chunks of a row tile with the associative operator of "Mamba CUDA 实现解析"
+// eq (10): (P1, v1) (+) (P2, e2) = (P2*P1, P2*v1 + e2), where a chunk's
+// aggregate is P = prod of its decays a = exp(dt*A) and e = the state it
+// reaches from zero.  The state entering chunk k is the prefix
+// s_0 (+) E_1 (+) ... (+) E_{k-1} of eq (11)-(12).
+//
+// Scheduling.  CTAs take tickets from a global counter; ticket t is unit
+// (chunk k = t / tiles, tile i = t % tiles), so every unit's predecessor
+// (k-1, i) was handed out earlier to a CTA that is running or done, and
+// every wait below ends.  The mode of a launch is fixed by the host:
+//  * chained (at least as many row tiles as CTAs): a unit waits for the
+//    state its predecessor reached, runs its single pass from it and
+//    publishes its own end state; the predecessor was handed out a full
+//    round of tickets earlier, so the wait is normally over at once and no
+//    work is repeated.
+//  * decoupled (fewer row tiles than CTAs): every unit after the first of
+//    its tile computes its own aggregate (a pass without C, z or y) and
+//    publishes it, then looks back to the nearest predecessor whose end
+//    state is published and folds the aggregates in between forward, in
+//    chunk order; that gives its carry, it publishes its own end state
+//    P*carry + e at once and runs the main pass from the carry.
+// Both modes evaluate every carry by the same sequence of operations whatever
+// the timing, so results are bitwise reproducible from run to run.
+// Every wait polls with back-off and gives up after kSpinLimit polls: it then
+// sets the device error word (ss_selective_scan_check reports SS_ERR_TIMEOUT),
+// uses a zero carry and carries on, so no call can hang the device.
+//
+// Thread layout inside a unit: groups of TGS adjacent lanes share two channel
+// rows; lane q of a group holds states [q*G, (q+1)*G) (G = NT / TGS) of both
+// rows, so every B/C value it loads serves two rows.  Row work (streaming
+// u/delta/z, dt and du, the skip/gate epilogue) is split between the lanes of
+// a group: with TGS = 1 the lane does both rows; with TGS = 2 lane q does row
+// q; with TGS = 4 lane q does row q % 2 for half of each vector's steps (half
+// q / 2).  The lanes of a group gather dt and du and reduce the partial
+// read-outs by shuffle.  More lanes per row pair means more resident warps,
+// which hides the MUFU/FMA dependency latency of the recurrence.
+//
+// Memory latency is taken off the critical path by asynchronous copies: u,
+// delta (and z) of a lane's own rows stream through a STAGES-deep ring of
+// per-lane shared-memory slots filled with cp.async (a lane only reads the
+// slots it filled, so the ring needs no barrier); B (and C) tiles of
+// kTileSteps steps are copied raw one tile ahead and widened/transposed to
+// [t][n] fp32 at the tile boundary (two barriers per tile).
+#pragma once
+
+#include <type_traits>
+
+#include "ss_fwd.cuh"
+
+namespace ss {
+
+// Error word of the device-side waits (one per device context).
+__device__ unsigned int g_ss_device_error = 0;
+
+constexpr unsigned kUnitAgg = 1u;             // unit aggregate published
+constexpr unsigned kUnitIncl = 2u;            // state at the unit's end published
+constexpr long long kSpinLimit = 1LL << 20;   // polls before a wait gives up (~0.3 s)
+constexpr unsigned kErrTimeout = 1u;
+
+__device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release(unsigned* p, unsigned v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Thread 0 waits until *flag >= want (bounded); returns the flag value seen,
+// or 0 after giving up (the device error word is then set).
+__device__ __forceinline__ unsigned wait_flag(const unsigned* flag, unsigned want) {
+  unsigned v = ld_acquire(flag);
+  long long polls = 0;
+  while (v < want) {
+    if (++polls > kSpinLimit) {
+      atomicOr(&g_ss_device_error, kErrTimeout);
+      return 0u;
+    }
+    __nanosleep(polls < 64 ? 32 : 256);
+    v = ld_acquire(flag);
+  }
+  return v;
+}
+
+template <int TGS, int TPB>
+struct PairRows {
+  static constexpr int kRowsPerCta = 2 * TPB / TGS;
+  int64_t row[2];  // slot 0: own row; slot 1: the other row of the group
+  int64_t d[2];
+  int rc[2];       // row index inside the tile
+  bool valid[2];
+  int64_t b;
+  int q;           // lane in group
+
+  __device__ __forceinline__ PairRows(int64_t tile, int64_t dim) {
+    const int64_t dtiles = (dim + kRowsPerCta - 1) / kRowsPerCta;
+    b = tile / dtiles;
+    const int64_t base = (tile - b * dtiles) * kRowsPerCta;
+    const int g = threadIdx.x / TGS;
+    q = threadIdx.x % TGS;
+#pragma unroll
+    for (int s = 0; s < 2; ++s) {
+      const int which = TGS == 1 ? s : (s == 0 ? (q & 1) : 1 - (q & 1));
+      rc[s] = which * (TPB / TGS) + g;
+      const int64_t dd = base + rc[s];
+      valid[s] = dd < dim;
+      d[s] = valid[s] ? dd : dim - 1;
+      row[s] = b * dim + d[s];
+    }
+  }
+};
+
+template <typename T, int NT, int TGS, int TPB, int STAGES>
+struct PipeSmem {
+  static constexpr int kOwn = TGS == 1 ? 2 : 1;
+  static constexpr int kRaw = kTileSteps + 16 / (int)sizeof(T);  // padded raw row
+  // u, delta, z ring: a lane's own rows, a whole 16-byte vector each, or half
+  // of one when four lanes share a row pair
+  using Slot = typename std::conditional<TGS == 4, uint2, uint4>::type;
+  Slot x[STAGES][3][kOwn][TPB];
+  T raw[2][NT][kRaw];                 // raw B, C tile
+  float m[2][kTileSteps][NT];         // widened, transposed B, C tile
+};
+
+// One pass over steps [t_begin, t_end) of a unit: AGG = false runs the
+// recurrence from h and writes y; AGG = true runs it from h (zero) without C,
+// z or y and accumulates sum dt of the lane's own steps (for the aggregate's
+// decay).
+template <typename T, int NT, int TGS, int TPB, int STAGES, bool AGG>
+__device__ __forceinline__ void scan_pass(const FwdParams& p,
+                                          PipeSmem<T, NT, TGS, TPB, STAGES>& sm,
+                                          const PairRows<TGS, TPB>& rs, int64_t t_begin,
+                                          int64_t t_end, f2 (&h)[2][NT / TGS / 2],
+                                          const f2 (&A2)[2][NT / TGS / 2],
+                                          const float (&bias)[TGS == 1 ? 2 : 1],
+                                          const float (&Dd)[TGS == 1 ? 2 : 1],
+                                          float (&dt_sum)[TGS == 1 ? 2 : 1]) {
+  constexpr int V = Elem<T>::kVec;
+  constexpr bool HALF = TGS == 4;      // a lane does half of its row's steps
+  constexpr int VO = HALF ? V / 2 : V; // own steps per vector
+  constexpr int VOP = VO / 2;          // own step pairs
+  constexpr int G = NT / TGS;          // states per lane
+  constexpr int GP = G / 2;            // state pairs per lane
+  constexpr int OWN = TGS == 1 ? 2 : 1;  // own rows (row work) per lane
+  constexpr int NM = AGG ? 1 : 2;      // staged state tensors: B (, C)
+  constexpr int VPT = kTileSteps / V;  // vectors per tile
+  constexpr int CPR = kTileSteps * (int)sizeof(T) / 16;  // 16-byte chunks per state row
+  constexpr int EPC = 16 / (int)sizeof(T);                // elements per 16-byte chunk
+  constexpr int WPO = VO * (int)sizeof(T) / 4;            // 32-bit words of own steps
+  static_assert(STAGES >= 2 && STAGES <= VPT, "pipeline depth must fit in a tile");
+
+  const int tid = threadIdx.x;
+  const int64_t L = p.seqlen, N = p.dstate;
+  const int ng0 = p.group * NT;  // first state of this launch's group
+  const int nl0 = rs.q * G;      // first state of this lane within the group
+  const int hv = HALF ? (rs.q >> 1) : 0;  // which half of the vector this lane owns
+  const int gbase = (threadIdx.x & 31) & ~(TGS - 1);  // first lane of the group
+  const int64_t nvec = (t_end - t_begin) / V;
+  const T* __restrict__ ug = static_cast<const T*>(p.u);
+  const T* __restrict__ dg = static_cast<const T*>(p.delta);
+  const T* __restrict__ zg = AGG ? nullptr : static_cast<const T*>(p.z);
+  const T* __restrict__ Bg = static_cast<const T*>(p.B);
+  const T* __restrict__ Cg = static_cast<const T*>(p.C);
+  T* __restrict__ y = static_cast<T*>(p.y);
+
+  auto copy_own = [&](void* dst, const T* src) {
+    if constexpr (HALF) {
+      cp_async8(dst, src);
+    } else {
+      cp_async16(dst, src);
+    }
+  };
+  auto issue_vec = [&](int64_t j) {
+    if (j < nvec) {
+      const int slot = (int)(j % STAGES);
+      const int64_t t = t_begin + j * V + hv * VO;
+#pragma unroll
+      for (int o = 0; o < OWN; ++o) {
+        const int64_t off = rs.row[o] * L + t;
+        copy_own(&sm.x[slot][0][o][tid], ug + off);
+        copy_own(&sm.x[slot][1][o][tid], dg + off);
+        if (!AGG && zg) copy_own(&sm.x[slot][2][o][tid], zg + off);
+      }
+    }
+    cp_async_commit();
+  };
+  auto issue_tile = [&](int64_t t0) {
+    if (t0 >= t_end) return;
+    const int tlen = (int)min((int64_t)kTileSteps, t_end - t0);
+    for (int i = tid; i < NM * NT * CPR; i += TPB) {
+      const int m = i / (NT * CPR);
+      const int rem = i - m * NT * CPR;
+      const int n = rem / CPR;
+      const int j = (rem - n * CPR) * EPC;
+      const int64_t ng = ng0 + n;
+      if (ng < N && j < tlen)
+        cp_async16(&sm.raw[m][n][j], (m == 0 ? Bg : Cg) + (rs.b * N + ng) * L + t0 + j);
+    }
+  };
+
+  issue_tile(t_begin);
+#pragma unroll
+  for (int s = 0; s < STAGES - 1; ++s) issue_vec(s);
+
+  for (int64_t j = 0; j < nvec; ++j) {
+    issue_vec(j + STAGES - 1);
+    cp_async_wait<STAGES - 1>();  // this lane's copies of vector j (and older) landed
+    const int jt = (int)(j % VPT) * V;
+    if (jt == 0) {
+      // tile boundary: widen + transpose the raw tile, then prefetch the next one
+      const int64_t t0 = t_begin + j * V;
+      const int tlen = (int)min((int64_t)kTileSteps, t_end - t0);
+      __syncthreads();  // every lane's raw copies landed; the previous tile is consumed
+      for (int i = tid; i < NM * NT * CPR; i += TPB) {
+        const int n = i % NT;  // state fastest: conflict-free transposed stores
+        const int c = (i / NT) % CPR;
+        const int m = i / (NT * CPR);
+        const Vec16<T> v = *reinterpret_cast<const Vec16<T>*>(&sm.raw[m][n][c * EPC]);
+        const bool nok = ng0 + n < N;
+#pragma unroll
+        for (int e = 0; e < EPC; ++e) {
+          const int t = c * EPC + e;
+          sm.m[m][t][n] = (nok && t < tlen) ? Elem<T>::to_f32(v.e[e]) : 0.f;
+        }
+      }
+      __syncthreads();
+      issue_tile(t0 + kTileSteps);
+    }
+
+    const int slot = (int)(j % STAGES);
+    // row work of the own steps, two at a time: dt = softplus(delta + bias), du = dt*u
+    f2 dtp[OWN][VOP], dup[OWN][VOP], up[OWN][VOP];
+#pragma unroll
+    for (int o = 0; o < OWN; ++o) {
+      f2 dp[VOP];
+      words_to_pairs<T, VOP>(reinterpret_cast<const unsigned*>(&sm.x[slot][0][o][tid]), up[o]);
+      words_to_pairs<T, VOP>(reinterpret_cast<const unsigned*>(&sm.x[slot][1][o][tid]), dp);
+#pragma unroll
+      for (int m = 0; m < VOP; ++m) {
+        const f2 x = add2(dp[m], splat(bias[o]));
+        dtp[o][m] = p.softplus ? softplus2(x) : x;
+        dup[o][m] = mul2(dtp[o][m], up[o][m]);
+        if (AGG) dt_sum[o] += lo_of(dtp[o][m]) + hi_of(dtp[o][m]);
+      }
+    }
+    // dt and du of both rows of the group for all V steps, gathered before the
+    // recurrence so the shuffles stay off its dependency chain
+    float dts[2][V], dus[2][V];
+    {
+      float odt[OWN][VO], odu[OWN][VO];
+#pragma unroll
+      for (int o = 0; o < OWN; ++o)
+#pragma unroll
+        for (int m = 0; m < VOP; ++m) {
+          unpack(dtp[o][m], odt[o][2 * m], odt[o][2 * m + 1]);
+          unpack(dup[o][m], odu[o][2 * m], odu[o][2 * m + 1]);
+        }
+      if constexpr (TGS == 1) {
+#pragma unroll
+        for (int r = 0; r < 2; ++r)
+#pragma unroll
+          for (int e = 0; e < V; ++e) {
+            dts[r][e] = odt[r][e];
+            dus[r][e] = odu[r][e];
+          }
+      } else if constexpr (TGS == 2) {
+#pragma unroll
+        for (int e = 0; e < V; ++e) {
+          dts[0][e] = odt[0][e];
+          dus[0][e] = odu[0][e];
+          dts[1][e] = __shfl_xor_sync(0xffffffffu, odt[0][e], 1);
+          dus[1][e] = __shfl_xor_sync(0xffffffffu, odu[0][e], 1);
+        }
+      } else {
+        // block (row slot r, half hh) lives on lane ((q&1) ^ r) + 2*hh of the group
+#pragma unroll
+        for (int r = 0; r < 2; ++r)
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const int src = gbase + (((rs.q & 1) ^ r) + 2 * hh);
+#pragma unroll
+            for (int e = 0; e < VO; ++e) {
+              dts[r][hh * VO + e] = __shfl_sync(0xffffffffu, odt[0][e], src);
+              dus[r][hh * VO + e] = __shfl_sync(0xffffffffu, odu[0][e], src);
+            }
+          }
+      }
+    }
+
+    float part[2][V];  // read-out over this lane's states, per row slot and step
+#pragma unroll
+    for (int s = 0; s < V; ++s) {
+      const int t = jt + s;
+      f2 dt2[2], du2[2], yacc[2][2];
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        dt2[r] = splat(dts[r][s]);
+        du2[r] = splat(dus[r][s]);
+        yacc[r][0] = yacc[r][1] = splat(0.f);
+      }
+#pragma unroll
+      for (int k4 = 0; k4 < G / 4; ++k4) {
+        const ulonglong2 bq = *reinterpret_cast<const ulonglong2*>(&sm.m[0][t][nl0 + 4 * k4]);
+        const f2 bp[2] = {{bq.x}, {bq.y}};
+        f2 cp[2];
+        if (!AGG) {
+          const ulonglong2 cq =
+              *reinterpret_cast<const ulonglong2*>(&sm.m[NM - 1][t][nl0 + 4 * k4]);
+          cp[0].v = cq.x;
+          cp[1].v = cq.y;
+        }
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int k = 2 * k4 + e;
+#pragma unroll
+          for (int r = 0; r < 2; ++r) {
+            const f2 a = ex2x2(mul2(dt2[r], A2[r][k]));
+            h[r][k] = fma2(a, h[r][k], mul2(du2[r], bp[e]));
+            if (!AGG) yacc[r][e] = fma2(cp[e], h[r][k], yacc[r][e]);
+          }
+        }
+      }
+      if (!AGG) {
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          const f2 ys = add2(yacc[r][0], yacc[r][1]);
+          part[r][s] = lo_of(ys) + hi_of(ys);
+        }
+      }
+    }
+
+    if constexpr (!AGG) {
+      // read-out of the own steps: this lane's partials plus the group's
+      float yv[OWN][VO];
+      if constexpr (TGS == 1) {
+#pragma unroll
+        for (int s = 0; s < V; ++s) {
+          yv[0][s] = part[0][s];
+          yv[1][s] = part[1][s];
+        }
+      } else if constexpr (TGS == 2) {
+#pragma unroll
+        for (int s = 0; s < V; ++s)
+          yv[0][s] = part[0][s] + __shfl_xor_sync(0xffffffffu, part[1][s], 1);
+      } else {
+        float yfull[V];
+#pragma unroll
+        for (int s = 0; s < V; ++s) {
+          const float w = part[0][s] + __shfl_xor_sync(0xffffffffu, part[1][s], 1);
+          yfull[s] = w + __shfl_xor_sync(0xffffffffu, w, 2);
+        }
+#pragma unroll
+        for (int e = 0; e < VO; ++e) yv[0][e] = hv ? yfull[VO + e] : yfull[e];
+      }
+      // epilogue of the own steps: earlier groups' read-out, skip, gate, store
+#pragma unroll
+      for (int o = 0; o < OWN; ++o) {
+        const int64_t off = rs.row[o] * L + t_begin + j * V + hv * VO;
+        if (p.accum_in) {
+#pragma unroll
+          for (int e = 0; e < VO; ++e) yv[o][e] += p.y_partial[off + e];
+        }
+        if (!p.final_group) {
+          if (rs.valid[o]) {
+#pragma unroll
+            for (int e = 0; e < VO; ++e) p.y_partial[off + e] = yv[o][e];
+          }
+          continue;
+        }
+        f2 yp[VOP];
+#pragma unroll
+        for (int m = 0; m < VOP; ++m)
+          yp[m] = fma2(splat(Dd[o]), up[o][m], pack(yv[o][2 * m], yv[o][2 * m + 1]));
+        if (zg) {
+          f2 zp[VOP];
+          words_to_pairs<T, VOP>(reinterpret_cast<const unsigned*>(&sm.x[slot][2][o][tid]), zp);
+#pragma unroll
+          for (int m = 0; m < VOP; ++m) yp[m] = mul2(yp[m], silu2(zp[m]));
+        }
+        if (rs.valid[o]) {
+          unsigned w[WPO];
+          pairs_to_words<T, VOP>(yp, w);
+          if constexpr (WPO == 4) {
+            *reinterpret_cast<uint4*>(y + off) = make_uint4(w[0], w[1], w[2], w[3]);
+          } else {
+            *reinterpret_cast<uint2*>(y + off) = make_uint2(w[0], w[1]);
+          }
+        }
+      }
+    }
+  }
+  cp_async_wait<0>();
+}
+
+// The persistent, ticketed kernel.  grid = resident CTAs (at most the unit
+// count), block = TPB; one launch per state group of NT states.
+template <typename T, int NT, int TGS, int TPB, int STAGES>
+__global__ void __launch_bounds__(TPB) ss_fwd_sched(const FwdParams p) {
+  constexpr int G = NT / TGS;
+  constexpr int GP = G / 2;
+  constexpr int OWN = TGS == 1 ? 2 : 1;
+  constexpr int RPC = PairRows<TGS, TPB>::kRowsPerCta;
+  static_assert(TGS == 1 || TGS == 2 || TGS == 4, "one, two or four lanes per row pair");
+  static_assert(G % 4 == 0, "a lane holds a multiple of four states");
+  __shared__ __align__(16) PipeSmem<T, NT, TGS, TPB, STAGES> sm;
+  __shared__ unsigned s_ticket, s_flag;
+
+  const int tid = threadIdx.x;
+  const int64_t L = p.seqlen, N = p.dstate;
+  const int64_t M = p.tiles;
+  const int64_t units = M * p.nchunks;
+  const int ng0 = p.group * NT;
+
+  for (;;) {
+    if (tid == 0) s_ticket = atomicAdd(p.ticket, 1u);
+    __syncthreads();
+    const int64_t t = s_ticket;
+    __syncthreads();
+    if (t >= units) break;
+    const int k = (int)(t / M);
+    const int64_t tile = t - (int64_t)k * M;
+    const PairRows<TGS, TPB> rs(tile, p.dim);
+    const int nl0 = rs.q * G;
+    const int64_t t_begin = (int64_t)k * p.chunk_len;
+    const int64_t t_end = min(L, t_begin + p.chunk_len);
+    auto rec = [&](int kk, int s, int n) -> int64_t {  // record index of (unit kk of this tile)
+      return (((int64_t)kk * M + tile) * RPC + rs.rc[s]) * NT + n;
+    };
+
+    f2 A2[2][GP], h[2][GP];
+    float bias[OWN], Dd[OWN], dt_sum[OWN];
+#pragma unroll
+    for (int o = 0; o < OWN; ++o) {
+      bias[o] = p.bias ? p.bias[rs.d[o]] : 0.f;
+      Dd[o] = p.D ? p.D[rs.d[o]] : 0.f;
+      dt_sum[o] = 0.f;
+    }
+#pragma unroll
+    for (int s = 0; s < 2; ++s) {
+#pragma unroll
+      for (int kk = 0; kk < GP; ++kk) {
+        float a[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int64_t n = ng0 + nl0 + 2 * kk + e;
+          a[e] = n < N ? p.A[rs.d[s] * N + n] * kLog2e : 0.f;
+        }
+        A2[s][kk] = pack(a[0], a[1]);
+        h[s][kk] = splat(0.f);
+      }
+    }
+
+    // ---- carry into this unit ----
+    bool published = false;  // this unit's end state already published
+    if (k > 0 && p.chained) {
+      if (tid == 0) s_flag = wait_flag(&p.flags[(int64_t)(k - 1) * M + tile], kUnitIncl);
+      __syncthreads();
+      const bool ok = s_flag >= kUnitIncl;
+      __syncthreads();
+      if (ok) {
+#pragma unroll
+        for (int s = 0; s < 2; ++s)
+#pragma unroll
+          for (int kk = 0; kk < GP; ++kk)
+            h[s][kk] = pack(__ldcg(&p.unit_incl[rec(k - 1, s, nl0 + 2 * kk)]),
+                            __ldcg(&p.unit_incl[rec(k - 1, s, nl0 + 2 * kk + 1)]));
+      }
+    } else if (k == 0 && !p.chained && p.nchunks > 1) {
+      // decoupled, first chunk: its carry is zero, so the state its aggregate
+      // pass reaches is its end state; publishing that before the main pass
+      // lets the look-backs of the later chunks finish early
+      scan_pass<T, NT, TGS, TPB, STAGES, true>(p, sm, rs, t_begin, t_end, h, A2, bias, Dd,
+                                               dt_sum);
+#pragma unroll
+      for (int s = 0; s < 2; ++s)
+#pragma unroll
+        for (int kk = 0; kk < GP; ++kk) {
+          float hv[2];
+          unpack(h[s][kk], hv[0], hv[1]);
+          p.unit_incl[rec(0, s, nl0 + 2 * kk)] = hv[0];
+          p.unit_incl[rec(0, s, nl0 + 2 * kk + 1)] = hv[1];
+          h[s][kk] = splat(0.f);
+        }
+      __threadfence();
+      __syncthreads();
+      if (tid == 0) st_release(&p.flags[tile], kUnitIncl);
+      published = true;
+    } else if (k > 0) {
+      // decoupled: own aggregate first, published for successors
+      scan_pass<T, NT, TGS, TPB, STAGES, true>(p, sm, rs, t_begin, t_end, h, A2, bias, Dd,
+                                               dt_sum);
+      float sum[2];
+      if constexpr (TGS == 1) {
+        sum[0] = dt_sum[0];
+        sum[1] = dt_sum[1];
+      } else {
+        sum[0] = dt_sum[0];
+        if constexpr (TGS == 4) sum[0] += __shfl_xor_sync(0xffffffffu, sum[0], 2);
+        sum[1] = __shfl_xor_sync(0xffffffffu, sum[0], 1);
+      }
+      f2 Pk[2][GP], ek[2][GP];
+#pragma unroll
+      for (int s = 0; s < 2; ++s) {
+#pragma unroll
+        for (int kk = 0; kk < GP; ++kk) {
+          Pk[s][kk] = ex2x2(mul2(splat(sum[s]), A2[s][kk]));
+          ek[s][kk] = h[s][kk];
+          float pv[2], ev[2];
+          unpack(Pk[s][kk], pv[0], pv[1]);
+          unpack(ek[s][kk], ev[0], ev[1]);
+          p.unit_agg[rec(k, s, nl0 + 2 * kk)] = make_float2(pv[0], ev[0]);
+          p.unit_agg[rec(k, s, nl0 + 2 * kk + 1)] = make_float2(pv[1], ev[1]);
+        }
+      }
+      __threadfence();
+      __syncthreads();
+      if (tid == 0) {
+        st_release(&p.flags[(int64_t)k * M + tile], kUnitAgg);
+        // look back to the nearest predecessor whose end state is published
+        int j0 = k - 1;
+        unsigned f = 0;
+        for (;; --j0) {
+          f = wait_flag(&p.flags[(int64_t)j0 * M + tile], kUnitAgg);
+          if (f == 0u || f >= kUnitIncl || j0 == 0) break;
+        }
+        s_flag = (f >= kUnitIncl) ? (unsigned)j0 + 1u : 0u;  // 0: a wait gave up
+      }
+      __syncthreads();
+      const unsigned found = s_flag;
+      __syncthreads();
+      // carry into unit k: the end state of chunk j0, then the aggregates of
+      // chunks j0+1 .. k-1 applied in chunk order
+#pragma unroll
+      for (int s = 0; s < 2; ++s)
+#pragma unroll
+        for (int kk = 0; kk < GP; ++kk) h[s][kk] = splat(0.f);
+      if (found != 0u) {
+        const int j0 = (int)found - 1;
+#pragma unroll
+        for (int s = 0; s < 2; ++s)
+#pragma unroll
+          for (int kk = 0; kk < GP; ++kk)
+            h[s][kk] = pack(__ldcg(&p.unit_incl[rec(j0, s, nl0 + 2 * kk)]),
+                            __ldcg(&p.unit_incl[rec(j0, s, nl0 + 2 * kk + 1)]));
+        for (int jj = j0 + 1; jj < k; ++jj) {
+#pragma unroll
+          for (int s = 0; s < 2; ++s)
+#pragma unroll
+            for (int kk = 0; kk < GP; ++kk) {
+              const float2 r0 = __ldcg(&p.unit_agg[rec(jj, s, nl0 + 2 * kk)]);
+              const float2 r1 = __ldcg(&p.unit_agg[rec(jj, s, nl0 + 2 * kk + 1)]);
+              h[s][kk] = fma2(pack(r0.x, r1.x), h[s][kk], pack(r0.y, r1.y));
+            }
+        }
+      }
+      // own end state = own aggregate applied to the carry, published before the main pass
+      if (k + 1 < p.nchunks) {
+#pragma unroll
+        for (int s = 0; s < 2; ++s)
+#pragma unroll
+          for (int kk = 0; kk < GP; ++kk) {
+            const f2 hend = fma2(Pk[s][kk], h[s][kk], ek[s][kk]);
+            float hv[2];
+            unpack(hend, hv[0], hv[1]);
+            p.unit_incl[rec(k, s, nl0 + 2 * kk)] = hv[0];
+            p.unit_incl[rec(k, s, nl0 + 2 * kk + 1)] = hv[1];
+          }
+        __threadfence();
+        __syncthreads();
+        if (tid == 0) st_release(&p.flags[(int64_t)k * M + tile], kUnitIncl);
+      }
+      published = true;
+    }
+
+    // ---- main pass from the carry ----
+    scan_pass<T, NT, TGS, TPB, STAGES, false>(p, sm, rs, t_begin, t_end, h, A2, bias, Dd,
+                                              dt_sum);
+
+    if (k + 1 < p.nchunks) {
+      if (!published) {
+#pragma unroll
+        for (int s = 0; s < 2; ++s)
+#pragma unroll
+          for (int kk = 0; kk < GP; ++kk) {
+            float hv[2];
+            unpack(h[s][kk], hv[0], hv[1]);
+            p.unit_incl[rec(k, s, nl0 + 2 * kk)] = hv[0];
+            p.unit_incl[rec(k, s, nl0 + 2 * kk + 1)] = hv[1];
+          }
+        __threadfence();
+        __syncthreads();
+        if (tid == 0) st_release(&p.flags[(int64_t)k * M + tile], kUnitIncl);
+      }
+    } else if (p.last_state) {
+#pragma unroll
+      for (int s = 0; s < 2; ++s) {
+        if (!rs.valid[s]) continue;
+#pragma unroll
+        for (int kk = 0; kk < GP; ++kk) {
+          float hv[2];
+          unpack(h[s][kk], hv[0], hv[1]);
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int64_t n = ng0 + nl0 + 2 * kk + e;
+            if (n < N) p.last_state[rs.row[s] * N + n] = hv[e];
+          }
+        }
+      }
+    }
+    __syncthreads();  // shared buffers are reused by the next unit
+  }
+}
+
+}  // namespace ss

@@ -82,24 +82,28 @@ def test_validation_rejects_bad_arguments(lib):
 
 def test_plan_is_host_only_and_consistent(lib, monkeypatch):
     monkeypatch.delenv("SS_NCHUNKS", raising=False)
-    # a short sequence with many rows runs as one chunk, one launch, no scratch
+    monkeypatch.delenv("SS_CTAS_PER_SM", raising=False)
+    # vector path: one scheduled launch per call, chunks joined inside the kernel
     p = ss.ss_selective_scan_plan(8, 5120, 16, 2048, ss.SS_BF16, True, 152)
-    assert p["nchunks"] >= 1 and p["state_groups"] == 1 and p["vector_path"] == 1
-    if p["nchunks"] == 1:
-        assert p["kernel_launches"] == 1 and p["scratch_bytes"] == 0
-    # few rows and a long sequence are split into chunks joined by carries
+    assert p["state_groups"] == 1 and p["vector_path"] == 1 and p["kernel_launches"] == 1
+    assert p["nchunks"] >= 1 and p["ctas"] <= 152 * 8
+    # few rows and a long sequence: many chunks, still one launch
     p = ss.ss_selective_scan_plan(1, 2048, 16, 65536, ss.SS_BF16, True, 152)
-    assert p["nchunks"] > 1 and p["kernel_launches"] == 3
+    assert p["nchunks"] > 1 and p["kernel_launches"] == 1
     assert p["chunk_len"] % 64 == 0 and (p["nchunks"] - 1) * p["chunk_len"] < 65536
-    assert p["scratch_bytes"] == (p["nchunks"] - 1) * 2048 * 16 * 8 + p["nchunks"] * 2048 * 16 * 4
-    # dstate above 16 runs in state groups, one main launch per group
+    assert p["scratch_bytes"] > 0
+    # dstate above 16 runs in state groups, one launch per group
     p = ss.ss_selective_scan_plan(2, 64, 40, 256, ss.SS_F32, True, 152)
-    assert p["state_groups"] == 3
-    # misaligned pointers or odd lengths take the scalar path
-    assert ss.ss_selective_scan_plan(2, 64, 16, 250, ss.SS_BF16, True, 152)["vector_path"] == 0
+    assert p["state_groups"] == 3 and p["kernel_launches"] == 3
+    # misaligned pointers or odd lengths take the scalar path (aggregate + carry + main)
+    p = ss.ss_selective_scan_plan(2, 64, 16, 250, ss.SS_BF16, True, 152)
+    assert p["vector_path"] == 0
     assert ss.ss_selective_scan_plan(2, 64, 16, 256, ss.SS_BF16, False, 152)["vector_path"] == 0
-    # the tuning override forces the chunk count
     monkeypatch.setenv("SS_NCHUNKS", "4")
+    p = ss.ss_selective_scan_plan(2, 64, 16, 1024, ss.SS_F32, False, 152)
+    assert p["nchunks"] == 4 and p["kernel_launches"] == 3
+    assert p["scratch_bytes"] == 3 * 128 * 16 * 8 + 4 * 128 * 16 * 4
+    # the tuning override forces the chunk count on the vector path too
     assert ss.ss_selective_scan_plan(2, 64, 16, 1024, ss.SS_F32, True, 152)["nchunks"] == 4
     with pytest.raises(ss.SelectiveScanError):
         ss.ss_selective_scan_plan(0, 64, 16, 1024, ss.SS_F32, True, 152)

@@ -124,6 +124,37 @@ def test_chunked_sequence(orc, monkeypatch, dtype, nchunks, L, dstate):
     check(orc, W(2, 70, dstate, L, dtype, seed=nchunks + L, dt_lo=1e-4, dt_hi=1e-2))
 
 
+# ---- the ticketed scheduler in each of its modes ----
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("ctas_per_sm,shape,nchunks", [
+    (1, (4, 2560, 16, 1024), 4),   # more row tiles than CTAs: chained chunks
+    (2, (2, 5120, 16, 1024), 8),   # fewer tiles than CTAs: decoupled, long look-backs
+    (4, (1, 256, 16, 4096), 32),   # few tiles, many chunks: decoupled look-back
+])
+def test_scheduler_modes(orc, monkeypatch, dtype, ctas_per_sm, shape, nchunks):
+    monkeypatch.setenv("SS_CTAS_PER_SM", str(ctas_per_sm))
+    monkeypatch.setenv("SS_NCHUNKS", str(nchunks))
+    w = W(*shape, dtype, seed=ctas_per_sm * 7 + nchunks, dt_lo=1e-4, dt_hi=1e-2)
+    inp = make_inputs(w)
+    y, last = run_gpu(inp)
+    rows = sample_rows(w, 64, seed=5)
+    ref = oracle_rows(orc, inp, w, rows)
+    yf = y.reshape(-1, w.seqlen)
+    sf = last.reshape(-1, w.dstate)
+    for r in sorted(ref):
+        assert_close(yf[r], ref[r][0], dtype, f"row {r} y")
+        assert_close(sf[r], ref[r][1], dtype, f"row {r} state")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("nchunks", [1, 5])
+def test_four_lanes_per_row_pair(orc, monkeypatch, dtype, nchunks):
+    """The four-lanes-per-row-pair layout (16 states, tuning option) matches too."""
+    monkeypatch.setenv("SS_LANES_PER_PAIR", "4")
+    monkeypatch.setenv("SS_NCHUNKS", str(nchunks))
+    check(orc, W(2, 100, 16, 640, dtype, seed=nchunks, dt_lo=1e-4, dt_hi=1e-2))
+
+
 # ---- unaligned rows take the scalar path ----
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_unaligned_rows(orc, dtype):
