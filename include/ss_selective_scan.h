@@ -54,8 +54,10 @@ typedef enum {
   SS_ERR_UNSUPPORTED = 2,      /* unknown dtype, dstate outside 1..256, or a
                                   size that overflows 64-bit indexing */
   SS_ERR_CUDA = 3,             /* a CUDA runtime call or a launch failed */
-  SS_ERR_TIMEOUT = 4           /* a device-side wait gave up (reported by
+  SS_ERR_TIMEOUT = 4,          /* a device-side wait gave up (reported by
                                   ss_selective_scan_check only) */
+  SS_ERR_SCRATCH_LIMIT = 5     /* ss_selective_scan_fwd_noalloc: the problem needs
+                                  more scratch than its fixed buffer holds */
 } ss_status_t;
 
 /*
@@ -113,6 +115,46 @@ SS_API const char* ss_status_string(ss_status_t status);
  * error.
  */
 SS_API ss_status_t ss_selective_scan_check(void* stream);
+
+/*
+ * ss_selective_scan_fwd_noalloc -- the same forward as ss_selective_scan_fwd
+ * for callers that cannot allocate device memory during a call: code that
+ * runs where cudaMalloc/cudaMallocAsync is not allowed or not wanted, for
+ * example under a caching allocator it must not bypass, inside a real-time
+ * path that forbids allocator calls, or in a host that owns all device memory
+ * up front.  The pages have no counterpart to this entry point; it is a
+ * library service.
+ *
+ * Arguments, layouts, ownership and the result are those of
+ * ss_selective_scan_fwd.  Instead of stream-ordered scratch it uses one
+ * fixed 16 MiB buffer in the library's own device memory (a file-scope
+ * __device__ array, present on every GPU that loads the library until the
+ * process exits).  It calls no allocating function: it zeroes the part of the
+ * buffer that must start at zero with cudaMemsetAsync on `stream` and
+ * launches the scheduled kernel.
+ *
+ * Set-up: the first call on a device (with that device current) looks up the
+ * buffer's device address with cudaGetSymbolAddress; make that first call
+ * before any stream capture on that device.
+ *
+ * Limits: the vector path only (every u/delta/z/y/B/C pointer 16-byte aligned
+ * and seqlen a multiple of 4 for float32, of 8 for bf16), else
+ * SS_ERR_UNSUPPORTED.  Long sequences are split into fewer chunks than
+ * ss_selective_scan_fwd would use when its carries would not fit the buffer;
+ * a problem that does not fit even unsplit (dstate > 16 needs a float32 row
+ * of batch * dim * seqlen partial read-outs) returns SS_ERR_SCRATCH_LIMIT.
+ *
+ * Concurrency: every call shares the one buffer per device, so calls whose
+ * execution overlaps on the GPU (different streams, or graphs replayed
+ * concurrently) race on it and give wrong results; order such calls on one
+ * stream or use ss_selective_scan_fwd.
+ */
+SS_API ss_status_t ss_selective_scan_fwd_noalloc(
+    const void* u, const void* delta, const float* A, const void* B, const void* C,
+    const float* D, const void* z, const float* delta_bias, int delta_softplus,
+    void* y, float* last_state,
+    int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
+    ss_dtype_t dtype, void* stream);
 
 /*
  * ss_selective_scan_plan -- describe, without any CUDA call, how

@@ -18,13 +18,14 @@ from pathlib import Path
 
 __all__ = [
     "SS_F32", "SS_BF16", "SS_OK", "SS_ERR_INVALID_ARGUMENT", "SS_ERR_UNSUPPORTED",
-    "SS_ERR_CUDA", "SS_ERR_TIMEOUT", "SelectiveScanError", "library_path", "load_library",
+    "SS_ERR_CUDA", "SS_ERR_TIMEOUT", "SS_ERR_SCRATCH_LIMIT", "SelectiveScanError", "library_path", "load_library",
     "ss_selective_scan_fwd", "ss_status_string", "ss_selective_scan_check",
-    "ss_selective_scan_plan", "selective_scan_fwd",
+    "ss_selective_scan_plan", "ss_selective_scan_fwd_noalloc", "selective_scan_fwd",
 ]
 
 SS_F32, SS_BF16 = 0, 1
-SS_OK, SS_ERR_INVALID_ARGUMENT, SS_ERR_UNSUPPORTED, SS_ERR_CUDA, SS_ERR_TIMEOUT = range(5)
+(SS_OK, SS_ERR_INVALID_ARGUMENT, SS_ERR_UNSUPPORTED, SS_ERR_CUDA, SS_ERR_TIMEOUT,
+ SS_ERR_SCRATCH_LIMIT) = range(6)
 
 _PKG = Path(__file__).resolve().parent
 _LIB = None
@@ -58,6 +59,8 @@ def load_library():
         lib.ss_status_string.argtypes = [ctypes.c_int]
         lib.ss_selective_scan_check.restype = ctypes.c_int
         lib.ss_selective_scan_check.argtypes = [vp]
+        lib.ss_selective_scan_fwd_noalloc.restype = ctypes.c_int
+        lib.ss_selective_scan_fwd_noalloc.argtypes = list(lib.ss_selective_scan_fwd.argtypes)
         lib.ss_selective_scan_plan.restype = ctypes.c_int
         lib.ss_selective_scan_plan.argtypes = [i64, i64, i64, i64, ctypes.c_int, ctypes.c_int,
                                                ctypes.c_int, ctypes.POINTER(_Plan)]
@@ -86,6 +89,19 @@ def ss_selective_scan_fwd(u, delta, A, B, C, D, z, delta_bias, delta_softplus, y
                           batch, dim, dstate, seqlen, dtype, stream) -> int:
     """Direct call of the C entry point; pointers are ints (0/None = NULL)."""
     return load_library().ss_selective_scan_fwd(
+        u, delta, A, B, C, D, z, delta_bias, int(delta_softplus), y, last_state,
+        batch, dim, dstate, seqlen, int(dtype), stream)
+
+
+def ss_selective_scan_fwd_noalloc(u, delta, A, B, C, D, z, delta_bias, delta_softplus, y,
+                                  last_state, batch, dim, dstate, seqlen, dtype, stream) -> int:
+    """The forward for callers that cannot allocate device memory during a call.
+
+    Same arguments as ``ss_selective_scan_fwd``; the library uses its own fixed
+    16 MiB device buffer instead of allocating scratch, so calls that overlap
+    on the GPU must not be issued (they would share that buffer).
+    """
+    return load_library().ss_selective_scan_fwd_noalloc(
         u, delta, A, B, C, D, z, delta_bias, int(delta_softplus), y, last_state,
         batch, dim, dstate, seqlen, int(dtype), stream)
 

@@ -11,6 +11,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <algorithm>
+#include <mutex>
 
 #include "ss_sched.cuh"
 #include "ss_selective_scan.h"
@@ -228,6 +229,7 @@ SS_API const char* ss_status_string(ss_status_t status) {
     case SS_ERR_UNSUPPORTED: return "SS_ERR_UNSUPPORTED";
     case SS_ERR_CUDA: return "SS_ERR_CUDA";
     case SS_ERR_TIMEOUT: return "SS_ERR_TIMEOUT";
+    case SS_ERR_SCRATCH_LIMIT: return "SS_ERR_SCRATCH_LIMIT";
     default: return "SS_UNKNOWN_STATUS";
   }
 }
@@ -364,3 +366,132 @@ SS_API ss_status_t ss_selective_scan_check(void* stream) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// No-allocation entry point: the scheduled kernel with its scratch in a fixed
+// buffer of the library's own device memory instead of stream-ordered
+// allocations, for callers that cannot allocate during a call.
+namespace {
+
+constexpr int64_t kNoAllocScratchBytes = int64_t(16) << 20;  // 16 MiB per device
+constexpr int kNoAllocMaxDevices = 64;
+
+// The buffer itself.  In host code this name is only a stand-in for the
+// symbol; its device address comes from cudaGetSymbolAddress.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_noalloc_mutex;
+void* g_noalloc_address[kNoAllocMaxDevices] = {};
+
+// Device address of the buffer on the current device, looked up once per
+// device (the first call on a device does this set-up).
+cudaError_t noalloc_scratch(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kNoAllocMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (!g_noalloc_address[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    g_noalloc_address[dev] = p;
+  }
+  *out = g_noalloc_address[dev];
+  return cudaSuccess;
+}
+
+// Re-derive the chunked part of a vector-path plan for a forced chunk count.
+void set_chunks(LaunchPlan* plan, int64_t seqlen, int64_t slots, int64_t want) {
+  want = std::max<int64_t>(1, std::min<int64_t>(want, seqlen / ss::kTileSteps));
+  plan->chunk_len = round_up((seqlen + want - 1) / want, ss::kTileSteps);
+  plan->nchunks = (int)((seqlen + plan->chunk_len - 1) / plan->chunk_len);
+  plan->grid = std::min<int64_t>(plan->tiles * plan->nchunks, slots);
+  plan->chained = plan->tiles >= plan->grid;
+  plan->sched_bytes_per_group = round_up(128 + plan->nchunks * plan->tiles * 4, 256);
+  plan->sched_bytes = plan->sched_bytes_per_group * plan->groups;
+  const int64_t rec = (int64_t)plan->nchunks * plan->tiles * plan->rows_per_cta * plan->nt;
+  plan->unit_agg_bytes = round_up(rec * 8, 256);
+  plan->unit_incl_bytes = round_up(rec * 4, 256);
+}
+
+}  // namespace
+
+extern "C" SS_API ss_status_t ss_selective_scan_fwd_noalloc(
+    const void* u, const void* delta, const float* A, const void* B, const void* C,
+    const float* D, const void* z, const float* delta_bias, int delta_softplus,
+    void* y, float* last_state,
+    int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
+    ss_dtype_t dtype, void* stream) {
+  // ---- validation, as ss_selective_scan_fwd ----
+  if (dtype != SS_F32 && dtype != SS_BF16) return SS_ERR_UNSUPPORTED;
+  if (!u || !delta || !A || !B || !C || !y) return SS_ERR_INVALID_ARGUMENT;
+  if (batch <= 0 || dim <= 0 || dstate <= 0 || seqlen <= 0) return SS_ERR_INVALID_ARGUMENT;
+  if (dstate > 256) return SS_ERR_UNSUPPORTED;
+  const int64_t elt = dtype == SS_F32 ? 4 : 2;
+  Sizes sz;
+  if (!sizes_ok(batch, dim, dstate, seqlen, elt, &sz)) return SS_ERR_UNSUPPORTED;
+  const uintptr_t ea = (uintptr_t)elt;
+  if (!aligned(u, ea) || !aligned(delta, ea) || !aligned(B, ea) || !aligned(C, ea) ||
+      !aligned(y, ea) || (z && !aligned(z, ea)) || !aligned(A, 4) || (D && !aligned(D, 4)) ||
+      (delta_bias && !aligned(delta_bias, 4)) || (last_state && !aligned(last_state, 4)))
+    return SS_ERR_INVALID_ARGUMENT;
+  const void* ins[] = {u, delta, B, C, z, A, D, delta_bias};
+  const int64_t in_bytes[] = {sz.x_bytes, sz.x_bytes, sz.bc_bytes, sz.bc_bytes,
+                              z ? sz.x_bytes : 0, sz.a_elems * 4, D ? dim * 4 : 0,
+                              delta_bias ? dim * 4 : 0};
+  for (int i = 0; i < 8; ++i) {
+    if (range_overlap(y, sz.x_bytes, ins[i], in_bytes[i])) return SS_ERR_INVALID_ARGUMENT;
+    if (last_state && range_overlap(last_state, sz.st_elems * 4, ins[i], in_bytes[i]))
+      return SS_ERR_INVALID_ARGUMENT;
+  }
+  if (last_state && range_overlap(last_state, sz.st_elems * 4, y, sz.x_bytes))
+    return SS_ERR_INVALID_ARGUMENT;
+
+  // ---- plan: the vector path only, its carries fitted into the fixed buffer ----
+  const bool aligned16 = aligned(u, 16) && aligned(delta, 16) && aligned(B, 16) &&
+                         aligned(C, 16) && aligned(y, 16) && (!z || aligned(z, 16));
+  if (!aligned16 || seqlen % (16 / elt) != 0) return SS_ERR_UNSUPPORTED;
+  const int sms = sm_count();
+  if (sms <= 0) return SS_ERR_CUDA;
+  LaunchPlan plan{};
+  if (!make_plan(batch, dim, dstate, seqlen, elt, true, sms, &plan) || !plan.vec)
+    return SS_ERR_UNSUPPORTED;
+  const int64_t slots = (int64_t)sms * std::max(1, env_int("SS_CTAS_PER_SM", kCtasPerSm));
+  while (scratch_bytes(plan) > kNoAllocScratchBytes && plan.nchunks > 1)
+    set_chunks(&plan, seqlen, slots, plan.nchunks / 2);
+  if (plan.nchunks == 1) {  // one chunk needs no carries
+    plan.unit_agg_bytes = plan.unit_incl_bytes = 0;
+  }
+  if (scratch_bytes(plan) > kNoAllocScratchBytes) return SS_ERR_SCRATCH_LIMIT;
+
+  void* base_ptr = nullptr;
+  if (noalloc_scratch(&base_ptr) != cudaSuccess) return SS_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  ss::FwdParams p{};
+  p.u = u; p.delta = delta; p.A = A; p.B = B; p.C = C; p.D = D; p.z = z; p.bias = delta_bias;
+  p.y = y; p.last_state = last_state;
+  p.batch = batch; p.dim = dim; p.dstate = dstate; p.seqlen = seqlen;
+  p.chunk_len = plan.chunk_len;
+  p.nchunks = plan.nchunks;
+  p.ns = plan.groups * plan.nt;
+  p.softplus = delta_softplus ? 1 : 0;
+  p.tiles = plan.tiles;
+  p.chained = plan.chained ? 1 : 0;
+  char* base = static_cast<char*>(base_ptr);
+  (void)cudaGetLastError();
+  // the tickets and unit flags of the previous call must not be seen
+  if (cudaMemsetAsync(base, 0, (size_t)plan.sched_bytes, st) != cudaSuccess) return SS_ERR_CUDA;
+  p.ticket = reinterpret_cast<unsigned*>(base);
+  base += plan.sched_bytes;
+  if (plan.unit_agg_bytes) {
+    p.unit_agg = reinterpret_cast<float2*>(base);
+    base += plan.unit_agg_bytes;
+    p.unit_incl = reinterpret_cast<float*>(base);
+    base += plan.unit_incl_bytes;
+  }
+  if (plan.part_bytes) p.y_partial = reinterpret_cast<float*>(base);
+  const cudaError_t err = dtype == SS_F32 ? dispatch<float>(p, plan, st)
+                                          : dispatch<__nv_bfloat16>(p, plan, st);
+  return err == cudaSuccess ? SS_OK : SS_ERR_CUDA;
+}

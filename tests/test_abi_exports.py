@@ -27,7 +27,8 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     assert declared_functions() == ["ss_selective_scan_check", "ss_selective_scan_fwd",
-                                    "ss_selective_scan_plan", "ss_status_string"]
+                                    "ss_selective_scan_fwd_noalloc", "ss_selective_scan_plan",
+                                    "ss_status_string"]
 
 
 def test_library_exports_every_declared_symbol(lib):
