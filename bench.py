@@ -403,7 +403,7 @@ def run_ours(args, world, rank, local):
     t_fp32 = 4 * w.updates / r_fp32
     t_step = ms_step * 1e-3 / world * world  # per-rank step time
     kernel_src = [REPO / "mamba_selective_scan_ss_gb300" / "csrc" / f
-                  for f in ("ss_fwd.cuh", "ss_device.cuh", "ss_api.cu")]
+                  for f in ("ss_fwd.cuh", "ss_sched.cuh", "ss_device.cuh", "ss_api.cu")]
     traffic, traffic_src = traffic_record(kernel_src, w.name)
     if t_hbm >= max(t_sfu, t_fp32):
         achieved = nbytes / t_step / 1e9
