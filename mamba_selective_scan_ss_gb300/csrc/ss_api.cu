@@ -99,11 +99,8 @@ bool make_plan(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, int64
   plan->nt = dstate <= 4 ? 4 : (dstate <= 8 ? 8 : 16);
   plan->groups = (int)((dstate + plan->nt - 1) / plan->nt);
   plan->vec = aligned16 && seqlen % (16 / elt) == 0;
-  // lanes sharing a row pair on the vector path: two for 8 or 16 states, one
-  // for 4 (SS_LANES_PER_PAIR=4 gives four lanes for 16 states: twice the
-  // resident warps for more shuffles and half-vector copies; a tuning aid)
+  // lanes sharing a row pair on the vector path: two for 8 or 16 states, one for 4
   plan->tgs = plan->nt >= 8 ? 2 : 1;
-  if (plan->nt == 16 && env_int("SS_LANES_PER_PAIR", 0) == 4) plan->tgs = 4;
   plan->rows_per_cta = plan->vec ? 2 * kThreads / plan->tgs : kThreads * kRows;
   plan->dim_tiles = (dim + plan->rows_per_cta - 1) / plan->rows_per_cta;
   if (plan->dim_tiles > INT_MAX / std::max<int64_t>(batch, 1)) return false;
@@ -165,9 +162,9 @@ int64_t scratch_bytes(const LaunchPlan& plan) {
          plan.carry_bytes + plan.part_bytes;
 }
 
-template <typename T, int NT, int TGS>
+template <typename T, int NT, int TGS, bool HAS_Z, bool MULTI>
 cudaError_t enqueue_vec(ss::FwdParams p, const LaunchPlan& plan, cudaStream_t st) {
-  auto kernel = ss::ss_fwd_sched<T, NT, TGS, kThreads, kStages>;
+  auto kernel = ss::ss_fwd_sched<T, NT, TGS, kThreads, kStages, HAS_Z, MULTI>;
   char* sched = reinterpret_cast<char*>(p.ticket);
   for (int g = 0; g < plan.groups; ++g) {
     p.group = g;
@@ -178,6 +175,16 @@ cudaError_t enqueue_vec(ss::FwdParams p, const LaunchPlan& plan, cudaStream_t st
     kernel<<<(unsigned)plan.grid, kThreads, 0, st>>>(p);
   }
   return cudaGetLastError();
+}
+
+template <typename T, int NT, int TGS>
+cudaError_t enqueue_vec_flags(const ss::FwdParams& p, const LaunchPlan& plan, cudaStream_t st) {
+  const bool has_z = p.z != nullptr;
+  if (plan.groups > 1)
+    return has_z ? enqueue_vec<T, NT, TGS, true, true>(p, plan, st)
+                 : enqueue_vec<T, NT, TGS, false, true>(p, plan, st);
+  return has_z ? enqueue_vec<T, NT, TGS, true, false>(p, plan, st)
+               : enqueue_vec<T, NT, TGS, false, false>(p, plan, st);
 }
 
 template <typename T, int NT>
@@ -204,11 +211,9 @@ template <typename T>
 cudaError_t dispatch(const ss::FwdParams& p, const LaunchPlan& plan, cudaStream_t st) {
   if (plan.vec) {
     switch (plan.nt) {
-      case 4: return enqueue_vec<T, 4, 1>(p, plan, st);
-      case 8: return enqueue_vec<T, 8, 2>(p, plan, st);
-      default:
-        return plan.tgs == 2 ? enqueue_vec<T, 16, 2>(p, plan, st)
-                             : enqueue_vec<T, 16, 4>(p, plan, st);
+      case 4: return enqueue_vec_flags<T, 4, 1>(p, plan, st);
+      case 8: return enqueue_vec_flags<T, 8, 2>(p, plan, st);
+      default: return enqueue_vec_flags<T, 16, 2>(p, plan, st);
     }
   }
   switch (plan.nt) {

@@ -134,40 +134,6 @@ struct Elem<__nv_bfloat16> {
   __device__ __forceinline__ static __nv_bfloat16 from_f32(float x) { return __float2bfloat16_rn(x); }
 };
 
-// NP fp32 pairs (consecutive steps) from 32-bit words of packed elements:
-// two words per pair for float, one word (a bf16x2) per pair for bf16.
-template <typename T, int NP>
-__device__ __forceinline__ void words_to_pairs(const unsigned* w, f2 (&out)[NP]) {
-#pragma unroll
-  for (int i = 0; i < NP; ++i) {
-    if constexpr (sizeof(T) == 4) {
-      out[i] = pack(__uint_as_float(w[2 * i]), __uint_as_float(w[2 * i + 1]));
-    } else {  // low half is the earlier step
-      out[i] = pack(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u));
-    }
-  }
-}
-// ... and back (bf16: round to nearest even); writes NP * 2 * sizeof(T) bytes
-template <typename T, int NP>
-__device__ __forceinline__ void pairs_to_words(const f2 (&in)[NP], unsigned* w) {
-#pragma unroll
-  for (int i = 0; i < NP; ++i) {
-    float lo, hi;
-    unpack(in[i], lo, hi);
-    if constexpr (sizeof(T) == 4) {
-      w[2 * i] = __float_as_uint(lo);
-      w[2 * i + 1] = __float_as_uint(hi);
-    } else {
-      asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(w[i]) : "f"(hi), "f"(lo));
-    }
-  }
-}
-
-__device__ __forceinline__ void cp_async8(void* smem, const void* gmem) {
-  const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(s), "l"(gmem) : "memory");
-}
-
 // A 16-byte vector of V elements as V/2 fp32 pairs (consecutive steps).
 template <typename T>
 __device__ __forceinline__ void to_pairs(const uint4& raw, f2 (&out)[Elem<T>::kVec / 2]);

@@ -31,11 +31,8 @@
 // rows; lane q of a group holds states [q*G, (q+1)*G) (G = NT / TGS) of both
 // rows, so every B/C value it loads serves two rows.  Row work (streaming
 // u/delta/z, dt and du, the skip/gate epilogue) is split between the lanes of
-// a group: with TGS = 1 the lane does both rows; with TGS = 2 lane q does row
-// q; with TGS = 4 lane q does row q % 2 for half of each vector's steps (half
-// q / 2).  The lanes of a group gather dt and du and reduce the partial
-// read-outs by shuffle.  More lanes per row pair means more resident warps,
-// which hides the MUFU/FMA dependency latency of the recurrence.
+// a group: with TGS = 1 the lane does both rows, with TGS = 2 lane q does row
+// q and the partners swap dt, du and the partial read-outs by shuffle.
 //
 // Memory latency is taken off the critical path by asynchronous copies: u,
 // delta (and z) of a lane's own rows stream through a STAGES-deep ring of
@@ -44,8 +41,6 @@
 // kTileSteps steps are copied raw one tile ahead and widened/transposed to
 // [t][n] fp32 at the tile boundary (two barriers per tile).
 #pragma once
-
-#include <type_traits>
 
 #include "ss_fwd.cuh"
 
@@ -102,7 +97,7 @@ struct PairRows {
     q = threadIdx.x % TGS;
 #pragma unroll
     for (int s = 0; s < 2; ++s) {
-      const int which = TGS == 1 ? s : (s == 0 ? (q & 1) : 1 - (q & 1));
+      const int which = TGS == 1 ? s : (s == 0 ? q : 1 - q);
       rc[s] = which * (TPB / TGS) + g;
       const int64_t dd = base + rc[s];
       valid[s] = dd < dim;
@@ -114,12 +109,9 @@ struct PairRows {
 
 template <typename T, int NT, int TGS, int TPB, int STAGES>
 struct PipeSmem {
-  static constexpr int kOwn = TGS == 1 ? 2 : 1;
+  static constexpr int kOwn = 2 / TGS;
   static constexpr int kRaw = kTileSteps + 16 / (int)sizeof(T);  // padded raw row
-  // u, delta, z ring: a lane's own rows, a whole 16-byte vector each, or half
-  // of one when four lanes share a row pair
-  using Slot = typename std::conditional<TGS == 4, uint2, uint4>::type;
-  Slot x[STAGES][3][kOwn][TPB];
+  uint4 x[STAGES][3][kOwn][TPB];      // u, delta, z ring of the own rows
   T raw[2][NT][kRaw];                 // raw B, C tile
   float m[2][kTileSteps][NT];         // widened, transposed B, C tile
 };
@@ -127,61 +119,57 @@ struct PipeSmem {
 // One pass over steps [t_begin, t_end) of a unit: AGG = false runs the
 // recurrence from h and writes y; AGG = true runs it from h (zero) without C,
 // z or y and accumulates sum dt of the lane's own steps (for the aggregate's
-// decay).
-template <typename T, int NT, int TGS, int TPB, int STAGES, bool AGG>
+// decay).  HAS_Z: the gate input is present.  MULTI: dstate spans several
+// state groups (read-out accumulated in the fp32 partial row).
+//
+// The loop over 16-byte vectors is software-pipelined: the row work of
+// vector j+1 (its shared-memory reads, softplus and the dt/du exchange,
+// ~150 cycles of latency) is issued before the recurrence of vector j, and
+// each step's B/C loads are issued one step ahead, so those latencies overlap
+// the recurrence instead of stalling it.
+template <typename T, int NT, int TGS, int TPB, int STAGES, bool AGG, bool HAS_Z, bool MULTI>
 __device__ __forceinline__ void scan_pass(const FwdParams& p,
                                           PipeSmem<T, NT, TGS, TPB, STAGES>& sm,
                                           const PairRows<TGS, TPB>& rs, int64_t t_begin,
                                           int64_t t_end, f2 (&h)[2][NT / TGS / 2],
                                           const f2 (&A2)[2][NT / TGS / 2],
-                                          const float (&bias)[TGS == 1 ? 2 : 1],
-                                          const float (&Dd)[TGS == 1 ? 2 : 1],
-                                          float (&dt_sum)[TGS == 1 ? 2 : 1]) {
+                                          const float (&bias)[2 / TGS],
+                                          const float (&Dd)[2 / TGS],
+                                          float (&dt_sum)[2 / TGS]) {
   constexpr int V = Elem<T>::kVec;
-  constexpr bool HALF = TGS == 4;      // a lane does half of its row's steps
-  constexpr int VO = HALF ? V / 2 : V; // own steps per vector
-  constexpr int VOP = VO / 2;          // own step pairs
+  constexpr int VP = V / 2;            // step pairs in a vector
   constexpr int G = NT / TGS;          // states per lane
-  constexpr int GP = G / 2;            // state pairs per lane
-  constexpr int OWN = TGS == 1 ? 2 : 1;  // own rows (row work) per lane
+  constexpr int OWN = 2 / TGS;         // own rows (row work) per lane
   constexpr int NM = AGG ? 1 : 2;      // staged state tensors: B (, C)
+  constexpr bool GATE = !AGG && HAS_Z;
   constexpr int VPT = kTileSteps / V;  // vectors per tile
   constexpr int CPR = kTileSteps * (int)sizeof(T) / 16;  // 16-byte chunks per state row
   constexpr int EPC = 16 / (int)sizeof(T);                // elements per 16-byte chunk
-  constexpr int WPO = VO * (int)sizeof(T) / 4;            // 32-bit words of own steps
-  static_assert(STAGES >= 2 && STAGES <= VPT, "pipeline depth must fit in a tile");
+  static_assert(STAGES >= 3 && STAGES <= VPT + 1, "pipeline depth must fit in a tile");
 
   const int tid = threadIdx.x;
   const int64_t L = p.seqlen, N = p.dstate;
   const int ng0 = p.group * NT;  // first state of this launch's group
   const int nl0 = rs.q * G;      // first state of this lane within the group
-  const int hv = HALF ? (rs.q >> 1) : 0;  // which half of the vector this lane owns
-  const int gbase = (threadIdx.x & 31) & ~(TGS - 1);  // first lane of the group
   const int64_t nvec = (t_end - t_begin) / V;
   const T* __restrict__ ug = static_cast<const T*>(p.u);
   const T* __restrict__ dg = static_cast<const T*>(p.delta);
-  const T* __restrict__ zg = AGG ? nullptr : static_cast<const T*>(p.z);
+  const T* __restrict__ zg = static_cast<const T*>(p.z);
   const T* __restrict__ Bg = static_cast<const T*>(p.B);
   const T* __restrict__ Cg = static_cast<const T*>(p.C);
   T* __restrict__ y = static_cast<T*>(p.y);
+  const bool use_softplus = p.softplus != 0;
 
-  auto copy_own = [&](void* dst, const T* src) {
-    if constexpr (HALF) {
-      cp_async8(dst, src);
-    } else {
-      cp_async16(dst, src);
-    }
-  };
   auto issue_vec = [&](int64_t j) {
     if (j < nvec) {
       const int slot = (int)(j % STAGES);
-      const int64_t t = t_begin + j * V + hv * VO;
+      const int64_t t = t_begin + j * V;
 #pragma unroll
       for (int o = 0; o < OWN; ++o) {
         const int64_t off = rs.row[o] * L + t;
-        copy_own(&sm.x[slot][0][o][tid], ug + off);
-        copy_own(&sm.x[slot][1][o][tid], dg + off);
-        if (!AGG && zg) copy_own(&sm.x[slot][2][o][tid], zg + off);
+        cp_async16(&sm.x[slot][0][o][tid], ug + off);
+        cp_async16(&sm.x[slot][1][o][tid], dg + off);
+        if (GATE) cp_async16(&sm.x[slot][2][o][tid], zg + off);
       }
     }
     cp_async_commit();
@@ -200,13 +188,47 @@ __device__ __forceinline__ void scan_pass(const FwdParams& p,
     }
   };
 
+  // row work of vector j, kept in registers until its recurrence and epilogue
+  float dts[2][V], dus[2][V];   // dt and du of both row slots of the group
+  f2 up[OWN][VP], zp[OWN][VP];  // own u (skip) and z (gate)
+  auto rowwork = [&](int64_t j, float (&dt_o)[2][V], float (&du_o)[2][V], f2 (&u_o)[OWN][VP],
+                     f2 (&z_o)[OWN][VP]) {
+    const int slot = (int)(j % STAGES);
+#pragma unroll
+    for (int o = 0; o < OWN; ++o) {
+      f2 dp[VP];
+      to_pairs<T>(*reinterpret_cast<const uint4*>(&sm.x[slot][0][o][tid]), u_o[o]);
+      to_pairs<T>(*reinterpret_cast<const uint4*>(&sm.x[slot][1][o][tid]), dp);
+      if (GATE) to_pairs<T>(*reinterpret_cast<const uint4*>(&sm.x[slot][2][o][tid]), z_o[o]);
+#pragma unroll
+      for (int m = 0; m < VP; ++m) {
+        const f2 x = add2(dp[m], splat(bias[o]));
+        const f2 sp = softplus2(x);
+        f2 dtm;
+        dtm.v = use_softplus ? sp.v : x.v;
+        const f2 dum = mul2(dtm, u_o[o][m]);
+        unpack(dtm, dt_o[o][2 * m], dt_o[o][2 * m + 1]);
+        unpack(dum, du_o[o][2 * m], du_o[o][2 * m + 1]);
+      }
+    }
+    if constexpr (TGS == 2) {
+#pragma unroll
+      for (int e = 0; e < V; ++e) {
+        dt_o[1][e] = __shfl_xor_sync(0xffffffffu, dt_o[0][e], 1);
+        du_o[1][e] = __shfl_xor_sync(0xffffffffu, du_o[0][e], 1);
+      }
+    }
+  };
+
   issue_tile(t_begin);
 #pragma unroll
   for (int s = 0; s < STAGES - 1; ++s) issue_vec(s);
+  cp_async_wait<STAGES - 2>();  // vector 0 landed
+  rowwork(0, dts, dus, up, zp);
 
   for (int64_t j = 0; j < nvec; ++j) {
     issue_vec(j + STAGES - 1);
-    cp_async_wait<STAGES - 1>();  // this lane's copies of vector j (and older) landed
+    cp_async_wait<STAGES - 2>();  // this lane's copies of vector j+1 (and older) landed
     const int jt = (int)(j % VPT) * V;
     if (jt == 0) {
       // tile boundary: widen + transpose the raw tile, then prefetch the next one
@@ -229,70 +251,31 @@ __device__ __forceinline__ void scan_pass(const FwdParams& p,
       issue_tile(t0 + kTileSteps);
     }
 
-    const int slot = (int)(j % STAGES);
-    // row work of the own steps, two at a time: dt = softplus(delta + bias), du = dt*u
-    f2 dtp[OWN][VOP], dup[OWN][VOP], up[OWN][VOP];
-#pragma unroll
-    for (int o = 0; o < OWN; ++o) {
-      f2 dp[VOP];
-      words_to_pairs<T, VOP>(reinterpret_cast<const unsigned*>(&sm.x[slot][0][o][tid]), up[o]);
-      words_to_pairs<T, VOP>(reinterpret_cast<const unsigned*>(&sm.x[slot][1][o][tid]), dp);
-#pragma unroll
-      for (int m = 0; m < VOP; ++m) {
-        const f2 x = add2(dp[m], splat(bias[o]));
-        dtp[o][m] = p.softplus ? softplus2(x) : x;
-        dup[o][m] = mul2(dtp[o][m], up[o][m]);
-        if (AGG) dt_sum[o] += lo_of(dtp[o][m]) + hi_of(dtp[o][m]);
-      }
-    }
-    // dt and du of both rows of the group for all V steps, gathered before the
-    // recurrence so the shuffles stay off its dependency chain
-    float dts[2][V], dus[2][V];
-    {
-      float odt[OWN][VO], odu[OWN][VO];
-#pragma unroll
-      for (int o = 0; o < OWN; ++o)
-#pragma unroll
-        for (int m = 0; m < VOP; ++m) {
-          unpack(dtp[o][m], odt[o][2 * m], odt[o][2 * m + 1]);
-          unpack(dup[o][m], odu[o][2 * m], odu[o][2 * m + 1]);
-        }
-      if constexpr (TGS == 1) {
-#pragma unroll
-        for (int r = 0; r < 2; ++r)
-#pragma unroll
-          for (int e = 0; e < V; ++e) {
-            dts[r][e] = odt[r][e];
-            dus[r][e] = odu[r][e];
-          }
-      } else if constexpr (TGS == 2) {
-#pragma unroll
-        for (int e = 0; e < V; ++e) {
-          dts[0][e] = odt[0][e];
-          dus[0][e] = odu[0][e];
-          dts[1][e] = __shfl_xor_sync(0xffffffffu, odt[0][e], 1);
-          dus[1][e] = __shfl_xor_sync(0xffffffffu, odu[0][e], 1);
-        }
-      } else {
-        // block (row slot r, half hh) lives on lane ((q&1) ^ r) + 2*hh of the group
-#pragma unroll
-        for (int r = 0; r < 2; ++r)
-#pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            const int src = gbase + (((rs.q & 1) ^ r) + 2 * hh);
-#pragma unroll
-            for (int e = 0; e < VO; ++e) {
-              dts[r][hh * VO + e] = __shfl_sync(0xffffffffu, odt[0][e], src);
-              dus[r][hh * VO + e] = __shfl_sync(0xffffffffu, odu[0][e], src);
-            }
-          }
-      }
-    }
+    // row work of the next vector (the last vector repeats itself: unused)
+    float dts_n[2][V], dus_n[2][V];
+    f2 up_n[OWN][VP], zp_n[OWN][VP];
+    rowwork(j + 1 < nvec ? j + 1 : j, dts_n, dus_n, up_n, zp_n);
 
+    // the recurrence over the V steps of vector j
     float part[2][V];  // read-out over this lane's states, per row slot and step
+    ulonglong2 bq[G / 4], cq[G / 4];
+#pragma unroll
+    for (int k4 = 0; k4 < G / 4; ++k4) {
+      bq[k4] = *reinterpret_cast<const ulonglong2*>(&sm.m[0][jt][nl0 + 4 * k4]);
+      if (!AGG) cq[k4] = *reinterpret_cast<const ulonglong2*>(&sm.m[NM - 1][jt][nl0 + 4 * k4]);
+    }
 #pragma unroll
     for (int s = 0; s < V; ++s) {
       const int t = jt + s;
+      ulonglong2 bq_n[G / 4], cq_n[G / 4];
+      if (s + 1 < V) {
+#pragma unroll
+        for (int k4 = 0; k4 < G / 4; ++k4) {
+          bq_n[k4] = *reinterpret_cast<const ulonglong2*>(&sm.m[0][t + 1][nl0 + 4 * k4]);
+          if (!AGG)
+            cq_n[k4] = *reinterpret_cast<const ulonglong2*>(&sm.m[NM - 1][t + 1][nl0 + 4 * k4]);
+        }
+      }
       f2 dt2[2], du2[2], yacc[2][2];
 #pragma unroll
       for (int r = 0; r < 2; ++r) {
@@ -302,15 +285,8 @@ __device__ __forceinline__ void scan_pass(const FwdParams& p,
       }
 #pragma unroll
       for (int k4 = 0; k4 < G / 4; ++k4) {
-        const ulonglong2 bq = *reinterpret_cast<const ulonglong2*>(&sm.m[0][t][nl0 + 4 * k4]);
-        const f2 bp[2] = {{bq.x}, {bq.y}};
-        f2 cp[2];
-        if (!AGG) {
-          const ulonglong2 cq =
-              *reinterpret_cast<const ulonglong2*>(&sm.m[NM - 1][t][nl0 + 4 * k4]);
-          cp[0].v = cq.x;
-          cp[1].v = cq.y;
-        }
+        const f2 bp[2] = {{bq[k4].x}, {bq[k4].y}};
+        const f2 cp[2] = {{cq[k4].x}, {cq[k4].y}};
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           const int k = 2 * k4 + e;
@@ -329,80 +305,88 @@ __device__ __forceinline__ void scan_pass(const FwdParams& p,
           part[r][s] = lo_of(ys) + hi_of(ys);
         }
       }
+      if (s + 1 < V) {
+#pragma unroll
+        for (int k4 = 0; k4 < G / 4; ++k4) {
+          bq[k4] = bq_n[k4];
+          cq[k4] = cq_n[k4];
+        }
+      }
     }
 
-    if constexpr (!AGG) {
-      // read-out of the own steps: this lane's partials plus the group's
-      float yv[OWN][VO];
-      if constexpr (TGS == 1) {
+    if constexpr (AGG) {
 #pragma unroll
-        for (int s = 0; s < V; ++s) {
+      for (int o = 0; o < OWN; ++o)
+#pragma unroll
+        for (int e = 0; e < V; ++e) dt_sum[o] += dts[o][e];
+    } else {
+      float yv[OWN][V];
+#pragma unroll
+      for (int s = 0; s < V; ++s) {
+        if constexpr (TGS == 1) {
           yv[0][s] = part[0][s];
           yv[1][s] = part[1][s];
-        }
-      } else if constexpr (TGS == 2) {
-#pragma unroll
-        for (int s = 0; s < V; ++s)
+        } else {
           yv[0][s] = part[0][s] + __shfl_xor_sync(0xffffffffu, part[1][s], 1);
-      } else {
-        float yfull[V];
-#pragma unroll
-        for (int s = 0; s < V; ++s) {
-          const float w = part[0][s] + __shfl_xor_sync(0xffffffffu, part[1][s], 1);
-          yfull[s] = w + __shfl_xor_sync(0xffffffffu, w, 2);
         }
-#pragma unroll
-        for (int e = 0; e < VO; ++e) yv[0][e] = hv ? yfull[VO + e] : yfull[e];
       }
-      // epilogue of the own steps: earlier groups' read-out, skip, gate, store
+      // epilogue for V steps of the own rows: earlier groups' read-out, skip, gate, store
 #pragma unroll
       for (int o = 0; o < OWN; ++o) {
-        const int64_t off = rs.row[o] * L + t_begin + j * V + hv * VO;
-        if (p.accum_in) {
+        const int64_t off = rs.row[o] * L + t_begin + j * V;
+        if constexpr (MULTI) {
+          if (p.accum_in) {
 #pragma unroll
-          for (int e = 0; e < VO; ++e) yv[o][e] += p.y_partial[off + e];
-        }
-        if (!p.final_group) {
-          if (rs.valid[o]) {
-#pragma unroll
-            for (int e = 0; e < VO; ++e) p.y_partial[off + e] = yv[o][e];
+            for (int e = 0; e < V; ++e) yv[o][e] += p.y_partial[off + e];
           }
-          continue;
-        }
-        f2 yp[VOP];
+          if (!p.final_group) {
+            if (rs.valid[o]) {
 #pragma unroll
-        for (int m = 0; m < VOP; ++m)
+              for (int e = 0; e < V; ++e) p.y_partial[off + e] = yv[o][e];
+            }
+            continue;
+          }
+        }
+        f2 yp[VP];
+#pragma unroll
+        for (int m = 0; m < VP; ++m)
           yp[m] = fma2(splat(Dd[o]), up[o][m], pack(yv[o][2 * m], yv[o][2 * m + 1]));
-        if (zg) {
-          f2 zp[VOP];
-          words_to_pairs<T, VOP>(reinterpret_cast<const unsigned*>(&sm.x[slot][2][o][tid]), zp);
+        if constexpr (GATE) {
 #pragma unroll
-          for (int m = 0; m < VOP; ++m) yp[m] = mul2(yp[m], silu2(zp[m]));
+          for (int m = 0; m < VP; ++m) yp[m] = mul2(yp[m], silu2(zp[o][m]));
         }
-        if (rs.valid[o]) {
-          unsigned w[WPO];
-          pairs_to_words<T, VOP>(yp, w);
-          if constexpr (WPO == 4) {
-            *reinterpret_cast<uint4*>(y + off) = make_uint4(w[0], w[1], w[2], w[3]);
-          } else {
-            *reinterpret_cast<uint2*>(y + off) = make_uint2(w[0], w[1]);
-          }
-        }
+        if (rs.valid[o]) *reinterpret_cast<uint4*>(y + off) = from_pairs<T>(yp);
       }
     }
+
+    // the next vector's row work becomes the current one
+#pragma unroll
+    for (int r = 0; r < 2; ++r)
+#pragma unroll
+      for (int e = 0; e < V; ++e) {
+        dts[r][e] = dts_n[r][e];
+        dus[r][e] = dus_n[r][e];
+      }
+#pragma unroll
+    for (int o = 0; o < OWN; ++o)
+#pragma unroll
+      for (int m = 0; m < VP; ++m) {
+        up[o][m] = up_n[o][m];
+        zp[o][m] = zp_n[o][m];
+      }
   }
   cp_async_wait<0>();
 }
 
 // The persistent, ticketed kernel.  grid = resident CTAs (at most the unit
 // count), block = TPB; one launch per state group of NT states.
-template <typename T, int NT, int TGS, int TPB, int STAGES>
+template <typename T, int NT, int TGS, int TPB, int STAGES, bool HAS_Z, bool MULTI>
 __global__ void __launch_bounds__(TPB) ss_fwd_sched(const FwdParams p) {
   constexpr int G = NT / TGS;
   constexpr int GP = G / 2;
-  constexpr int OWN = TGS == 1 ? 2 : 1;
+  constexpr int OWN = 2 / TGS;
   constexpr int RPC = PairRows<TGS, TPB>::kRowsPerCta;
-  static_assert(TGS == 1 || TGS == 2 || TGS == 4, "one, two or four lanes per row pair");
+  static_assert(TGS == 1 || TGS == 2, "one or two lanes per row pair");
   static_assert(G % 4 == 0, "a lane holds a multiple of four states");
   __shared__ __align__(16) PipeSmem<T, NT, TGS, TPB, STAGES> sm;
   __shared__ unsigned s_ticket, s_flag;
@@ -471,7 +455,7 @@ __global__ void __launch_bounds__(TPB) ss_fwd_sched(const FwdParams p) {
       // decoupled, first chunk: its carry is zero, so the state its aggregate
       // pass reaches is its end state; publishing that before the main pass
       // lets the look-backs of the later chunks finish early
-      scan_pass<T, NT, TGS, TPB, STAGES, true>(p, sm, rs, t_begin, t_end, h, A2, bias, Dd,
+      scan_pass<T, NT, TGS, TPB, STAGES, true, HAS_Z, MULTI>(p, sm, rs, t_begin, t_end, h, A2, bias, Dd,
                                                dt_sum);
 #pragma unroll
       for (int s = 0; s < 2; ++s)
@@ -489,7 +473,7 @@ __global__ void __launch_bounds__(TPB) ss_fwd_sched(const FwdParams p) {
       published = true;
     } else if (k > 0) {
       // decoupled: own aggregate first, published for successors
-      scan_pass<T, NT, TGS, TPB, STAGES, true>(p, sm, rs, t_begin, t_end, h, A2, bias, Dd,
+      scan_pass<T, NT, TGS, TPB, STAGES, true, HAS_Z, MULTI>(p, sm, rs, t_begin, t_end, h, A2, bias, Dd,
                                                dt_sum);
       float sum[2];
       if constexpr (TGS == 1) {
@@ -497,7 +481,6 @@ __global__ void __launch_bounds__(TPB) ss_fwd_sched(const FwdParams p) {
         sum[1] = dt_sum[1];
       } else {
         sum[0] = dt_sum[0];
-        if constexpr (TGS == 4) sum[0] += __shfl_xor_sync(0xffffffffu, sum[0], 2);
         sum[1] = __shfl_xor_sync(0xffffffffu, sum[0], 1);
       }
       f2 Pk[2][GP], ek[2][GP];
@@ -575,7 +558,7 @@ __global__ void __launch_bounds__(TPB) ss_fwd_sched(const FwdParams p) {
     }
 
     // ---- main pass from the carry ----
-    scan_pass<T, NT, TGS, TPB, STAGES, false>(p, sm, rs, t_begin, t_end, h, A2, bias, Dd,
+    scan_pass<T, NT, TGS, TPB, STAGES, false, HAS_Z, MULTI>(p, sm, rs, t_begin, t_end, h, A2, bias, Dd,
                                               dt_sum);
 
     if (k + 1 < p.nchunks) {

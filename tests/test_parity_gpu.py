@@ -146,15 +146,6 @@ def test_scheduler_modes(orc, monkeypatch, dtype, ctas_per_sm, shape, nchunks):
         assert_close(sf[r], ref[r][1], dtype, f"row {r} state")
 
 
-@pytest.mark.parametrize("dtype", ["f32", "bf16"])
-@pytest.mark.parametrize("nchunks", [1, 5])
-def test_four_lanes_per_row_pair(orc, monkeypatch, dtype, nchunks):
-    """The four-lanes-per-row-pair layout (16 states, tuning option) matches too."""
-    monkeypatch.setenv("SS_LANES_PER_PAIR", "4")
-    monkeypatch.setenv("SS_NCHUNKS", str(nchunks))
-    check(orc, W(2, 100, 16, 640, dtype, seed=nchunks, dt_lo=1e-4, dt_hi=1e-2))
-
-
 # ---- unaligned rows take the scalar path ----
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_unaligned_rows(orc, dtype):
