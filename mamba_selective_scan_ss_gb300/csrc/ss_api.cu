@@ -68,6 +68,7 @@ struct LaunchPlan {
   int nchunks;
   int64_t chunk_len;
   int64_t grid;        // CTAs of each main launch
+  int64_t slots;       // vector path: CTAs the schedule is sized for
   bool chained;        // scheduled kernel: chained (true) or decoupled units
   // scratch (bytes)
   int64_t sched_bytes_per_group;  // ticket + unit flags (zeroed per call)
@@ -112,17 +113,23 @@ bool make_plan(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, int64
   plan->unit_incl_bytes = plan->agg_bytes = plan->carry_bytes = plan->part_bytes = 0;
   int64_t want;
   if (plan->vec) {
-    const int64_t per_sm = std::max(1, env_int("SS_CTAS_PER_SM", kCtasPerSm));
-    const int64_t slots = (int64_t)std::max(sms, 1) * per_sm;
+    const int64_t cap = std::max(1, env_int("SS_CTAS_PER_SM", kCtasPerSm));
+    const int64_t nsm = std::max(sms, 1);
+    // chained chunks need at least as many row tiles as CTAs: take the largest
+    // residency (at most cap CTAs per SM) that allows it
+    const int64_t chain_per_sm = std::min<int64_t>(cap, plan->tiles / nsm);
+    int64_t slots = nsm * cap;
     if (env_chunks > 0) {
       want = env_chunks;
-    } else if (plan->tiles >= slots) {
+    } else if (chain_per_sm >= 2 && seqlen >= 512) {
+      slots = nsm * chain_per_sm;
       want = std::min<int64_t>((8 * slots + plan->tiles - 1) / plan->tiles, seqlen / 256);
     } else if (2 * plan->tiles >= slots) {
       want = 1;  // one wave of whole rows costs less than decoupled chunks
     } else {
       want = std::min<int64_t>((4 * slots + plan->tiles - 1) / plan->tiles, seqlen / 128);
     }
+    plan->slots = slots;
     want = std::max<int64_t>(1, std::min<int64_t>({want, seqlen / ss::kTileSteps, kMaxChunks}));
     plan->chunk_len = round_up((seqlen + want - 1) / want, ss::kTileSteps);
     plan->nchunks = (int)((seqlen + plan->chunk_len - 1) / plan->chunk_len);
@@ -462,9 +469,8 @@ extern "C" SS_API ss_status_t ss_selective_scan_fwd_noalloc(
   LaunchPlan plan{};
   if (!make_plan(batch, dim, dstate, seqlen, elt, true, sms, &plan) || !plan.vec)
     return SS_ERR_UNSUPPORTED;
-  const int64_t slots = (int64_t)sms * std::max(1, env_int("SS_CTAS_PER_SM", kCtasPerSm));
   while (scratch_bytes(plan) > kNoAllocScratchBytes && plan.nchunks > 1)
-    set_chunks(&plan, seqlen, slots, plan.nchunks / 2);
+    set_chunks(&plan, seqlen, plan.slots, plan.nchunks / 2);
   if (plan.nchunks == 1) {  // one chunk needs no carries
     plan.unit_agg_bytes = plan.unit_incl_bytes = 0;
   }

@@ -124,9 +124,8 @@ struct PipeSmem {
 //
 // The loop over 16-byte vectors is software-pipelined: the row work of
 // vector j+1 (its shared-memory reads, softplus and the dt/du exchange,
-// ~150 cycles of latency) is issued before the recurrence of vector j, and
-// each step's B/C loads are issued one step ahead, so those latencies overlap
-// the recurrence instead of stalling it.
+// ~150 cycles of latency) is issued before the recurrence of vector j, so
+// that latency overlaps the recurrence instead of stalling it.
 template <typename T, int NT, int TGS, int TPB, int STAGES, bool AGG, bool HAS_Z, bool MULTI>
 __device__ __forceinline__ void scan_pass(const FwdParams& p,
                                           PipeSmem<T, NT, TGS, TPB, STAGES>& sm,
@@ -256,62 +255,42 @@ __device__ __forceinline__ void scan_pass(const FwdParams& p,
     f2 up_n[OWN][VP], zp_n[OWN][VP];
     rowwork(j + 1 < nvec ? j + 1 : j, dts_n, dus_n, up_n, zp_n);
 
-    // the recurrence over the V steps of vector j
+    // the recurrence over the V steps of vector j, one group of two state pairs
+    // at a time: inside a group the decays and inputs of all V steps depend only
+    // on dt and du, not on the state, so their MUFU and FMUL work issues as a
+    // batch while the state's own dependency chain (one FFMA2 per step) runs
     float part[2][V];  // read-out over this lane's states, per row slot and step
-    ulonglong2 bq[G / 4], cq[G / 4];
+    f2 yac[2][V];
+#pragma unroll
+    for (int r = 0; r < 2; ++r)
+#pragma unroll
+      for (int s = 0; s < V; ++s) yac[r][s] = splat(0.f);
 #pragma unroll
     for (int k4 = 0; k4 < G / 4; ++k4) {
-      bq[k4] = *reinterpret_cast<const ulonglong2*>(&sm.m[0][jt][nl0 + 4 * k4]);
-      if (!AGG) cq[k4] = *reinterpret_cast<const ulonglong2*>(&sm.m[NM - 1][jt][nl0 + 4 * k4]);
-    }
 #pragma unroll
-    for (int s = 0; s < V; ++s) {
-      const int t = jt + s;
-      ulonglong2 bq_n[G / 4], cq_n[G / 4];
-      if (s + 1 < V) {
-#pragma unroll
-        for (int k4 = 0; k4 < G / 4; ++k4) {
-          bq_n[k4] = *reinterpret_cast<const ulonglong2*>(&sm.m[0][t + 1][nl0 + 4 * k4]);
-          if (!AGG)
-            cq_n[k4] = *reinterpret_cast<const ulonglong2*>(&sm.m[NM - 1][t + 1][nl0 + 4 * k4]);
-        }
-      }
-      f2 dt2[2], du2[2], yacc[2][2];
-#pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        dt2[r] = splat(dts[r][s]);
-        du2[r] = splat(dus[r][s]);
-        yacc[r][0] = yacc[r][1] = splat(0.f);
-      }
-#pragma unroll
-      for (int k4 = 0; k4 < G / 4; ++k4) {
-        const f2 bp[2] = {{bq[k4].x}, {bq[k4].y}};
-        const f2 cp[2] = {{cq[k4].x}, {cq[k4].y}};
+      for (int s = 0; s < V; ++s) {
+        const ulonglong2 bq = *reinterpret_cast<const ulonglong2*>(&sm.m[0][jt + s][nl0 + 4 * k4]);
+        ulonglong2 cq = bq;
+        if (!AGG) cq = *reinterpret_cast<const ulonglong2*>(&sm.m[NM - 1][jt + s][nl0 + 4 * k4]);
+        const f2 bp[2] = {{bq.x}, {bq.y}};
+        const f2 cp[2] = {{cq.x}, {cq.y}};
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           const int k = 2 * k4 + e;
 #pragma unroll
           for (int r = 0; r < 2; ++r) {
-            const f2 a = ex2x2(mul2(dt2[r], A2[r][k]));
-            h[r][k] = fma2(a, h[r][k], mul2(du2[r], bp[e]));
-            if (!AGG) yacc[r][e] = fma2(cp[e], h[r][k], yacc[r][e]);
+            const f2 a = ex2x2(mul2(splat(dts[r][s]), A2[r][k]));
+            h[r][k] = fma2(a, h[r][k], mul2(splat(dus[r][s]), bp[e]));
+            if (!AGG) yac[r][s] = fma2(cp[e], h[r][k], yac[r][s]);
           }
         }
       }
-      if (!AGG) {
+    }
+    if (!AGG) {
 #pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          const f2 ys = add2(yacc[r][0], yacc[r][1]);
-          part[r][s] = lo_of(ys) + hi_of(ys);
-        }
-      }
-      if (s + 1 < V) {
+      for (int r = 0; r < 2; ++r)
 #pragma unroll
-        for (int k4 = 0; k4 < G / 4; ++k4) {
-          bq[k4] = bq_n[k4];
-          cq[k4] = cq_n[k4];
-        }
-      }
+        for (int s = 0; s < V; ++s) part[r][s] = lo_of(yac[r][s]) + hi_of(yac[r][s]);
     }
 
     if constexpr (AGG) {
