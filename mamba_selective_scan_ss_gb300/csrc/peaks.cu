@@ -126,11 +126,50 @@ __global__ void k_ffma2(float* out, int iters, float a, float b, ClockRec* rec) 
   out[blockIdx.x * blockDim.x + threadIdx.x] = s;
 }
 
+// The pipe mix of one state update with nothing else: per chain step two
+// packed FFMA2 (the four FP32 lane-ops of an update on a state pair count as
+// two instructions per update) and one MUFU ex2, in independent chains.  The
+// rate it reaches is the ceiling of any kernel whose updates cost one ex2 and
+// four FP32 lane-ops, before loads, row work or bookkeeping.
+__global__ void k_mix(float* out, int iters, float a, float b, ClockRec* rec) {
+  unsigned long long x[kChains], w[kChains];
+  float e[kChains];
+#pragma unroll
+  for (int j = 0; j < kChains; ++j) {
+    x[j] = pack2(1e-3f * (threadIdx.x + 7 * j), 2e-3f * (threadIdx.x + 5 * j));
+    w[j] = pack2(3e-3f * (threadIdx.x + 3 * j), 4e-3f * (threadIdx.x + 2 * j));
+    e[j] = 1e-3f * (threadIdx.x + 11 * j);
+  }
+  const unsigned long long A = pack2(a, a), B = pack2(b, b);
+  __syncthreads();
+  record_start(rec);
+  for (int i = 0; i < iters; ++i) {
+#pragma unroll
+    for (int j = 0; j < kChains; ++j) {
+      asm("fma.rn.f32x2 %0, %0, %1, %2;" : "+l"(x[j]) : "l"(A), "l"(B));
+      asm("fma.rn.f32x2 %0, %0, %1, %2;" : "+l"(w[j]) : "l"(A), "l"(B));
+      e[j] = ex2_approx(-e[j]);
+    }
+  }
+  float s = 0.f;
+#pragma unroll
+  for (int j = 0; j < kChains; ++j) {
+    float lo, hi, lo2, hi2;
+    unpack2(x[j], lo, hi);
+    unpack2(w[j], lo2, hi2);
+    s += lo + hi + lo2 + hi2 + e[j];
+  }
+  record_end(rec);
+  out[blockIdx.x * blockDim.x + threadIdx.x] = s;
+}
+
 // The selective-scan update body with every operand on chip.  Per time step a
 // thread owning one channel row and all 16 states does, for each state n,
 //   a = 2^(dt*A2[n]); h[n] = a*h[n] + du*B[n]; y += C[n]*h[n]
 // with dt, du and the B/C rows read from shared memory as the real kernel
-// does.  kPacked selects the scalar or the packed f32x2 form of the FP32 work.
+// does.  kPacked = false: one row and all 16 states per thread, scalar FP32,
+// `steps` time steps.  kPacked = true: the scan kernel's own layout (below),
+// `steps` vectors of 8 time steps.
 template <bool kPacked>
 __global__ void k_update(float* out, int steps, ClockRec* rec) {
   constexpr int N = 16;
@@ -182,47 +221,80 @@ __global__ void k_update(float* out, int steps, ClockRec* rec) {
 #pragma unroll
     for (int n = 0; n < N; ++n) ysum += h[n];
   } else {
-    unsigned long long h[N / 2], A2p[N / 2];
+    // the scan kernel's lane layout: two rows x 8 states per lane as f32x2
+    // state pairs, dt/du of both rows per 8-step vector, B/C quads of the
+    // lane's states per step, states outer and steps inner
+    constexpr int V = 8, G = 8;
+    const int nl0 = (threadIdx.x & 1) * G;
+    unsigned long long h[2][G / 2], A2p[2][G / 2];
 #pragma unroll
-    for (int p = 0; p < N / 2; ++p) {
-      h[p] = 0ull;
-      A2p[p] = pack2(A2[2 * p], A2[2 * p + 1]);
-    }
-    for (int s = 0; s < steps; ++s) {
-      const int t = s & (T - 1);
-      const float dt = sDt[t][lane];
-      const float du = sDu[t][lane];
-      const unsigned long long dt2 = pack2(dt, dt), du2 = pack2(du, du);
-      unsigned long long y2 = 0ull;
+    for (int r = 0; r < 2; ++r)
 #pragma unroll
-      for (int q = 0; q < N / 4; ++q) {
-        const ulonglong2 b4 = *reinterpret_cast<const ulonglong2*>(&sB[t][4 * q]);
-        const ulonglong2 c4 = *reinterpret_cast<const ulonglong2*>(&sC[t][4 * q]);
-        const unsigned long long bb[2] = {b4.x, b4.y};
-        const unsigned long long cc[2] = {c4.x, c4.y};
+      for (int k = 0; k < G / 2; ++k) {
+        h[r][k] = 0ull;
+        A2p[r][k] = pack2(A2[nl0 + 2 * k] * (1 + r), A2[nl0 + 2 * k + 1] * (1 + r));
+      }
+    for (int j = 0; j < steps; ++j) {  // steps counts vectors of V steps here
+      const int jt = (j & (T / V - 1)) * V;
+      float dts[2][V], dus[2][V];
 #pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          const int p = 2 * q + r;
-          unsigned long long x2, c2;
-          asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(x2) : "l"(dt2), "l"(A2p[p]));
-          float x0, x1;
-          unpack2(x2, x0, x1);
-          const unsigned long long a2 = pack2(ex2_approx(x0), ex2_approx(x1));
-          asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(c2) : "l"(du2), "l"(bb[r]));
-          asm("fma.rn.f32x2 %0, %1, %0, %2;" : "+l"(h[p]) : "l"(a2), "l"(c2));
-          asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(y2) : "l"(cc[r]), "l"(h[p]));
+      for (int r = 0; r < 2; ++r)
+#pragma unroll
+        for (int q = 0; q < V; q += 4) {
+          const float4 a4 = *reinterpret_cast<const float4*>(&sDt[jt + r][(lane & 3) * 8 + q]);
+          const float4 b4 = *reinterpret_cast<const float4*>(&sDu[jt + r][(lane & 3) * 8 + q]);
+          dts[r][q] = a4.x; dts[r][q + 1] = a4.y; dts[r][q + 2] = a4.z; dts[r][q + 3] = a4.w;
+          dus[r][q] = b4.x; dus[r][q + 1] = b4.y; dus[r][q + 2] = b4.z; dus[r][q + 3] = b4.w;
+        }
+      unsigned long long yac[2][V];
+#pragma unroll
+      for (int r = 0; r < 2; ++r)
+#pragma unroll
+        for (int v = 0; v < V; ++v) yac[r][v] = 0ull;
+#pragma unroll
+      for (int k4 = 0; k4 < G / 4; ++k4) {
+#pragma unroll
+        for (int v = 0; v < V; ++v) {
+          const ulonglong2 b4 = *reinterpret_cast<const ulonglong2*>(&sB[jt + v][nl0 + 4 * k4]);
+          const ulonglong2 c4 = *reinterpret_cast<const ulonglong2*>(&sC[jt + v][nl0 + 4 * k4]);
+          const unsigned long long bb[2] = {b4.x, b4.y};
+          const unsigned long long cc[2] = {c4.x, c4.y};
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int k = 2 * k4 + e;
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+              unsigned long long x2, c2;
+              const unsigned long long dt2 = pack2(dts[r][v], dts[r][v]);
+              const unsigned long long du2 = pack2(dus[r][v], dus[r][v]);
+              asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(x2) : "l"(dt2), "l"(A2p[r][k]));
+              float x0, x1;
+              unpack2(x2, x0, x1);
+              const unsigned long long a2 = pack2(ex2_approx(x0), ex2_approx(x1));
+              asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(c2) : "l"(du2), "l"(bb[e]));
+              asm("fma.rn.f32x2 %0, %1, %0, %2;" : "+l"(h[r][k]) : "l"(a2), "l"(c2));
+              asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(yac[r][v]) : "l"(cc[e]), "l"(h[r][k]));
+            }
+          }
         }
       }
-      float lo, hi;
-      unpack2(y2, lo, hi);
-      ysum += lo + hi;
+#pragma unroll
+      for (int r = 0; r < 2; ++r)
+#pragma unroll
+        for (int v = 0; v < V; ++v) {
+          float lo, hi;
+          unpack2(yac[r][v], lo, hi);
+          ysum += lo + hi;
+        }
     }
 #pragma unroll
-    for (int p = 0; p < N / 2; ++p) {
-      float lo, hi;
-      unpack2(h[p], lo, hi);
-      ysum += lo + hi;
-    }
+    for (int r = 0; r < 2; ++r)
+#pragma unroll
+      for (int k = 0; k < G / 2; ++k) {
+        float lo, hi;
+        unpack2(h[r][k], lo, hi);
+        ysum += lo + hi;
+      }
   }
   record_end(rec);
   out[blockIdx.x * blockDim.x + threadIdx.x] = ysum;
@@ -231,7 +303,7 @@ __global__ void k_update(float* out, int steps, ClockRec* rec) {
 }  // namespace
 
 // which: 0 = ex2, 1 = ffma, 2 = ffma2 (packed), 3 = update body scalar,
-//        4 = update body packed.
+//        4 = update body packed, 5 = pipe mix of one update (2 FFMA2 + 1 ex2).
 // result[0] = lane-ops (or state updates) per second over the whole GPU
 // result[1] = lane-ops (or updates) per clock per SM
 // result[2] = mean SM clock during the run, MHz
@@ -264,6 +336,7 @@ extern "C" __attribute__((visibility("default"))) int ss_peaks_measure(int which
       case 2: k_ffma2<<<blocks, threads>>>(out, iters, 0.999f, 1e-3f, rec); break;
       case 3: k_update<false><<<blocks, threads>>>(out, iters, rec); break;
       case 4: k_update<true><<<blocks, threads>>>(out, iters, rec); break;
+      case 5: k_mix<<<blocks, threads>>>(out, iters, 0.999f, 1e-3f, rec); break;
       default: break;
     }
   };
@@ -288,9 +361,10 @@ extern "C" __attribute__((visibility("default"))) int ss_peaks_measure(int which
   if (cnt) mhz /= cnt;
   double per_thread = 0.0;
   switch (which) {
-    case 0: case 1: per_thread = (double)iters * kChains; break;
+    case 0: case 1: case 5: per_thread = (double)iters * kChains; break;
     case 2: per_thread = 2.0 * iters * kChains; break;
-    case 3: case 4: per_thread = 16.0 * iters; break;
+    case 3: per_thread = 16.0 * iters; break;
+    case 4: per_thread = 128.0 * iters; break;  // iters vectors of 8 steps x 16 updates
     default: break;
   }
   const double total = per_thread * blocks * threads;

@@ -85,14 +85,46 @@ int env_int(const char* name, int fallback) {
 
 int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 
+// Speed of one warp of the scan kernel relative to a warp alone on its
+// scheduler, against the warps sharing the scheduler: the SM's throughput
+// grows by half from one to two warps per scheduler and little beyond
+// (fitted to the kernel's measured times on GB300 for several chunk counts
+// of the decoupled workloads).
+double warp_speed(double w) {
+  if (w <= 1.0) return 1.0;
+  const double sm_rate = w <= 2.0 ? 1.0 + 0.5 * (w - 1.0)
+                                  : (w <= 8.0 ? 1.5 + 0.025 * (w - 2.0) : 1.65);
+  return sm_rate / w;
+}
+
+// Estimated duration, in step-times of a lone warp, of a decoupled launch with
+// chunks of len steps: units run in rounds of at most `slots` CTAs; a unit of
+// a split row makes two passes over its chunk (aggregate, then main), a whole
+// row one; each unit also pays a fixed cost (look-back, pipeline fill) of
+// kUnitOverheadSteps.
+constexpr double kUnitOverheadSteps = 64.0;
+double decoupled_makespan(int64_t tiles, int64_t seqlen, int64_t len, int64_t slots, int64_t nsm) {
+  const int64_t n = (seqlen + len - 1) / len;
+  const int64_t units = tiles * n;
+  const double unit_steps = (n > 1 ? 2.0 : 1.0) * (double)len + kUnitOverheadSteps;
+  const double warps_per_cta = kThreads / 32.0;
+  auto round_time = [&](int64_t ctas) {
+    const double w = (double)ctas / (double)nsm * warps_per_cta / 4.0;
+    return unit_steps / warp_speed(w);
+  };
+  const int64_t full = units / slots, last = units % slots;
+  return (double)full * round_time(slots) + (last > 0 ? round_time(last) : 0.0);
+}
+
 // Launch plan shared by ss_selective_scan_fwd and ss_selective_scan_plan.
 //
 // Vector path: one persistent kernel per state group with sms * ctas_per_sm
 // CTAs taking (row tile, chunk) units.  With at least as many row tiles as
 // CTAs, chunks are chained and cost nothing extra; they only give the
 // dynamic balance (about eight units per CTA).  With fewer row tiles than
-// CTAs the split over time is what provides the parallelism (about four
-// units per CTA), at the cost of an aggregate pass in each decoupled unit.
+// CTAs the split over time is what provides the parallelism, at the cost of
+// an aggregate pass in each decoupled unit; the chunk length is the one that
+// minimises decoupled_makespan.
 // Scalar path: aggregate, carry and main kernels over a fixed chunk grid.
 // SS_NCHUNKS and SS_CTAS_PER_SM override the heuristics (tuning aids).
 bool make_plan(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, int64_t elt,
@@ -124,10 +156,20 @@ bool make_plan(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, int64
     } else if (chain_per_sm >= 2 && seqlen >= 512) {
       slots = nsm * chain_per_sm;
       want = std::min<int64_t>((8 * slots + plan->tiles - 1) / plan->tiles, seqlen / 256);
-    } else if (2 * plan->tiles >= slots) {
-      want = 1;  // one wave of whole rows costs less than decoupled chunks
     } else {
-      want = std::min<int64_t>((4 * slots + plan->tiles - 1) / plan->tiles, seqlen / 128);
+      // decoupled (or one wave of whole rows): the shortest estimated makespan
+      const int64_t max_n = std::max<int64_t>(1, std::min<int64_t>(seqlen / ss::kTileSteps, kMaxChunks));
+      double best = 0.0;
+      want = 1;
+      for (int64_t n = 1; n <= max_n; ++n) {
+        const int64_t len = round_up((seqlen + n - 1) / n, ss::kTileSteps);
+        if ((seqlen + len - 1) / len != n) continue;  // same chunks as a smaller n
+        const double t = decoupled_makespan(plan->tiles, seqlen, len, slots, nsm);
+        if (n == 1 || t < best) {
+          best = t;
+          want = n;
+        }
+      }
     }
     plan->slots = slots;
     want = std::max<int64_t>(1, std::min<int64_t>({want, seqlen / ss::kTileSteps, kMaxChunks}));

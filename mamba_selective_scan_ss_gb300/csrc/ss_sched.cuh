@@ -18,9 +18,10 @@
 //  * decoupled (fewer row tiles than CTAs): every unit after the first of
 //    its tile computes its own aggregate (a pass without C, z or y) and
 //    publishes it, then looks back to the nearest predecessor whose end
-//    state is published and folds the aggregates in between forward, in
-//    chunk order; that gives its carry, it publishes its own end state
-//    P*carry + e at once and runs the main pass from the carry.
+//    state is published (one warp polls 32 predecessors at a time) and
+//    folds the aggregates in between forward, in chunk order; that gives
+//    its carry, it publishes its own end state P*carry + e at once and runs
+//    the main pass from the carry.
 // Both modes evaluate every carry by the same sequence of operations whatever
 // the timing, so results are bitwise reproducible from run to run.
 // Every wait polls with back-off and gives up after kSpinLimit polls: it then
@@ -41,6 +42,8 @@
 // kTileSteps steps are copied raw one tile ahead and widened/transposed to
 // [t][n] fp32 at the tile boundary (two barriers per tile).
 #pragma once
+
+#include <type_traits>
 
 #include "ss_fwd.cuh"
 
@@ -77,6 +80,39 @@ __device__ __forceinline__ unsigned wait_flag(const unsigned* flag, unsigned wan
     v = ld_acquire(flag);
   }
   return v;
+}
+
+// Decoupled look-back of unit (chunk k, tile) by one warp: lane i inspects
+// chunk base - i, so one poll covers 32 predecessors.  The search ends when
+// the nearest predecessor whose end state is published (flag kUnitIncl) and
+// every chunk after it have at least their aggregates published; a window of
+// aggregates only moves the search 32 chunks back.  Chunk 0 always publishes
+// its end state, so the search ends.  Returns j0 + 1 for the chunk j0 found,
+// or 0 after kSpinLimit polls (the device error word is then set).  Called by
+// all 32 lanes of one warp.
+__device__ __forceinline__ unsigned look_back(const unsigned* flags, int64_t M, int64_t tile,
+                                              int k, int lane) {
+  int base = k - 1;
+  long long polls = 0;
+  for (;;) {
+    const int j = base - lane;
+    const unsigned f = j >= 0 ? ld_acquire(&flags[(int64_t)j * M + tile]) : 0u;
+    const unsigned incl = __ballot_sync(0xffffffffu, j >= 0 && f >= kUnitIncl);
+    const unsigned ready = __ballot_sync(0xffffffffu, j < 0 || f >= kUnitAgg);
+    if (incl != 0u) {
+      const int fi = __ffs(incl) - 1;  // nearest published end state
+      const unsigned need = fi == 31 ? 0xffffffffu : (2u << fi) - 1u;
+      if ((ready & need) == need) return (unsigned)(base - fi) + 1u;
+    } else if (ready == 0xffffffffu) {
+      base -= 32;  // aggregates only: search further back
+      continue;
+    }
+    if (++polls > kSpinLimit) {
+      if (lane == 0) atomicOr(&g_ss_device_error, kErrTimeout);
+      return 0u;
+    }
+    __nanosleep(polls < 64 ? 32 : 256);
+  }
 }
 
 template <int TGS, int TPB>
@@ -478,16 +514,10 @@ __global__ void __launch_bounds__(TPB) ss_fwd_sched(const FwdParams p) {
       }
       __threadfence();
       __syncthreads();
-      if (tid == 0) {
-        st_release(&p.flags[(int64_t)k * M + tile], kUnitAgg);
-        // look back to the nearest predecessor whose end state is published
-        int j0 = k - 1;
-        unsigned f = 0;
-        for (;; --j0) {
-          f = wait_flag(&p.flags[(int64_t)j0 * M + tile], kUnitAgg);
-          if (f == 0u || f >= kUnitIncl || j0 == 0) break;
-        }
-        s_flag = (f >= kUnitIncl) ? (unsigned)j0 + 1u : 0u;  // 0: a wait gave up
+      if (tid < 32) {
+        if (tid == 0) st_release(&p.flags[(int64_t)k * M + tile], kUnitAgg);
+        const unsigned r = look_back(p.flags, M, tile, k, tid);
+        if (tid == 0) s_flag = r;  // 0: a wait gave up
       }
       __syncthreads();
       const unsigned found = s_flag;
@@ -506,16 +536,32 @@ __global__ void __launch_bounds__(TPB) ss_fwd_sched(const FwdParams p) {
           for (int kk = 0; kk < GP; ++kk)
             h[s][kk] = pack(__ldcg(&p.unit_incl[rec(j0, s, nl0 + 2 * kk)]),
                             __ldcg(&p.unit_incl[rec(j0, s, nl0 + 2 * kk + 1)]));
-        for (int jj = j0 + 1; jj < k; ++jj) {
+        // two chunks' records are loaded before either is applied, so their
+        // loads overlap; the fold itself stays in chunk order
+        auto fold = [&](int jj, auto count) {
+          constexpr int NC = decltype(count)::value;
+          float2 r[NC][2][GP][2];
 #pragma unroll
-          for (int s = 0; s < 2; ++s)
+          for (int c = 0; c < NC; ++c)
 #pragma unroll
-            for (int kk = 0; kk < GP; ++kk) {
-              const float2 r0 = __ldcg(&p.unit_agg[rec(jj, s, nl0 + 2 * kk)]);
-              const float2 r1 = __ldcg(&p.unit_agg[rec(jj, s, nl0 + 2 * kk + 1)]);
-              h[s][kk] = fma2(pack(r0.x, r1.x), h[s][kk], pack(r0.y, r1.y));
-            }
-        }
+            for (int s = 0; s < 2; ++s)
+#pragma unroll
+              for (int kk = 0; kk < GP; ++kk)
+#pragma unroll
+                for (int e = 0; e < 2; ++e)
+                  r[c][s][kk][e] = __ldcg(&p.unit_agg[rec(jj + c, s, nl0 + 2 * kk + e)]);
+#pragma unroll
+          for (int c = 0; c < NC; ++c)
+#pragma unroll
+            for (int s = 0; s < 2; ++s)
+#pragma unroll
+              for (int kk = 0; kk < GP; ++kk)
+                h[s][kk] = fma2(pack(r[c][s][kk][0].x, r[c][s][kk][1].x), h[s][kk],
+                                pack(r[c][s][kk][0].y, r[c][s][kk][1].y));
+        };
+        int jj = j0 + 1;
+        for (; jj + 1 < k; jj += 2) fold(jj, std::integral_constant<int, 2>{});
+        if (jj < k) fold(jj, std::integral_constant<int, 1>{});
       }
       // own end state = own aggregate applied to the carry, published before the main pass
       if (k + 1 < p.nchunks) {

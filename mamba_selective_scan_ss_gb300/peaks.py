@@ -16,11 +16,12 @@ PROBES = {
     "ffma": 1,            # scalar FP32 FMA lane-ops
     "ffma2": 2,           # packed f32x2 FMA lane-ops
     "update_scalar": 3,   # selective-scan state updates, scalar FP32 body
-    "update_packed": 4,   # selective-scan state updates, f32x2 body
+    "update_packed": 4,   # selective-scan state updates, the scan kernel's f32x2 lane layout
+    "update_mix": 5,      # pipe mix of one update (2 FFMA2 + 1 ex2), nothing else
 }
 
 DEFAULT_ITERS = {"ex2": 20000, "ffma": 40000, "ffma2": 20000,
-                 "update_scalar": 4000, "update_packed": 4000}
+                 "update_scalar": 4000, "update_packed": 500, "update_mix": 20000}
 
 
 def _lib():
@@ -48,3 +49,21 @@ def measure(probe: str, iters: int | None = None, blocks_per_sm: int = 4,
     return {"probe": probe, "per_s": res[0], "per_clk_per_sm": res[1],
             "sm_mhz": res[2], "sms": int(res[3]), "ms": res[4],
             "blocks_per_sm": blocks_per_sm, "threads": threads}
+
+
+def main() -> None:
+    """Print every probe as one JSON line, at 1, 2 and 8 warps per scheduler
+    for the update probes (occupancy scaling of the update body)."""
+    import json
+
+    runs = [("ex2", 4, 256), ("ffma", 4, 256), ("ffma2", 4, 256)]
+    for probe in ("update_mix", "update_packed", "update_scalar"):
+        runs += [(probe, 2, 64), (probe, 4, 64), (probe, 4, 256)]
+    for probe, bps, thr in runs:
+        r = measure(probe, blocks_per_sm=bps, threads=thr)
+        r["warps_per_scheduler"] = bps * thr / 32 / 4
+        print(json.dumps(r), flush=True)
+
+
+if __name__ == "__main__":
+    main()
