@@ -126,7 +126,9 @@ double decoupled_makespan(int64_t tiles, int64_t seqlen, int64_t len, int64_t sl
 // an aggregate pass in each decoupled unit; the chunk length is the one that
 // minimises decoupled_makespan.
 // Scalar path: aggregate, carry and main kernels over a fixed chunk grid.
-// SS_NCHUNKS and SS_CTAS_PER_SM override the heuristics (tuning aids).
+// SS_NCHUNKS and SS_CTAS_PER_SM override the heuristics (tuning aids);
+// SS_TEST_SKIP_UNITS (ss_selective_scan_fwd only) is the test hook that makes
+// the device-side waits run out.
 bool make_plan(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, int64_t elt,
                bool aligned16, int sms, LaunchPlan* plan) {
   plan->nt = dstate <= 4 ? 4 : (dstate <= 8 ? 8 : 16);
@@ -353,6 +355,18 @@ SS_API ss_status_t ss_selective_scan_fwd(
         return SS_ERR_CUDA;
       }
       p.ticket = reinterpret_cast<unsigned*>(base);
+      // test hook: the first SS_TEST_SKIP_UNITS units of every launch are
+      // never handed out, so their successors' bounded waits run out
+      const int skip = env_int("SS_TEST_SKIP_UNITS", 0);
+      if (skip > 0) {
+        for (int g = 0; g < plan.groups; ++g)
+          ss::ss_set_ticket<<<1, 1, 0, st>>>(
+              reinterpret_cast<unsigned*>(base + g * plan.sched_bytes_per_group), (unsigned)skip);
+        if (cudaGetLastError() != cudaSuccess) {
+          cudaFreeAsync(scratch, st);
+          return SS_ERR_CUDA;
+        }
+      }
       base += plan.sched_bytes;
     }
     if (plan.unit_agg_bytes) {

@@ -115,6 +115,11 @@ __device__ __forceinline__ unsigned look_back(const unsigned* flags, int64_t M, 
   }
 }
 
+// Test hook of the host (SS_TEST_SKIP_UNITS): start a launch's ticket counter
+// at `first`, so units below it are never handed out and the waits of their
+// successors run out (bounded; the device error word reports it).
+__global__ void ss_set_ticket(unsigned* ticket, unsigned first) { *ticket = first; }
+
 template <int TGS, int TPB>
 struct PairRows {
   static constexpr int kRowsPerCta = 2 * TPB / TGS;
