@@ -1,7 +1,7 @@
 """Benchmark of the selective-scan forward on GB300: state-updates/s and roofline.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload KEY]
+                    [--workload KEY] [--op fwd|decode]
 
 A step is one selective-scan forward (one ss_selective_scan_fwd call) over the
 workload's synthetic inputs, already resident in HBM.  The default workload is
@@ -16,6 +16,10 @@ whole-job throughput measured over the slowest rank.
 --impl reference times the CPU oracle (the plain fp64 C implementation the
 tests check against) on the host cores, on a bounded sample of the same
 workload, and prints the same metric.
+
+--op decode measures the one-token step instead (ss_selective_state_update,
+default workload: 64 sequences of a dim-5120, 16-state bf16 layer), with the
+state of every call taken from a rotating set larger than twice the L2.
 """
 from __future__ import annotations
 
@@ -44,7 +48,10 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=4000)
     ap.add_argument("--warmup", type=int, default=40)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="1", help="workload key (see inputs.WORKLOADS)")
+    ap.add_argument("--workload", default=None,
+                    help="workload key (inputs.WORKLOADS; with --op decode, inputs.DECODE_WORKLOADS)")
+    ap.add_argument("--op", choices=["fwd", "decode"], default="fwd",
+                    help="fwd: the forward scan (default); decode: one token per call")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-baseline-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -452,11 +459,192 @@ def run_ours(args, world, rank, local):
     print(json.dumps(line), flush=True)
 
 
+# ---------------------------------------------------------------- decode step
+DECODE_METRIC = "selective-scan decode state-updates/s (B*D*N per token) at 1 GB300; % of roofline"
+
+
+def run_decode(args, world, rank, local):
+    """One token per call (ss_selective_state_update): the state of each call is
+    a different buffer of a rotating set larger than 2x L2, as in a stack of
+    layers, so every call reads and writes its state in HBM."""
+    import torch
+    import mamba_selective_scan_ss_gb300 as ss
+    from mamba_selective_scan_ss_gb300 import _build
+    from mamba_selective_scan_ss_gb300.inputs import DECODE_WORKLOADS, make_decode_inputs
+
+    w = DECODE_WORKLOADS[args.workload]
+    inp = make_decode_inputs(w)
+    if args.impl == "reference":
+        if rank == 0:
+            r = decode_oracle_rate(w, inp, max(0.5, args.reference_seconds / 10))
+            print(json.dumps({
+                "metric": DECODE_METRIC, "value": r["value"], "unit": "state-updates/s",
+                "n_gpus": args.gpus, "steps": r["reps"], "warmup": 0,
+                "ms_per_step": 1e3 * r["seconds"] / r["reps"], "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "impl": "reference", "op": "decode",
+                "config": {"workload": w.name, "batch": w.batch, "dim": w.dim, "dstate": w.dstate,
+                           "io_dtype": w.dtype},
+                "cpu_baseline": {"value": r["value"], "unit": "state-updates/s",
+                                 "cores": r["cores"], "kind": "oracle", "sample": r["sample"]},
+                "e2e": {"value": r["value"], "unit": "state-updates/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}), flush=True)
+        return
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py: no CUDA device (the selective scan runs only on the GPU)")
+    if rank == 0:
+        _build.build_all()
+    barrier(world)
+    ss.load_library()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(dev)
+    nbytes = w.algorithmic_bytes()
+    nsets = int(math.ceil(2 * L2_BYTES / nbytes)) + 1
+    shared = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v)
+              for k, v in inp.items() if k in ("A", "D", "dt_bias")}
+    sets = []
+    for _ in range(nsets):
+        d = {k: v.to(dev) for k, v in inp.items()
+             if isinstance(v, torch.Tensor) and k not in shared}
+        d.update(shared)
+        d["y"] = torch.empty_like(d["x"])
+        sets.append(d)
+
+    def step(i):
+        d = sets[i % nsets]
+        ss.selective_state_update(d["state"], d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"],
+                                  d.get("z"), d["dt_bias"], True, y=d["y"], stream=stream)
+
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            step(i)
+    torch.cuda.synchronize(dev)
+    sampler = ClockSampler(gpu_id_for(dev.index))
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    sampler.start()
+    t_wall0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for i in range(args.steps):
+            step(i)
+        ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    t_wall = time.perf_counter() - t_wall0
+    clocks = sampler.stop()
+    barrier(world)
+    ms_max = max_over_ranks(ev0.elapsed_time(ev1), world)
+    ms_step = ms_max / args.steps
+    value = w.updates * args.steps * world / (ms_max * 1e-3)
+
+    # e2e: the token's inputs from pinned host memory, y back to it; the state
+    # stays resident on the device between tokens, as in serving
+    e2e = None
+    if args.e2e_steps > 0:
+        d = sets[0]
+        keys = [k for k in ("x", "dt", "B", "C", "z") if d.get(k) is not None]
+        host = {k: inp[k].pin_memory() for k in keys}
+        y_host = torch.empty(d["y"].shape, dtype=d["y"].dtype).pin_memory()
+        h2d = sum(v.numel() * v.element_size() for v in host.values())
+        d2h = y_host.numel() * y_host.element_size()
+
+        def e2e_step():
+            with torch.cuda.stream(stream):
+                for k, v in host.items():
+                    d[k].copy_(v, non_blocking=True)
+                ss.selective_state_update(d["state"], d["x"], d["dt"], d["A"], d["B"], d["C"],
+                                          d["D"], d.get("z"), d["dt_bias"], True, y=d["y"],
+                                          stream=stream)
+                y_host.copy_(d["y"], non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        e_ms = max_over_ranks(e0.elapsed_time(e1), world)
+        e2e = {"value": w.updates * args.e2e_steps * world / (e_ms * 1e-3),
+               "unit": "state-updates/s", "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(d2h), "ms_per_step": e_ms / args.e2e_steps}
+    if rank != 0:
+        return
+    pk = measured_peaks()
+    rates = unit_rates()
+    mhz = clocks["sm_mhz"] or rates["probe_mhz"]
+    t_hbm = nbytes / (pk["hbm_gbs"] * 1e9)
+    t_sfu = w.updates / (rates["ex2_per_clk_sm"] * rates["sms"] * mhz * 1e6)
+    t_step = ms_step * 1e-3
+    kernel_src = [REPO / "mamba_selective_scan_ss_gb300" / "csrc" / f
+                  for f in ("ss_decode.cuh", "ss_device.cuh", "ss_api.cu")]
+    traffic, traffic_src = traffic_record(kernel_src, w.name)
+    achieved = nbytes / t_step / 1e9
+    roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+            "frac": achieved / pk["hbm_gbs"], "peak_source": pk["source"],
+            "traffic": traffic, "traffic_source": traffic_src,
+            "algorithmic_bytes_per_step": nbytes, "updates_per_step": w.updates,
+            "t_hbm_us": t_hbm * 1e6, "t_sfu_us": t_sfu * 1e6, "measured_step_us": t_step * 1e6,
+            "scope": "one ss_selective_state_update call = 1 kernel"}
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        r = decode_oracle_rate(w, inp, min(args.cpu_baseline_seconds, 4.0))
+        cpu = {"value": r["value"], "unit": "state-updates/s", "cores": r["cores"],
+               "kind": "oracle", "sample": r["sample"]}
+    print(json.dumps({
+        "metric": DECODE_METRIC, "value": value, "unit": "state-updates/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic", "op": "decode",
+        "config": {"workload": w.name, "batch": w.batch, "dim": w.dim, "dstate": w.dstate,
+                   "io_dtype": w.dtype, "z_gate": w.has_z,
+                   "l2": f"{nsets} rotating state sets ({nsets * nbytes / 2**20:.0f} MiB > 2x L2)",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": int(args.steps), "clocks": clocks, "wall_s_timed_region": t_wall,
+    }), flush=True)
+
+
+def decode_oracle_rate(w, inp, budget_s: float) -> dict:
+    """The oracle's one-step forward from the state, repeated for about budget_s."""
+    import oracle
+
+    orc = oracle.default()
+
+    def col(v):
+        return None if v is None else v.unsqueeze(-1).contiguous()
+
+    args = (col(inp["x"]), col(inp["dt"]), inp["A"], col(inp["B"]), col(inp["C"]), inp["D"],
+            col(inp["z"]), inp["dt_bias"], True)
+    h0 = inp["state"].double().numpy()
+    cores = os.cpu_count() or 1
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        orc.fwd(*args, h0=h0, dtype=w.dtype, nthreads=cores)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    return {"value": w.updates * reps / el, "reps": reps, "seconds": el, "cores": cores,
+            "sample": f"{reps} full decode step(s) of the workload ({w.updates} updates each) "
+                      f"in {el:.1f} s"}
+
+
 def main():
     args = parse_args()
+    if args.workload is None:
+        args.workload = "decode_64" if args.op == "decode" else "1"
     world, rank, local = dist_setup(args)
     try:
-        if args.impl == "reference":
+        if args.op == "decode":
+            run_decode(args, world, rank, local)
+        elif args.impl == "reference":
             run_reference(args, world, rank)
         else:
             run_ours(args, world, rank, local)

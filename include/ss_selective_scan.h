@@ -104,6 +104,64 @@ SS_API ss_status_t ss_selective_scan_fwd(
     int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
     ss_dtype_t dtype, void* stream);
 
+/*
+ * ss_selective_scan_fwd_h0 -- the forward of ss_selective_scan_fwd started
+ * from a given state instead of zero: the recurrence of
+ * "从顺序到并行用PyTorch实现Blelloch算法加速Mamba状态空间模型" section 1 (the
+ * sequential form suited to inference) run over a new segment of a sequence
+ * whose earlier part ended in state h0.  Chaining calls with h0 = the previous
+ * call's last_state gives the same y and last_state as one call over the
+ * concatenated sequence (within the tolerances of the fp32 arithmetic).
+ *
+ * Arguments: those of ss_selective_scan_fwd, plus
+ *   h0         [batch, dim, dstate]      float32    state before step 0, or NULL (zero)
+ *
+ * last_state may be h0 itself (the state updated in place); any other
+ * overlap of an output with an input is SS_ERR_INVALID_ARGUMENT.  Validation,
+ * asynchrony, scratch, errors and limits are those of ss_selective_scan_fwd.
+ */
+SS_API ss_status_t ss_selective_scan_fwd_h0(
+    const void* u, const void* delta, const float* A, const void* B, const void* C,
+    const float* D, const void* z, const float* delta_bias, int delta_softplus,
+    const float* h0, void* y, float* last_state,
+    int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
+    ss_dtype_t dtype, void* stream);
+
+/*
+ * ss_selective_state_update -- one decode step (one token) of the selective
+ * scan for every (batch, channel), with the state updated in place: the
+ * token-by-token recurrent form that "从顺序到并行用PyTorch实现Blelloch算法加速Mamba
+ * 状态空间模型" section 1 names as the one for inference, with the step of
+ * "Mamba CUDA 实现解析" eq (4)-(7):
+ *   dt   = softplus(dt_raw + dt_bias)      (or dt_raw + dt_bias)
+ *   h[n] = exp(dt * A[d,n]) * h[n] + dt * B[b,n] * x
+ *   y    = (sum_n C[b,n] * h[n] + D[d] * x) * silu(z)
+ * It equals ss_selective_scan_fwd_h0 with seqlen = 1, h0 = last_state = state.
+ *
+ * Arguments (DEVICE pointers owned by the caller, dense, row-major):
+ *   state      [batch, dim, dstate]      float32    state, read and overwritten
+ *   x          [batch, dim]              dtype      token input (u of the scan)
+ *   dt         [batch, dim]              dtype      raw step size
+ *   A          [dim, dstate]             float32
+ *   B, C       [batch, dstate]           dtype      the token's projections
+ *   D          [dim]                     float32    or NULL (0)
+ *   z          [batch, dim]              dtype      gate input, or NULL (no gate)
+ *   dt_bias    [dim]                     float32    or NULL (0)
+ *   dt_softplus                          nonzero: softplus on dt_raw + dt_bias
+ *   y          [batch, dim]              dtype      output (written, never read)
+ *   batch, dim, dstate                   sizes >= 1; dstate <= 256
+ *   dtype, stream                        as for ss_selective_scan_fwd
+ *
+ * Behaviour: validated on the host (errors launch nothing and write
+ * nothing); one kernel is enqueued on `stream` and the call returns without
+ * synchronising.  It allocates no memory and has no device-side wait.  state
+ * and y must not overlap each other or any input.
+ */
+SS_API ss_status_t ss_selective_state_update(
+    float* state, const void* x, const void* dt, const float* A, const void* B, const void* C,
+    const float* D, const void* z, const float* dt_bias, int dt_softplus, void* y,
+    int64_t batch, int64_t dim, int64_t dstate, ss_dtype_t dtype, void* stream);
+
 /* Human-readable name of a status code (static storage, never NULL). */
 SS_API const char* ss_status_string(ss_status_t status);
 

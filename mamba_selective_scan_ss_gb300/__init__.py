@@ -6,10 +6,14 @@ library's CUDA kernels.  If the library has not been built, the functions
 raise: there is no fallback implementation.
 
 Low-level names mirror the C ABI exactly (raw device pointers as ints):
-    ss_selective_scan_fwd, ss_status_string, ss_selective_scan_check
-plus a convenience wrapper for torch CUDA tensors:
+    ss_selective_scan_fwd, ss_selective_scan_fwd_h0, ss_selective_state_update,
+    ss_status_string, ss_selective_scan_check, ss_selective_scan_plan,
+    ss_selective_scan_fwd_noalloc
+plus convenience wrappers for torch CUDA tensors:
     selective_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None,
-                       delta_softplus=True, ...)
+                       delta_softplus=True, h0=None, ...)
+    selective_state_update(state, x, dt, A, B, C, D=None, z=None, dt_bias=None,
+                           dt_softplus=True, y=None)
 """
 from __future__ import annotations
 
@@ -20,7 +24,8 @@ __all__ = [
     "SS_F32", "SS_BF16", "SS_OK", "SS_ERR_INVALID_ARGUMENT", "SS_ERR_UNSUPPORTED",
     "SS_ERR_CUDA", "SS_ERR_TIMEOUT", "SS_ERR_SCRATCH_LIMIT", "SelectiveScanError", "library_path", "load_library",
     "ss_selective_scan_fwd", "ss_status_string", "ss_selective_scan_check",
-    "ss_selective_scan_plan", "ss_selective_scan_fwd_noalloc", "selective_scan_fwd",
+    "ss_selective_scan_plan", "ss_selective_scan_fwd_noalloc", "ss_selective_scan_fwd_h0",
+    "ss_selective_state_update", "selective_scan_fwd", "selective_state_update",
 ]
 
 SS_F32, SS_BF16 = 0, 1
@@ -61,6 +66,13 @@ def load_library():
         lib.ss_selective_scan_check.argtypes = [vp]
         lib.ss_selective_scan_fwd_noalloc.restype = ctypes.c_int
         lib.ss_selective_scan_fwd_noalloc.argtypes = list(lib.ss_selective_scan_fwd.argtypes)
+        lib.ss_selective_scan_fwd_h0.restype = ctypes.c_int
+        lib.ss_selective_scan_fwd_h0.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_int,
+                                                 vp, vp, vp, i64, i64, i64, i64, ctypes.c_int, vp]
+        lib.ss_selective_state_update.restype = ctypes.c_int
+        lib.ss_selective_state_update.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                                  ctypes.c_int, vp, i64, i64, i64,
+                                                  ctypes.c_int, vp]
         lib.ss_selective_scan_plan.restype = ctypes.c_int
         lib.ss_selective_scan_plan.argtypes = [i64, i64, i64, i64, ctypes.c_int, ctypes.c_int,
                                                ctypes.c_int, ctypes.POINTER(_Plan)]
@@ -106,6 +118,22 @@ def ss_selective_scan_fwd_noalloc(u, delta, A, B, C, D, z, delta_bias, delta_sof
         batch, dim, dstate, seqlen, int(dtype), stream)
 
 
+def ss_selective_scan_fwd_h0(u, delta, A, B, C, D, z, delta_bias, delta_softplus, h0, y,
+                             last_state, batch, dim, dstate, seqlen, dtype, stream) -> int:
+    """The forward started from state h0 (fp32 [batch, dim, dstate], 0/None = zero)."""
+    return load_library().ss_selective_scan_fwd_h0(
+        u, delta, A, B, C, D, z, delta_bias, int(delta_softplus), h0, y, last_state,
+        batch, dim, dstate, seqlen, int(dtype), stream)
+
+
+def ss_selective_state_update(state, x, dt, A, B, C, D, z, dt_bias, dt_softplus, y,
+                              batch, dim, dstate, dtype, stream) -> int:
+    """One decode step; state (fp32 [batch, dim, dstate]) is updated in place."""
+    return load_library().ss_selective_state_update(
+        state, x, dt, A, B, C, D, z, dt_bias, int(dt_softplus), y, batch, dim, dstate,
+        int(dtype), stream)
+
+
 def ss_status_string(status: int) -> str:
     return load_library().ss_status_string(int(status)).decode()
 
@@ -118,52 +146,97 @@ def _ptr(t):
     return None if t is None else t.data_ptr()
 
 
+def _io_dtype(t):
+    import torch
+
+    if t.dtype == torch.float32:
+        return SS_F32
+    if t.dtype == torch.bfloat16:
+        return SS_BF16
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _check_tensors(ref, io, fp32):
+    import torch
+
+    for name, t in io:
+        if t is not None and t.dtype != ref.dtype:
+            raise TypeError(f"{name} must have dtype {ref.dtype}")
+    for name, t in fp32:
+        if t is not None and t.dtype != torch.float32:
+            raise TypeError(f"{name} must be float32")
+    for _, t in (*io, *fp32):
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError("all tensors must be contiguous CUDA tensors")
+
+
+def _stream(stream, device):
+    import torch
+
+    if stream is None:
+        return torch.cuda.current_stream(device).cuda_stream
+    return stream if isinstance(stream, int) else stream.cuda_stream
+
+
 def selective_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None,
                        delta_softplus: bool = True, return_last_state: bool = True,
-                       y=None, last_state=None, stream=None):
+                       y=None, last_state=None, stream=None, h0=None):
     """Run the forward on torch CUDA tensors in the ABI layouts.
 
     u, delta, z: [batch, dim, seqlen]; B, C: [batch, dstate, seqlen]; A:
     [dim, dstate] fp32; D, delta_bias: [dim] fp32.  u, delta, B, C, z share one
     dtype (float32 or bfloat16), which is also y's dtype.  Returns y, or
     (y, last_state) with last_state [batch, dim, dstate] fp32.  Outputs are
-    allocated with torch unless given.  Runs on ``stream`` (a torch.cuda.Stream
-    or a raw cudaStream_t int), default torch's current stream.
+    allocated with torch unless given.  h0 (fp32 [batch, dim, dstate]) is the
+    state before step 0 (default zero); last_state may be h0 itself.  Runs on
+    ``stream`` (a torch.cuda.Stream or a raw cudaStream_t int), default
+    torch's current stream.
     """
     import torch
 
-    if u.dtype == torch.float32:
-        dt = SS_F32
-    elif u.dtype == torch.bfloat16:
-        dt = SS_BF16
-    else:
-        raise TypeError(f"unsupported dtype {u.dtype}")
-    for name, t in (("delta", delta), ("B", B), ("C", C), ("z", z)):
-        if t is not None and t.dtype != u.dtype:
-            raise TypeError(f"{name} must have dtype {u.dtype}")
-    for name, t in (("A", A), ("D", D), ("delta_bias", delta_bias)):
-        if t is not None and t.dtype != torch.float32:
-            raise TypeError(f"{name} must be float32")
-    tensors = [u, delta, A, B, C, D, z, delta_bias]
-    for t in tensors:
-        if t is not None and (not t.is_cuda or not t.is_contiguous()):
-            raise ValueError("all tensors must be contiguous CUDA tensors")
+    dt = _io_dtype(u)
+    _check_tensors(u, (("u", u), ("delta", delta), ("B", B), ("C", C), ("z", z)),
+                   (("A", A), ("D", D), ("delta_bias", delta_bias), ("h0", h0)))
     batch, dim, seqlen = u.shape
     dstate = A.shape[1]
     if y is None:
         y = torch.empty_like(u)
     if last_state is None and return_last_state:
         last_state = torch.empty((batch, dim, dstate), device=u.device, dtype=torch.float32)
-    if stream is None:
-        s = torch.cuda.current_stream(u.device).cuda_stream
-    elif isinstance(stream, int):
-        s = stream
+    s = _stream(stream, u.device)
+    args = (_ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias),
+            delta_softplus)
+    outs = (_ptr(y), _ptr(last_state) if return_last_state else None,
+            batch, dim, dstate, seqlen, dt, s)
+    if h0 is None:
+        status = ss_selective_scan_fwd(*args, *outs)
     else:
-        s = stream.cuda_stream
-    status = ss_selective_scan_fwd(
-        _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias),
-        delta_softplus, _ptr(y), _ptr(last_state) if return_last_state else None,
-        batch, dim, dstate, seqlen, dt, s)
+        status = ss_selective_scan_fwd_h0(*args, _ptr(h0), *outs)
     if status != SS_OK:
-        raise SelectiveScanError(status)
+        raise SelectiveScanError(status, "ss_selective_scan_fwd" + ("" if h0 is None else "_h0"))
     return (y, last_state) if return_last_state else y
+
+
+def selective_state_update(state, x, dt, A, B, C, D=None, z=None, dt_bias=None,
+                           dt_softplus: bool = True, y=None, stream=None):
+    """One decode step on torch CUDA tensors; ``state`` is updated in place.
+
+    state: [batch, dim, dstate] fp32; x, dt, z: [batch, dim]; B, C: [batch,
+    dstate]; A: [dim, dstate] fp32; D, dt_bias: [dim] fp32.  x, dt, B, C, z
+    share one dtype (float32 or bfloat16), which is also y's.  Returns y.
+    """
+    import torch
+
+    io = _io_dtype(x)
+    _check_tensors(x, (("x", x), ("dt", dt), ("B", B), ("C", C), ("z", z)),
+                   (("state", state), ("A", A), ("D", D), ("dt_bias", dt_bias)))
+    batch, dim = x.shape
+    dstate = A.shape[1]
+    if y is None:
+        y = torch.empty_like(x)
+    status = ss_selective_state_update(
+        _ptr(state), _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
+        _ptr(dt_bias), dt_softplus, _ptr(y), batch, dim, dstate, io, _stream(stream, x.device))
+    if status != SS_OK:
+        raise SelectiveScanError(status, "ss_selective_state_update")
+    return y

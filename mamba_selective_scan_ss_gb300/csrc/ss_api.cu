@@ -13,6 +13,7 @@
 #include <algorithm>
 #include <mutex>
 
+#include "ss_decode.cuh"
 #include "ss_sched.cuh"
 #include "ss_selective_scan.h"
 
@@ -290,12 +291,17 @@ SS_API const char* ss_status_string(ss_status_t status) {
   }
 }
 
-SS_API ss_status_t ss_selective_scan_fwd(
-    const void* u, const void* delta, const float* A, const void* B, const void* C,
-    const float* D, const void* z, const float* delta_bias, int delta_softplus,
-    void* y, float* last_state,
-    int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
-    ss_dtype_t dtype, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// The forward from an initial state h0 (null: zero); both forward entry
+// points land here.
+ss_status_t fwd_impl(const void* u, const void* delta, const float* A, const void* B,
+                     const void* C, const float* D, const void* z, const float* delta_bias,
+                     int delta_softplus, const float* h0, void* y, float* last_state,
+                     int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
+                     ss_dtype_t dtype, void* stream) {
   // ---- validation: nothing is enqueued or written on error ----
   if (dtype != SS_F32 && dtype != SS_BF16) return SS_ERR_UNSUPPORTED;
   if (!u || !delta || !A || !B || !C || !y) return SS_ERR_INVALID_ARGUMENT;
@@ -309,15 +315,19 @@ SS_API ss_status_t ss_selective_scan_fwd(
   const uintptr_t ea = (uintptr_t)elt;
   if (!aligned(u, ea) || !aligned(delta, ea) || !aligned(B, ea) || !aligned(C, ea) ||
       !aligned(y, ea) || (z && !aligned(z, ea)) || !aligned(A, 4) || (D && !aligned(D, 4)) ||
-      (delta_bias && !aligned(delta_bias, 4)) || (last_state && !aligned(last_state, 4)))
+      (delta_bias && !aligned(delta_bias, 4)) || (last_state && !aligned(last_state, 4)) ||
+      (h0 && !aligned(h0, 4)))
     return SS_ERR_INVALID_ARGUMENT;
-  // outputs must not overlap any input, nor each other
-  const void* ins[] = {u, delta, B, C, z, A, D, delta_bias};
+  // outputs must not overlap any input, nor each other; last_state may be h0
+  // itself (the state updated in place)
+  const void* ins[] = {u, delta, B, C, z, A, D, delta_bias, h0};
   const int64_t in_bytes[] = {x_bytes, x_bytes, bc_bytes, bc_bytes, z ? x_bytes : 0,
-                              a_elems * 4, D ? dim * 4 : 0, delta_bias ? dim * 4 : 0};
-  for (int i = 0; i < 8; ++i) {
+                              a_elems * 4, D ? dim * 4 : 0, delta_bias ? dim * 4 : 0,
+                              h0 ? st_elems * 4 : 0};
+  for (int i = 0; i < 9; ++i) {
     if (range_overlap(y, x_bytes, ins[i], in_bytes[i])) return SS_ERR_INVALID_ARGUMENT;
-    if (last_state && range_overlap(last_state, st_elems * 4, ins[i], in_bytes[i]))
+    const bool in_place = i == 8 && last_state == h0;
+    if (last_state && !in_place && range_overlap(last_state, st_elems * 4, ins[i], in_bytes[i]))
       return SS_ERR_INVALID_ARGUMENT;
   }
   if (last_state && range_overlap(last_state, st_elems * 4, y, x_bytes))
@@ -335,6 +345,7 @@ SS_API ss_status_t ss_selective_scan_fwd(
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   ss::FwdParams p{};
   p.u = u; p.delta = delta; p.A = A; p.B = B; p.C = C; p.D = D; p.z = z; p.bias = delta_bias;
+  p.h0 = h0;
   p.y = y; p.last_state = last_state;
   p.batch = batch; p.dim = dim; p.dstate = dstate; p.seqlen = seqlen;
   p.chunk_len = plan.chunk_len;
@@ -393,6 +404,88 @@ SS_API ss_status_t ss_selective_scan_fwd(
     if (err == cudaSuccess && ferr != cudaSuccess) return SS_ERR_CUDA;
   }
   return err == cudaSuccess ? SS_OK : SS_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+SS_API ss_status_t ss_selective_scan_fwd(
+    const void* u, const void* delta, const float* A, const void* B, const void* C,
+    const float* D, const void* z, const float* delta_bias, int delta_softplus,
+    void* y, float* last_state,
+    int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
+    ss_dtype_t dtype, void* stream) {
+  return fwd_impl(u, delta, A, B, C, D, z, delta_bias, delta_softplus, nullptr, y, last_state,
+                  batch, dim, dstate, seqlen, dtype, stream);
+}
+
+SS_API ss_status_t ss_selective_scan_fwd_h0(
+    const void* u, const void* delta, const float* A, const void* B, const void* C,
+    const float* D, const void* z, const float* delta_bias, int delta_softplus,
+    const float* h0, void* y, float* last_state,
+    int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
+    ss_dtype_t dtype, void* stream) {
+  return fwd_impl(u, delta, A, B, C, D, z, delta_bias, delta_softplus, h0, y, last_state,
+                  batch, dim, dstate, seqlen, dtype, stream);
+}
+
+SS_API ss_status_t ss_selective_state_update(
+    float* state, const void* x, const void* dt, const float* A, const void* B, const void* C,
+    const float* D, const void* z, const float* dt_bias, int dt_softplus, void* y,
+    int64_t batch, int64_t dim, int64_t dstate, ss_dtype_t dtype, void* stream) {
+  // ---- validation: nothing is enqueued or written on error ----
+  if (dtype != SS_F32 && dtype != SS_BF16) return SS_ERR_UNSUPPORTED;
+  if (!state || !x || !dt || !A || !B || !C || !y) return SS_ERR_INVALID_ARGUMENT;
+  if (batch <= 0 || dim <= 0 || dstate <= 0) return SS_ERR_INVALID_ARGUMENT;
+  if (dstate > 256) return SS_ERR_UNSUPPORTED;
+  const int64_t elt = dtype == SS_F32 ? 4 : 2;
+  Sizes sz;  // one step: [b,d] rows, [b,N] B/C, [b,d,N] state
+  if (!sizes_ok(batch, dim, dstate, 1, elt, &sz)) return SS_ERR_UNSUPPORTED;
+  const uintptr_t ea = (uintptr_t)elt;
+  if (!aligned(x, ea) || !aligned(dt, ea) || !aligned(B, ea) || !aligned(C, ea) ||
+      !aligned(y, ea) || (z && !aligned(z, ea)) || !aligned(state, 4) || !aligned(A, 4) ||
+      (D && !aligned(D, 4)) || (dt_bias && !aligned(dt_bias, 4)))
+    return SS_ERR_INVALID_ARGUMENT;
+  const void* ins[] = {x, dt, B, C, z, A, D, dt_bias};
+  const int64_t in_bytes[] = {sz.x_bytes, sz.x_bytes, sz.bc_bytes, sz.bc_bytes,
+                              z ? sz.x_bytes : 0, sz.a_elems * 4, D ? dim * 4 : 0,
+                              dt_bias ? dim * 4 : 0};
+  for (int i = 0; i < 8; ++i) {
+    if (range_overlap(y, sz.x_bytes, ins[i], in_bytes[i])) return SS_ERR_INVALID_ARGUMENT;
+    if (range_overlap(state, sz.st_elems * 4, ins[i], in_bytes[i])) return SS_ERR_INVALID_ARGUMENT;
+  }
+  if (range_overlap(state, sz.st_elems * 4, y, sz.x_bytes)) return SS_ERR_INVALID_ARGUMENT;
+
+  ss::DecodeParams p{};
+  p.state = state; p.x = x; p.dt = dt; p.A = A; p.B = B; p.C = C; p.D = D; p.z = z;
+  p.bias = dt_bias; p.y = y;
+  p.dim = dim; p.dstate = dstate;
+  p.softplus = dt_softplus ? 1 : 0;
+  p.quads = (int)((dstate + 3) / 4);
+  // lanes per row: enough that no lane holds more than kDecodeQuads quads
+  p.seg_shift = 0;
+  while ((ss::kDecodeQuads << p.seg_shift) < p.quads) ++p.seg_shift;
+  const int64_t blocks_x = ((dim << p.seg_shift) + 255) / 256;
+  if (blocks_x > INT_MAX) return SS_ERR_UNSUPPORTED;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  (void)cudaGetLastError();
+  const int64_t bcv = dtype == SS_F32 ? 16 : 8;  // bytes of four B/C elements
+  const bool vec4 = dstate % 4 == 0 && aligned(state, 16) && aligned(A, 16) &&
+                    aligned(B, (uintptr_t)bcv) && aligned(C, (uintptr_t)bcv);
+  constexpr int64_t kMaxGridY = 65535;
+  for (int64_t b0 = 0; b0 < batch; b0 += kMaxGridY) {  // grid.y = batch rows
+    p.batch0 = b0;
+    const dim3 grid((unsigned)blocks_x, (unsigned)std::min(kMaxGridY, batch - b0));
+    if (dtype == SS_F32) {
+      if (vec4) ss::ss_state_update<float, true><<<grid, 256, 0, st>>>(p);
+      else ss::ss_state_update<float, false><<<grid, 256, 0, st>>>(p);
+    } else {
+      if (vec4) ss::ss_state_update<__nv_bfloat16, true><<<grid, 256, 0, st>>>(p);
+      else ss::ss_state_update<__nv_bfloat16, false><<<grid, 256, 0, st>>>(p);
+    }
+  }
+  return cudaGetLastError() == cudaSuccess ? SS_OK : SS_ERR_CUDA;
 }
 
 SS_API ss_status_t ss_selective_scan_plan(int64_t batch, int64_t dim, int64_t dstate,

@@ -46,6 +46,7 @@ struct FwdParams {
   const float* D;
   const void* z;
   const float* bias;
+  const float* h0;    // [b,d,N] state before step 0 (null: zero)
   void* y;
   float* last_state;
   float* y_partial;   // fp32 [rows, L]: read-out of earlier state groups (dstate > NT)
@@ -169,9 +170,12 @@ __global__ void __launch_bounds__(TPB) ss_fwd_main(const FwdParams p) {
       for (int k = 0; k < 2; ++k) {
         const int64_t n = n0 + 2 * q + k;
         a[k] = n < N ? p.A[rs.d[r] * N + n] * kLog2e : 0.f;
-        h0[k] = (chunk > 0 && n < N)
-                    ? p.carry[((int64_t)chunk * rows + rs.row[r]) * p.ns + n]
-                    : 0.f;
+        // a split row takes every chunk's carry from ss_chunk_carry (chunk 0's
+        // is h0), so h0 is read before this launch and may alias last_state;
+        // an unsplit row reads h0 here, in the thread that writes last_state
+        h0[k] = n >= N ? 0.f
+                : p.nchunks > 1 ? p.carry[((int64_t)chunk * rows + rs.row[r]) * p.ns + n]
+                : (p.h0 ? p.h0[rs.row[r] * N + n] : 0.f);
       }
       A2[r][q] = pack(a[0], a[1]);
       h[r][q] = pack(h0[0], h0[1]);
@@ -420,13 +424,15 @@ __global__ void __launch_bounds__(TPB) ss_chunk_aggregate(const FwdParams p) {
 
 // ---------------------------------------------------------------------------
 // Carry across chunks: for every (row, state) fold the chunk aggregates in
-// order, carry[k] = (P_{k-1}, e_{k-1}) applied to carry[k-1], carry[0] = 0.
+// order, carry[k] = (P_{k-1}, e_{k-1}) applied to carry[k-1], carry[0] = h0
+// (zero without an initial state).
 // One thread per (row, state); grid covers rows * ns.
 __global__ void ss_chunk_carry(const FwdParams p) {
   const int64_t rows = p.batch * p.dim;
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= rows * p.ns) return;
-  float h = 0.f;
+  const int64_t row = i / p.ns, n = i - row * p.ns;
+  float h = (p.h0 && n < p.dstate) ? p.h0[row * p.dstate + n] : 0.f;
   for (int k = 0; k < p.nchunks; ++k) {
     p.carry[(int64_t)k * rows * p.ns + i] = h;
     if (k + 1 < p.nchunks) {

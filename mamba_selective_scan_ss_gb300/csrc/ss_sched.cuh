@@ -455,6 +455,22 @@ __global__ void __launch_bounds__(TPB) ss_fwd_sched(const FwdParams p) {
         h[s][kk] = splat(0.f);
       }
     }
+    // the state before step 0 (chunk 0 only)
+    auto load_h0 = [&]() {
+#pragma unroll
+      for (int s = 0; s < 2; ++s)
+#pragma unroll
+        for (int kk = 0; kk < GP; ++kk) {
+          float v[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int64_t n = ng0 + nl0 + 2 * kk + e;
+            v[e] = (p.h0 && n < N) ? p.h0[rs.row[s] * N + n] : 0.f;
+          }
+          h[s][kk] = pack(v[0], v[1]);
+        }
+    };
+    if (k == 0) load_h0();
 
     // ---- carry into this unit ----
     bool published = false;  // this unit's end state already published
@@ -472,9 +488,11 @@ __global__ void __launch_bounds__(TPB) ss_fwd_sched(const FwdParams p) {
                             __ldcg(&p.unit_incl[rec(k - 1, s, nl0 + 2 * kk + 1)]));
       }
     } else if (k == 0 && !p.chained && p.nchunks > 1) {
-      // decoupled, first chunk: its carry is zero, so the state its aggregate
-      // pass reaches is its end state; publishing that before the main pass
-      // lets the look-backs of the later chunks finish early
+      // decoupled, first chunk: its carry is h0, so the state its first pass
+      // reaches from h0 is its end state; publishing that before the main
+      // pass lets the look-backs of the later chunks finish early.  h0 is read
+      // again for the main pass before the flag is released, so a successor
+      // that writes last_state over h0 (in-place update) cannot come first.
       scan_pass<T, NT, TGS, TPB, STAGES, true, HAS_Z, MULTI>(p, sm, rs, t_begin, t_end, h, A2, bias, Dd,
                                                dt_sum);
 #pragma unroll
@@ -485,8 +503,8 @@ __global__ void __launch_bounds__(TPB) ss_fwd_sched(const FwdParams p) {
           unpack(h[s][kk], hv[0], hv[1]);
           p.unit_incl[rec(0, s, nl0 + 2 * kk)] = hv[0];
           p.unit_incl[rec(0, s, nl0 + 2 * kk + 1)] = hv[1];
-          h[s][kk] = splat(0.f);
         }
+      load_h0();
       __threadfence();
       __syncthreads();
       if (tid == 0) st_release(&p.flags[tile], kUnitIncl);

@@ -120,3 +120,84 @@ def make_inputs(w: ScanWorkload) -> dict:
         "delta_softplus": bool(w.softplus),
     }
     return out
+
+
+# ---- decode step: one token from a given state -------------------------------
+@dataclass(frozen=True)
+class DecodeWorkload:
+    name: str
+    batch: int
+    dim: int
+    dstate: int
+    dtype: str = "bf16"
+    has_z: bool = True
+    has_D: bool = True
+    has_bias: bool = True
+    seed: int = 0
+
+    @property
+    def updates(self) -> int:
+        """State updates of one step: batch * dim * dstate."""
+        return self.batch * self.dim * self.dstate
+
+    @property
+    def elt(self) -> int:
+        return 4 if self.dtype == "f32" else 2
+
+    def algorithmic_bytes(self) -> int:
+        """State read and written once; x, dt, z read and y written once; B, C,
+        A, D and the bias read once."""
+        rows = self.batch * self.dim
+        streams = 3 + int(self.has_z)
+        b = 8 * rows * self.dstate
+        b += streams * rows * self.elt
+        b += 2 * self.batch * self.dstate * self.elt
+        b += 4 * self.dim * self.dstate
+        b += 4 * self.dim * (int(self.has_D) + int(self.has_bias))
+        return b
+
+
+DECODE_WORKLOADS = {
+    # one token of a Mamba-2.8B-shaped layer (dim 5120) for 64 sequences
+    "decode_64": DecodeWorkload("decode-b64-d5120-n16-bf16", 64, 5120, 16, "bf16", seed=7),
+    "decode_256": DecodeWorkload("decode-b256-d5120-n16-bf16", 256, 5120, 16, "bf16", seed=8),
+}
+
+
+def make_decode_inputs(w: DecodeWorkload) -> dict:
+    """One token's inputs and a state, on the CPU, in the C ABI layouts.
+
+    The forward's recipe restricted to one step: x, dt_raw, z ~ N(0, 1) [b, d];
+    dt ~ LogUniform[1e-3, 1e-1] per channel and dt_bias = log(expm1(dt));
+    A[d, n] = -(n + 1); B, C ~ N(0, 1) [b, N]; D ~ N(0, 1) [d]; the state
+    ~ N(0, 1) [b, d, N] fp32.  Draw order x, dt_raw, dt, B, C, D, z, state.
+    bf16 workloads round x, dt_raw, B, C and z to bf16 before either side sees
+    them.
+    """
+    g = torch.Generator(device="cpu")
+    g.manual_seed(w.seed)
+    b, d, n = w.batch, w.dim, w.dstate
+    io = torch.float32 if w.dtype == "f32" else torch.bfloat16
+    x = torch.randn((b, d), generator=g, dtype=torch.float32)
+    dt_raw = torch.randn((b, d), generator=g, dtype=torch.float32)
+    lo, hi = math.log(1e-3), math.log(1e-1)
+    dt = torch.exp(torch.rand((d,), generator=g, dtype=torch.float64) * (hi - lo) + lo)
+    Bm = torch.randn((b, n), generator=g, dtype=torch.float32)
+    Cm = torch.randn((b, n), generator=g, dtype=torch.float32)
+    D = torch.randn((d,), generator=g, dtype=torch.float32)
+    z = torch.randn((b, d), generator=g, dtype=torch.float32)
+    state = torch.randn((b, d, n), generator=g, dtype=torch.float32)
+    A = -torch.arange(1, n + 1, dtype=torch.float32).repeat(d, 1).contiguous()
+    bias = torch.log(torch.expm1(dt)).to(torch.float32)
+    return {
+        "state": state,
+        "x": x.to(io).contiguous(),
+        "dt": dt_raw.to(io).contiguous(),
+        "A": A,
+        "B": Bm.to(io).contiguous(),
+        "C": Cm.to(io).contiguous(),
+        "D": D if w.has_D else None,
+        "z": z.to(io).contiguous() if w.has_z else None,
+        "dt_bias": bias if w.has_bias else None,
+        "dt_softplus": True,
+    }

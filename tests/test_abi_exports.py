@@ -27,7 +27,8 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     assert declared_functions() == ["ss_selective_scan_check", "ss_selective_scan_fwd",
-                                    "ss_selective_scan_fwd_noalloc", "ss_selective_scan_plan",
+                                    "ss_selective_scan_fwd_h0", "ss_selective_scan_fwd_noalloc",
+                                    "ss_selective_scan_plan", "ss_selective_state_update",
                                     "ss_status_string"]
 
 
@@ -79,6 +80,47 @@ def test_validation_rejects_bad_arguments(lib):
     assert call(u=u + 1) == ss.SS_ERR_INVALID_ARGUMENT       # misaligned fp32 pointer
     assert call(A=A + 2) == ss.SS_ERR_INVALID_ARGUMENT
     assert call(u=u + 1, dtype=ss.SS_BF16) == ss.SS_ERR_INVALID_ARGUMENT  # odd bf16 address
+
+
+def test_validation_of_the_initial_state_entry_point(lib):
+    bufs, p = _fake_ptrs()
+    u, dl, A, B, C, D, z, bias, y, st, h0 = p
+    ok = dict(u=u, delta=dl, A=A, B=B, C=C, D=D, z=z, delta_bias=bias, delta_softplus=1, h0=h0,
+              y=y, last_state=st, batch=1, dim=2, dstate=4, seqlen=8, dtype=ss.SS_F32,
+              stream=None)
+
+    def call(**kw):
+        return ss.ss_selective_scan_fwd_h0(**dict(ok, **kw))
+
+    assert call(u=None) == ss.SS_ERR_INVALID_ARGUMENT
+    assert call(h0=h0 + 2) == ss.SS_ERR_INVALID_ARGUMENT       # misaligned fp32 state
+    assert call(y=h0) == ss.SS_ERR_INVALID_ARGUMENT            # output over the initial state
+    assert call(last_state=h0 + 4) == ss.SS_ERR_INVALID_ARGUMENT  # partial overlap (not in place)
+    assert call(last_state=u) == ss.SS_ERR_INVALID_ARGUMENT
+    assert call(dstate=300) == ss.SS_ERR_UNSUPPORTED
+    assert call(seqlen=0) == ss.SS_ERR_INVALID_ARGUMENT
+
+
+def test_validation_of_the_decode_step(lib):
+    bufs, p = _fake_ptrs()
+    state, x, dt, A, B, C, D, z, bias, y, _ = p
+    ok = dict(state=state, x=x, dt=dt, A=A, B=B, C=C, D=D, z=z, dt_bias=bias, dt_softplus=1,
+              y=y, batch=2, dim=3, dstate=4, dtype=ss.SS_F32, stream=None)
+
+    def call(**kw):
+        return ss.ss_selective_state_update(**dict(ok, **kw))
+
+    assert call(state=None) == ss.SS_ERR_INVALID_ARGUMENT
+    assert call(C=None) == ss.SS_ERR_INVALID_ARGUMENT
+    assert call(batch=0) == ss.SS_ERR_INVALID_ARGUMENT
+    assert call(dstate=257) == ss.SS_ERR_UNSUPPORTED
+    assert call(dtype=5) == ss.SS_ERR_UNSUPPORTED
+    assert call(batch=1 << 40, dim=1 << 30) == ss.SS_ERR_UNSUPPORTED
+    assert call(y=x) == ss.SS_ERR_INVALID_ARGUMENT             # output over an input
+    assert call(state=B) == ss.SS_ERR_INVALID_ARGUMENT         # state over an input
+    assert call(y=state + 8) == ss.SS_ERR_INVALID_ARGUMENT     # output over the state
+    assert call(state=state + 2) == ss.SS_ERR_INVALID_ARGUMENT  # misaligned fp32 state
+    assert call(x=x + 1, dtype=ss.SS_BF16) == ss.SS_ERR_INVALID_ARGUMENT
 
 
 def test_plan_is_host_only_and_consistent(lib, monkeypatch):
