@@ -12,6 +12,9 @@ Functions and the passages they follow:
     "Mamba CUDA 实现解析" eq (4)-(7); the Blelloch article's section 4.1.
   * ``Oracle.combine``  -- the associative operator of "Mamba CUDA 实现解析",
     eq (10).
+  * ``Oracle.bwd``      -- the exact derivative of ``fwd`` in reverse mode (the
+    backward that the Russian task spec asks to verify with gradcheck, Этап 3
+    step 4 and section 5; the Blelloch article, section 5.3).
 
 Parity status: pinned.  The pins (closed forms, the unrolled sum of eq (8) by
 brute force, composition under eq (10)-(12), special cases) live in
@@ -92,6 +95,9 @@ class Oracle:
             ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
             ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
             ctypes.c_int, ctypes.c_int]
+        lib.ss_oracle_bwd.restype = ctypes.c_int
+        lib.ss_oracle_bwd.argtypes = [ctypes.c_void_p] * 8 + [ctypes.c_int] + \
+            [ctypes.c_void_p] * 12 + [ctypes.c_int64] * 4 + [ctypes.c_int, ctypes.c_int]
         lib.ss_oracle_combine.restype = None
         lib.ss_oracle_combine.argtypes = [ctypes.c_void_p] * 6 + [ctypes.c_int64]
         self.lib = lib
@@ -129,6 +135,44 @@ class Oracle:
         if rc != 0:
             raise RuntimeError(f"ss_oracle_fwd failed with status {rc}")
         return y, last
+
+    def bwd(self, u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=True,
+            h0=None, dy=None, dlast=None, dtype: str = "f32", nthreads: int | None = None):
+        """Reverse-mode derivative of ``fwd`` for a loss with gradient dy on y
+        (and dlast on last_state); returns a dict of fp64 gradients: du,
+        ddelta, dA, dB, dC, dD, dz, dbias, dh0 (None for absent inputs)."""
+        u_, dl_, B_, C_, z_, dy_ = (_as_input(t, dtype) for t in (u, delta, B, C, z, dy))
+        A_ = _as_input(A, "f32")
+        D_ = _as_input(D, "f32")
+        bias_ = _as_input(delta_bias, "f32")
+        batch, dim, seqlen = u_.shape
+        dstate = A_.shape[1]
+        if dy_ is None or tuple(dy_.shape) != (batch, dim, seqlen):
+            raise ValueError("dy must have the shape of y")
+        h0_ = None if h0 is None else np.ascontiguousarray(h0, dtype=np.float64)
+        dl_last = None if dlast is None else np.ascontiguousarray(dlast, dtype=np.float64)
+        for name, arr in (("h0", h0_), ("dlast", dl_last)):
+            if arr is not None and arr.shape != (batch, dim, dstate):
+                raise ValueError(f"{name} has the wrong shape")
+        f64 = np.float64
+        out = {
+            "du": np.empty((batch, dim, seqlen), f64), "ddelta": np.empty((batch, dim, seqlen), f64),
+            "dA": np.empty((dim, dstate), f64), "dB": np.empty((batch, dstate, seqlen), f64),
+            "dC": np.empty((batch, dstate, seqlen), f64),
+            "dD": np.empty(dim, f64) if D_ is not None else None,
+            "dz": np.empty((batch, dim, seqlen), f64) if z_ is not None else None,
+            "dbias": np.empty(dim, f64) if bias_ is not None else None,
+            "dh0": np.empty((batch, dim, dstate), f64) if h0_ is not None else None,
+        }
+        nt = nthreads if nthreads is not None else (os.cpu_count() or 1)
+        rc = self.lib.ss_oracle_bwd(
+            _ptr(u_), _ptr(dl_), _ptr(A_), _ptr(B_), _ptr(C_), _ptr(D_), _ptr(z_), _ptr(bias_),
+            int(bool(delta_softplus)), _ptr(h0_), _ptr(dy_), _ptr(dl_last),
+            *(_ptr(out[k]) for k in ("du", "ddelta", "dA", "dB", "dC", "dD", "dz", "dbias", "dh0")),
+            batch, dim, dstate, seqlen, DTYPES[dtype], nt)
+        if rc != 0:
+            raise RuntimeError(f"ss_oracle_bwd failed with status {rc}")
+        return out
 
     def combine(self, a1, v1, a2, c2):
         """Elementwise (a1, v1) (+) (a2, c2) of eq (10); returns (a, v)."""

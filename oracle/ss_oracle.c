@@ -195,3 +195,204 @@ void ss_oracle_combine(const double* a1, const double* v1, const double* a2,
     v_out[i] = v;
   }
 }
+
+/* ---------------------------------------------------------------------------
+ * Backward pass: the exact derivative of ss_oracle_fwd, in reverse mode.
+ *
+ * The pages ask for a backward checked with gradcheck ("ТЕХНИЧЕСКОЕ ЗАДАНИЕ:
+ * Реализовать selective scan (Mamba)", Этап 3 step 4 and section 5, the
+ * acceptance criteria; the Blelloch article, section 5.3, a custom backward
+ * for autograd) but print no formulas for it.  What follows is the chain rule
+ * applied to the forward definition above, for a loss whose gradient with
+ * respect to y is dy (and, optionally, to last_state is dlast):
+ *   gate:     dy'_t = dy_t * silu(z_t),  dz_t = dy_t * y'_t * silu'(z_t)
+ *             silu'(z) = s (1 + z (1 - s)), s = 1 / (1 + e^-z)
+ *   skip:     dD += dy'_t u_t,  du_t += dy'_t D
+ *   read-out: dC[n,t] += dy'_t h_t[n];  g_t[n] = C[n,t] dy'_t + a_{t+1}[n] g_{t+1}[n]
+ *             (g_t = dL/dh_t; g after the last step is dlast)
+ *   update h_t = a_t h_{t-1} + dt_t B[n,t] u_t with a_t = exp(dt_t A[n]):
+ *             d(dt_t) += g_t[n] (A[n] a_t h_{t-1}[n] + B[n,t] u_t)
+ *             dA[n]   += g_t[n] dt_t a_t h_{t-1}[n]
+ *             dB[n,t] += g_t[n] dt_t u_t,   du_t += g_t[n] dt_t B[n,t]
+ *   step:     dx_t = d(dt_t) * (softplus ? sigmoid(x_t) : 1), x_t = delta_t + bias;
+ *             ddelta_t = dx_t, dbias += dx_t
+ *   initial:  dh0[n] = a_0[n] g_0[n]
+ * The forward states are recomputed and kept for the whole row.  Gradients of
+ * inputs shared between rows (dA, dB, dC, dD, dbias) are summed per thread and
+ * the per-thread sums added in thread order, so the result is deterministic.
+ * All outputs are double.  Optional outputs (dD, dz, dbias, dh0) may be NULL.
+ * ------------------------------------------------------------------------- */
+typedef struct {
+  const oracle_job* fwd;        /* inputs, sizes, dtype */
+  const void* dy;
+  const double* dlast;
+  double *du, *ddelta, *dz, *dh0;
+  double *dA, *dB, *dC, *dD, *dbias;  /* this thread's partial sums (zeroed) */
+  int status;
+} oracle_bwd_job;
+
+static void bwd_rows(oracle_bwd_job* j) {
+  const oracle_job* f = j->fwd;
+  const int64_t N = f->dstate, L = f->seqlen, dim = f->dim;
+  double* h = (double*)malloc(sizeof(double) * (size_t)(N * L));
+  double* a = (double*)malloc(sizeof(double) * (size_t)(N * L));
+  double* ypre = (double*)malloc(sizeof(double) * (size_t)L);
+  double* dtv = (double*)malloc(sizeof(double) * (size_t)L);
+  double* xv = (double*)malloc(sizeof(double) * (size_t)L);
+  double* g = (double*)malloc(sizeof(double) * (size_t)N);
+  if (!h || !a || !ypre || !dtv || !xv || !g) {
+    j->status = 2;
+    free(h); free(a); free(ypre); free(dtv); free(xv); free(g);
+    return;
+  }
+  for (int64_t row = f->row_begin; row < f->row_end; ++row) {
+    const int64_t d = row % dim, b = row / dim;
+    const double bias = f->bias ? (double)f->bias[d] : 0.0;
+    const double Dd = f->D ? (double)f->D[d] : 0.0;
+    /* forward, keeping every state */
+    for (int64_t t = 0; t < L; ++t) {
+      const int64_t xi = row * L + t;
+      const double u = load_elem(f->u, xi, f->dtype);
+      const double x = load_elem(f->delta, xi, f->dtype) + bias;
+      const double dt = f->softplus ? softplus(x) : x;
+      xv[t] = x;
+      dtv[t] = dt;
+      double yp = 0.0;
+      for (int64_t n = 0; n < N; ++n) {
+        const double prev = t > 0 ? h[(t - 1) * N + n] : (f->h0 ? f->h0[row * N + n] : 0.0);
+        const double an = exp(dt * (double)f->A[d * N + n]);
+        const double hn = an * prev + dt * load_elem(f->B, (b * N + n) * L + t, f->dtype) * u;
+        a[t * N + n] = an;
+        h[t * N + n] = hn;
+        yp += load_elem(f->C, (b * N + n) * L + t, f->dtype) * hn;
+      }
+      ypre[t] = yp + Dd * u;
+    }
+    /* reverse */
+    for (int64_t n = 0; n < N; ++n) g[n] = j->dlast ? j->dlast[row * N + n] : 0.0;
+    double dD = 0.0, dbias = 0.0;
+    for (int64_t t = L - 1; t >= 0; --t) {
+      const int64_t xi = row * L + t;
+      const double u = load_elem(f->u, xi, f->dtype);
+      const double dy = load_elem(j->dy, xi, f->dtype);
+      double dyp = dy;
+      if (f->z) {
+        const double zt = load_elem(f->z, xi, f->dtype);
+        const double s = 1.0 / (1.0 + exp(-zt));
+        dyp = dy * zt * s;
+        if (j->dz) j->dz[xi] = dy * ypre[t] * s * (1.0 + zt * (1.0 - s));
+      }
+      dD += dyp * u;
+      double du = dyp * Dd, ddt = 0.0;
+      const double dt = dtv[t];
+      for (int64_t n = 0; n < N; ++n) {
+        const double Bn = load_elem(f->B, (b * N + n) * L + t, f->dtype);
+        const double Cn = load_elem(f->C, (b * N + n) * L + t, f->dtype);
+        const double gn = Cn * dyp + g[n];              /* g[n] holds a_{t+1} g_{t+1} */
+        const double prev = t > 0 ? h[(t - 1) * N + n] : (f->h0 ? f->h0[row * N + n] : 0.0);
+        const double an = a[t * N + n];
+        const double An = (double)f->A[d * N + n];
+        j->dC[(b * N + n) * L + t] += dyp * h[t * N + n];
+        j->dB[(b * N + n) * L + t] += gn * dt * u;
+        j->dA[d * N + n] += gn * dt * an * prev;
+        ddt += gn * (An * an * prev + Bn * u);
+        du += gn * dt * Bn;
+        g[n] = an * gn;
+      }
+      const double dx = f->softplus ? ddt / (1.0 + exp(-xv[t])) : ddt;
+      j->ddelta[xi] = dx;
+      j->du[xi] = du;
+      dbias += dx;
+    }
+    if (j->dD) j->dD[d] += dD;
+    if (j->dbias) j->dbias[d] += dbias;
+    if (j->dh0)
+      for (int64_t n = 0; n < N; ++n) j->dh0[row * N + n] = g[n];
+  }
+  free(h); free(a); free(ypre); free(dtv); free(xv); free(g);
+}
+
+static void* bwd_thread_main(void* arg) {
+  bwd_rows((oracle_bwd_job*)arg);
+  return NULL;
+}
+
+/* Returns 0 on success, 1 on a bad argument, 2 on an allocation or thread
+ * failure.  Inputs as for ss_oracle_fwd plus dy (dtype, [b,d,L]) and dlast
+ * (double [b,d,N] or NULL).  Outputs (double): du, ddelta [b,d,L]; dA [d,N];
+ * dB, dC [b,N,L]; dD, dbias [d] (may be NULL); dz [b,d,L] (NULL when z is
+ * NULL); dh0 [b,d,N] (may be NULL). */
+int ss_oracle_bwd(const void* u, const void* delta, const float* A, const void* B,
+                  const void* C, const float* D, const void* z, const float* delta_bias,
+                  int delta_softplus, const double* h0, const void* dy, const double* dlast,
+                  double* du, double* ddelta, double* dA, double* dB, double* dC, double* dD,
+                  double* dz, double* dbias, double* dh0, int64_t batch, int64_t dim,
+                  int64_t dstate, int64_t seqlen, int dtype, int nthreads) {
+  if (!u || !delta || !A || !B || !C || !dy || !du || !ddelta || !dA || !dB || !dC) return 1;
+  if (batch <= 0 || dim <= 0 || dstate <= 0 || seqlen <= 0) return 1;
+  if (dtype != ORACLE_F32 && dtype != ORACLE_BF16) return 1;
+  const int64_t rows = batch * dim;
+  if (nthreads < 1) nthreads = 1;
+  if ((int64_t)nthreads > rows) nthreads = (int)rows;
+  const size_t nA = (size_t)(dim * dstate), nBC = (size_t)(batch * dstate * seqlen);
+  const size_t per = nA + 2 * nBC + 2 * (size_t)dim;
+
+  oracle_job* fj = (oracle_job*)calloc((size_t)nthreads, sizeof(oracle_job));
+  oracle_bwd_job* bj = (oracle_bwd_job*)calloc((size_t)nthreads, sizeof(oracle_bwd_job));
+  pthread_t* tids = (pthread_t*)calloc((size_t)nthreads, sizeof(pthread_t));
+  char* created = (char*)calloc((size_t)nthreads, 1);
+  double* partial = (double*)calloc((size_t)nthreads * per, sizeof(double));
+  int status = 0;
+  if (!fj || !bj || !tids || !created || !partial) {
+    status = 2;
+    goto done;
+  }
+  for (int i = 0; i < nthreads; ++i) {
+    oracle_job* f = &fj[i];
+    f->u = u; f->delta = delta; f->A = A; f->B = B; f->C = C; f->D = D; f->z = z;
+    f->bias = delta_bias; f->softplus = delta_softplus; f->h0 = h0;
+    f->batch = batch; f->dim = dim; f->dstate = dstate; f->seqlen = seqlen; f->dtype = dtype;
+    f->row_begin = rows * i / nthreads;
+    f->row_end = rows * (i + 1) / nthreads;
+    oracle_bwd_job* j = &bj[i];
+    double* base = partial + (size_t)i * per;
+    j->fwd = f; j->dy = dy; j->dlast = dlast;
+    j->du = du; j->ddelta = ddelta; j->dz = z ? dz : NULL; j->dh0 = dh0;
+    j->dA = base; j->dB = base + nA; j->dC = base + nA + nBC;
+    j->dD = D ? base + nA + 2 * nBC : NULL;
+    j->dbias = delta_bias ? base + nA + 2 * nBC + dim : NULL;
+    if (nthreads == 1) {
+      bwd_rows(j);
+    } else if (pthread_create(&tids[i], NULL, bwd_thread_main, j) == 0) {
+      created[i] = 1;
+    } else {
+      bwd_rows(j);
+    }
+  }
+  for (int i = 0; i < nthreads; ++i)
+    if (created[i]) pthread_join(tids[i], NULL);
+  for (int i = 0; i < nthreads; ++i)
+    if (bj[i].status) status = bj[i].status;
+  if (status == 0) {
+    /* per-thread sums, added in thread order */
+    memset(dA, 0, sizeof(double) * nA);
+    memset(dB, 0, sizeof(double) * nBC);
+    memset(dC, 0, sizeof(double) * nBC);
+    if (dD) memset(dD, 0, sizeof(double) * (size_t)dim);
+    if (dbias) memset(dbias, 0, sizeof(double) * (size_t)dim);
+    for (int i = 0; i < nthreads; ++i) {
+      const double* base = partial + (size_t)i * per;
+      for (size_t k = 0; k < nA; ++k) dA[k] += base[k];
+      for (size_t k = 0; k < nBC; ++k) dB[k] += base[nA + k];
+      for (size_t k = 0; k < nBC; ++k) dC[k] += base[nA + nBC + k];
+      if (dD)
+        for (int64_t k = 0; k < dim; ++k) dD[k] += D ? base[nA + 2 * nBC + k] : 0.0;
+      if (dbias)
+        for (int64_t k = 0; k < dim; ++k)
+          dbias[k] += delta_bias ? base[nA + 2 * nBC + dim + k] : 0.0;
+    }
+  }
+done:
+  free(fj); free(bj); free(tids); free(created); free(partial);
+  return status;
+}

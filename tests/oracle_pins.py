@@ -316,6 +316,62 @@ def pin_bf16_widening(orc, seed=21):
     assert np.array_equal(ya, yb) and np.array_equal(sa, sb)
 
 
+# --------------------------------------------------------------------------
+# The backward against finite differences of the forward.  The task spec asks
+# for the gradients to be verified with gradcheck (Этап 3 step 4, section 5);
+# here every gradient the oracle's backward returns is compared with central
+# differences of the oracle's forward (itself pinned above) for the loss
+# sum(dy * y) + sum(dlast * last_state).  Inputs are fp32, so each one is
+# moved to the neighbouring fp32 values v +- e (e a power of two, exact), and
+# two step sizes are combined by Richardson extrapolation, which leaves an
+# O(e^4) truncation error (about 1e-9 here); h0 is fp64 and moved the same way.
+def _fd_loss(orc, p, dy, dlast, softplus):
+    y, last = orc.fwd(**p, delta_softplus=softplus)
+    return float(np.sum(dy.astype(np.float64) * y) + np.sum(dlast * last))
+
+
+def _fd_grad(orc, p, key, idx, dy, dlast, softplus):
+    base = p[key]
+    def at(delta):
+        q = dict(p)
+        arr = base.copy()
+        arr[idx] = base[idx] + delta
+        q[key] = arr
+        return _fd_loss(orc, q, dy, dlast, softplus), float(arr[idx]) - float(base[idx])
+
+    def central(e):
+        lp, sp = at(e)
+        lm, sm = at(-e)
+        return (lp - lm) / (sp - sm)
+
+    e = 2.0 ** -7
+    return (4.0 * central(e / 2) - central(e)) / 3.0
+
+
+def pin_backward_finite_differences(orc, seed=22):
+    rng = np.random.default_rng(seed)
+    for softplus, z, D, bias in ((True, True, True, True), (False, False, False, False),
+                                 (True, False, True, False)):
+        b, d, n, L = 2, 2, 3, 4
+        p = _rand_problem(rng, b, d, n, L, z=z, D=D, bias=bias)
+        if not softplus:  # a positive step without softplus
+            p["delta"] = np.abs(p["delta"]).astype(np.float32) + np.float32(0.05)
+            p["delta_bias"] = None
+        p["h0"] = rng.standard_normal((b, d, n))
+        dy = rng.standard_normal((b, d, L)).astype(np.float32)
+        dlast = rng.standard_normal((b, d, n))
+        g = orc.bwd(**p, delta_softplus=softplus, dy=dy, dlast=dlast)
+        names = {"u": "du", "delta": "ddelta", "A": "dA", "B": "dB", "C": "dC", "D": "dD",
+                 "z": "dz", "delta_bias": "dbias", "h0": "dh0"}
+        for key, gname in names.items():
+            if p.get(key) is None:
+                assert g[gname] is None, f"{gname} returned for an absent input"
+                continue
+            fd = np.array([_fd_grad(orc, p, key, idx, dy, dlast, softplus)
+                           for idx in np.ndindex(p[key].shape)]).reshape(p[key].shape)
+            _close(g[gname], fd, rtol=1e-6, atol=1e-7, what=f"{gname} (softplus={softplus})")
+
+
 ALL_PINS = [
     pin_unrolled_sum,
     pin_zero_A_is_cumsum,
@@ -328,4 +384,5 @@ ALL_PINS = [
     pin_zero_B_or_C,
     pin_invariances,
     pin_bf16_widening,
+    pin_backward_finite_differences,
 ]

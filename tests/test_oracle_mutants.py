@@ -46,6 +46,18 @@ MUTANTS = {
                                "const double v = a1[i] * v1[i] + c2[i];"),
     "combine_product_wrong": ("const double a = a2[i] * a1[i];",
                               "const double a = a2[i] + a1[i] - 1.0;"),
+    # the backward
+    "bwd_carry_without_decay": ("        g[n] = an * gn;\n", "        g[n] = gn;\n"),
+    "bwd_sigmoid_of_dt_not_x": ("ddt / (1.0 + exp(-xv[t]))", "ddt / (1.0 + exp(-dtv[t]))"),
+    "bwd_dA_missing_dt": ("j->dA[d * N + n] += gn * dt * an * prev;",
+                          "j->dA[d * N + n] += gn * an * prev;"),
+    "bwd_silu_derivative_sign": ("s * (1.0 + zt * (1.0 - s))", "s * (1.0 - zt * (1.0 - s))"),
+    "bwd_dC_from_previous_state": ("j->dC[(b * N + n) * L + t] += dyp * h[t * N + n];",
+                                   "j->dC[(b * N + n) * L + t] += dyp * prev;"),
+    "bwd_du_without_skip": ("double du = dyp * Dd, ddt = 0.0;", "double du = 0.0, ddt = 0.0;"),
+    "bwd_dB_without_u": ("j->dB[(b * N + n) * L + t] += gn * dt * u;",
+                         "j->dB[(b * N + n) * L + t] += gn * dt;"),
+    "bwd_dlast_ignored": ("g[n] = j->dlast ? j->dlast[row * N + n] : 0.0;", "g[n] = 0.0;"),
 }
 
 
