@@ -162,6 +162,41 @@ SS_API ss_status_t ss_selective_state_update(
     const float* D, const void* z, const float* dt_bias, int dt_softplus, void* y,
     int64_t batch, int64_t dim, int64_t dstate, ss_dtype_t dtype, void* stream);
 
+/*
+ * ss_selective_scan_bwd -- the backward pass of ss_selective_scan_fwd: the
+ * gradients of every input for a loss whose gradient is dy on y (and
+ * dlast_state on last_state), which "ТЕХНИЧЕСКОЕ ЗАДАНИЕ: Реализовать
+ * selective scan (Mamba)" asks for and to verify with gradcheck (Этап 3
+ * step 4; section 5).  It is the chain rule through the forward's definition
+ * run backwards in time: g_t = C_t dy'_t + a_{t+1} g_{t+1} over the states,
+ * with the forward states recomputed from checkpoints.
+ *
+ * Inputs: those of ss_selective_scan_fwd (zero initial state), plus
+ *   dy          [batch, dim, seqlen]     dtype      gradient of y
+ *   dlast_state [batch, dim, dstate]     float32    gradient of last_state, or NULL (0)
+ * Outputs (written, never read):
+ *   du, ddelta  [batch, dim, seqlen]     dtype
+ *   dA          [dim, dstate]            float32
+ *   dB, dC      [batch, dstate, seqlen]  float32    summed over the channels
+ *   dD          [dim]                    float32    or NULL (not computed; ignored if D is NULL)
+ *   dz          [batch, dim, seqlen]     dtype      required when z is given, else ignored
+ *   dbias       [dim]                    float32    or NULL (ignored if delta_bias is NULL)
+ *
+ * Limits: dstate <= 16 (else SS_ERR_UNSUPPORTED).  Sums over channels, time
+ * and batch are evaluated in a fixed order: results are bitwise reproducible.
+ * Behaviour: validated on the host (errors launch nothing and write nothing);
+ * three kernels are enqueued on `stream` with stream-ordered scratch
+ * (cudaMallocAsync/cudaFreeAsync, about 8 bytes per (row, step) for the state
+ * checkpoints plus 128 bytes per 64-channel tile and step); no synchronisation
+ * and no device-side wait.  No output may overlap an input or another output.
+ */
+SS_API ss_status_t ss_selective_scan_bwd(
+    const void* u, const void* delta, const float* A, const void* B, const void* C,
+    const float* D, const void* z, const float* delta_bias, int delta_softplus,
+    const void* dy, const float* dlast_state, void* du, void* ddelta, float* dA, float* dB,
+    float* dC, float* dD, void* dz, float* dbias,
+    int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, ss_dtype_t dtype, void* stream);
+
 /* Human-readable name of a status code (static storage, never NULL). */
 SS_API const char* ss_status_string(ss_status_t status);
 

@@ -7,6 +7,7 @@ raise: there is no fallback implementation.
 
 Low-level names mirror the C ABI exactly (raw device pointers as ints):
     ss_selective_scan_fwd, ss_selective_scan_fwd_h0, ss_selective_state_update,
+    ss_selective_scan_bwd,
     ss_status_string, ss_selective_scan_check, ss_selective_scan_plan,
     ss_selective_scan_fwd_noalloc
 plus convenience wrappers for torch CUDA tensors:
@@ -14,6 +15,8 @@ plus convenience wrappers for torch CUDA tensors:
                        delta_softplus=True, h0=None, ...)
     selective_state_update(state, x, dt, A, B, C, D=None, z=None, dt_bias=None,
                            dt_softplus=True, y=None)
+    selective_scan_bwd(u, delta, A, B, C, D, z, delta_bias, delta_softplus, dy,
+                       dlast_state=None)
 """
 from __future__ import annotations
 
@@ -25,7 +28,8 @@ __all__ = [
     "SS_ERR_CUDA", "SS_ERR_TIMEOUT", "SS_ERR_SCRATCH_LIMIT", "SelectiveScanError", "library_path", "load_library",
     "ss_selective_scan_fwd", "ss_status_string", "ss_selective_scan_check",
     "ss_selective_scan_plan", "ss_selective_scan_fwd_noalloc", "ss_selective_scan_fwd_h0",
-    "ss_selective_state_update", "selective_scan_fwd", "selective_state_update",
+    "ss_selective_state_update", "ss_selective_scan_bwd", "selective_scan_fwd",
+    "selective_state_update", "selective_scan_bwd",
 ]
 
 SS_F32, SS_BF16 = 0, 1
@@ -73,6 +77,9 @@ def load_library():
         lib.ss_selective_state_update.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                                   ctypes.c_int, vp, i64, i64, i64,
                                                   ctypes.c_int, vp]
+        lib.ss_selective_scan_bwd.restype = ctypes.c_int
+        lib.ss_selective_scan_bwd.argtypes = [vp] * 8 + [ctypes.c_int] + [vp] * 10 + \
+            [i64, i64, i64, i64, ctypes.c_int, vp]
         lib.ss_selective_scan_plan.restype = ctypes.c_int
         lib.ss_selective_scan_plan.argtypes = [i64, i64, i64, i64, ctypes.c_int, ctypes.c_int,
                                                ctypes.c_int, ctypes.POINTER(_Plan)]
@@ -132,6 +139,15 @@ def ss_selective_state_update(state, x, dt, A, B, C, D, z, dt_bias, dt_softplus,
     return load_library().ss_selective_state_update(
         state, x, dt, A, B, C, D, z, dt_bias, int(dt_softplus), y, batch, dim, dstate,
         int(dtype), stream)
+
+
+def ss_selective_scan_bwd(u, delta, A, B, C, D, z, delta_bias, delta_softplus, dy, dlast_state,
+                          du, ddelta, dA, dB, dC, dD, dz, dbias, batch, dim, dstate, seqlen,
+                          dtype, stream) -> int:
+    """Direct call of the backward entry point; pointers are ints (0/None = NULL)."""
+    return load_library().ss_selective_scan_bwd(
+        u, delta, A, B, C, D, z, delta_bias, int(delta_softplus), dy, dlast_state, du, ddelta,
+        dA, dB, dC, dD, dz, dbias, batch, dim, dstate, seqlen, int(dtype), stream)
 
 
 def ss_status_string(status: int) -> str:
@@ -240,3 +256,37 @@ def selective_state_update(state, x, dt, A, B, C, D=None, z=None, dt_bias=None,
     if status != SS_OK:
         raise SelectiveScanError(status, "ss_selective_state_update")
     return y
+
+
+def selective_scan_bwd(u, delta, A, B, C, D=None, z=None, delta_bias=None,
+                       delta_softplus: bool = True, dy=None, dlast_state=None, stream=None):
+    """Gradients of the forward on torch CUDA tensors (zero initial state).
+
+    Returns a dict: du, ddelta (and dz) in the I/O dtype; dA [dim, dstate],
+    dB, dC [batch, dstate, seqlen], dD, dbias [dim] in float32 (None for an
+    absent input).  dy has y's shape and dtype; dlast_state (float32
+    [batch, dim, dstate]) is the gradient of last_state, default zero.
+    """
+    import torch
+
+    io = _io_dtype(u)
+    _check_tensors(u, (("u", u), ("delta", delta), ("B", B), ("C", C), ("z", z), ("dy", dy)),
+                   (("A", A), ("D", D), ("delta_bias", delta_bias), ("dlast_state", dlast_state)))
+    batch, dim, seqlen = u.shape
+    dstate = A.shape[1]
+    f32 = dict(device=u.device, dtype=torch.float32)
+    g = {"du": torch.empty_like(u), "ddelta": torch.empty_like(u),
+         "dA": torch.empty((dim, dstate), **f32),
+         "dB": torch.empty((batch, dstate, seqlen), **f32),
+         "dC": torch.empty((batch, dstate, seqlen), **f32),
+         "dD": torch.empty((dim,), **f32) if D is not None else None,
+         "dz": torch.empty_like(u) if z is not None else None,
+         "dbias": torch.empty((dim,), **f32) if delta_bias is not None else None}
+    status = ss_selective_scan_bwd(
+        _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias),
+        delta_softplus, _ptr(dy), _ptr(dlast_state),
+        *(_ptr(g[k]) for k in ("du", "ddelta", "dA", "dB", "dC", "dD", "dz", "dbias")),
+        batch, dim, dstate, seqlen, io, _stream(stream, u.device))
+    if status != SS_OK:
+        raise SelectiveScanError(status, "ss_selective_scan_bwd")
+    return g

@@ -13,6 +13,7 @@
 #include <algorithm>
 #include <mutex>
 
+#include "ss_bwd.cuh"
 #include "ss_decode.cuh"
 #include "ss_sched.cuh"
 #include "ss_selective_scan.h"
@@ -486,6 +487,95 @@ SS_API ss_status_t ss_selective_state_update(
     }
   }
   return cudaGetLastError() == cudaSuccess ? SS_OK : SS_ERR_CUDA;
+}
+
+SS_API ss_status_t ss_selective_scan_bwd(
+    const void* u, const void* delta, const float* A, const void* B, const void* C,
+    const float* D, const void* z, const float* delta_bias, int delta_softplus,
+    const void* dy, const float* dlast_state, void* du, void* ddelta, float* dA, float* dB,
+    float* dC, float* dD, void* dz, float* dbias,
+    int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, ss_dtype_t dtype, void* stream) {
+  // ---- validation: nothing is enqueued or written on error ----
+  if (dtype != SS_F32 && dtype != SS_BF16) return SS_ERR_UNSUPPORTED;
+  if (!u || !delta || !A || !B || !C || !dy || !du || !ddelta || !dA || !dB || !dC)
+    return SS_ERR_INVALID_ARGUMENT;
+  if (z && !dz) return SS_ERR_INVALID_ARGUMENT;
+  if (batch <= 0 || dim <= 0 || dstate <= 0 || seqlen <= 0) return SS_ERR_INVALID_ARGUMENT;
+  if (dstate > ss::kBwdLanes) return SS_ERR_UNSUPPORTED;
+  const int64_t elt = dtype == SS_F32 ? 4 : 2;
+  Sizes sz;
+  if (!sizes_ok(batch, dim, dstate, seqlen, elt, &sz)) return SS_ERR_UNSUPPORTED;
+  const int64_t dtiles = (dim + ss::kBwdRows - 1) / ss::kBwdRows;
+  const int64_t ctas = batch * dtiles;
+  const int64_t nblk = (seqlen + ss::kBwdBlock - 1) / ss::kBwdBlock;
+  int64_t ck_elems, bc_elems, tmp;
+  if (!mul_ok(ctas * ss::kBwdRows * ss::kBwdLanes, nblk, &ck_elems) ||
+      !mul_ok(ctas * 2 * ss::kBwdLanes, seqlen, &bc_elems) || !mul_ok(ck_elems + bc_elems, 4, &tmp) ||
+      ctas > INT_MAX)
+    return SS_ERR_UNSUPPORTED;
+  const uintptr_t ea = (uintptr_t)elt;
+  if (!aligned(u, ea) || !aligned(delta, ea) || !aligned(B, ea) || !aligned(C, ea) ||
+      !aligned(dy, ea) || !aligned(du, ea) || !aligned(ddelta, ea) || (z && !aligned(z, ea)) ||
+      (dz && !aligned(dz, ea)) || !aligned(A, 4) || (D && !aligned(D, 4)) ||
+      (delta_bias && !aligned(delta_bias, 4)) || (dlast_state && !aligned(dlast_state, 4)) ||
+      !aligned(dA, 4) || !aligned(dB, 4) || !aligned(dC, 4) || (dD && !aligned(dD, 4)) ||
+      (dbias && !aligned(dbias, 4)))
+    return SS_ERR_INVALID_ARGUMENT;
+  // outputs must not overlap any input, nor each other
+  const void* ins[] = {u, delta, A, B, C, D, z, delta_bias, dy, dlast_state};
+  const int64_t in_bytes[] = {sz.x_bytes, sz.x_bytes, sz.a_elems * 4, sz.bc_bytes, sz.bc_bytes,
+                              D ? dim * 4 : 0, z ? sz.x_bytes : 0, delta_bias ? dim * 4 : 0,
+                              sz.x_bytes, dlast_state ? sz.st_elems * 4 : 0};
+  const void* outs[] = {du, ddelta, dz, dA, dB, dC, dD, dbias};
+  const int64_t out_bytes[] = {sz.x_bytes, sz.x_bytes, dz ? sz.x_bytes : 0, sz.a_elems * 4,
+                               sz.bc_bytes / elt * 4, sz.bc_bytes / elt * 4, dD ? dim * 4 : 0,
+                               dbias ? dim * 4 : 0};
+  for (int o = 0; o < 8; ++o) {
+    for (int i = 0; i < 10; ++i)
+      if (range_overlap(outs[o], out_bytes[o], ins[i], in_bytes[i])) return SS_ERR_INVALID_ARGUMENT;
+    for (int k = o + 1; k < 8; ++k)
+      if (range_overlap(outs[o], out_bytes[o], outs[k], out_bytes[k])) return SS_ERR_INVALID_ARGUMENT;
+  }
+
+  // ---- scratch: checkpoints, per-CTA dB/dC sums, per-row dA/dD/dbias sums ----
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int64_t a_elems = batch * dim * ss::kBwdLanes, dd_elems = batch * dim * 2;
+  const int64_t scratch = round_up(ck_elems * 4, 256) + round_up(bc_elems * 4, 256) +
+                          round_up(a_elems * 4, 256) + round_up(dd_elems * 4, 256);
+  (void)cudaGetLastError();
+  void* base = nullptr;
+  if (cudaMallocAsync(&base, (size_t)scratch, st) != cudaSuccess) return SS_ERR_CUDA;
+  char* cur = static_cast<char*>(base);
+  ss::BwdParams p{};
+  p.u = u; p.delta = delta; p.A = A; p.B = B; p.C = C; p.D = D; p.z = z; p.bias = delta_bias;
+  p.softplus = delta_softplus ? 1 : 0;
+  p.dy = dy; p.dlast = dlast_state; p.du = du; p.ddelta = ddelta; p.dz = dz;
+  p.dA = dA; p.dB = dB; p.dC = dC; p.dD = D ? dD : nullptr; p.dbias = delta_bias ? dbias : nullptr;
+  p.ckpt = reinterpret_cast<float*>(cur);
+  cur += round_up(ck_elems * 4, 256);
+  p.part_bc = reinterpret_cast<float*>(cur);
+  cur += round_up(bc_elems * 4, 256);
+  p.part_a = reinterpret_cast<float*>(cur);
+  cur += round_up(a_elems * 4, 256);
+  p.part_dd = reinterpret_cast<float*>(cur);
+  p.batch = batch; p.dim = dim; p.dstate = dstate; p.seqlen = seqlen;
+  p.dtiles = dtiles; p.nblk = nblk;
+  if (dtype == SS_F32) {
+    if (z) ss::ss_bwd_main<float, true><<<(unsigned)ctas, ss::kBwdThreads, 0, st>>>(p);
+    else ss::ss_bwd_main<float, false><<<(unsigned)ctas, ss::kBwdThreads, 0, st>>>(p);
+  } else {
+    if (z) ss::ss_bwd_main<__nv_bfloat16, true><<<(unsigned)ctas, ss::kBwdThreads, 0, st>>>(p);
+    else ss::ss_bwd_main<__nv_bfloat16, false><<<(unsigned)ctas, ss::kBwdThreads, 0, st>>>(p);
+  }
+  const int sms = std::max(1, sm_count());
+  const int64_t bc_total = batch * dstate * seqlen, rows_total = dim * dstate;
+  ss::ss_bwd_reduce_bc<<<(unsigned)std::min<int64_t>((bc_total + 255) / 256, 8 * sms), 256, 0,
+                         st>>>(p);
+  ss::ss_bwd_reduce_rows<<<(unsigned)std::min<int64_t>((rows_total + 255) / 256, 8 * sms), 256, 0,
+                           st>>>(p);
+  const cudaError_t err = cudaGetLastError();
+  const cudaError_t ferr = cudaFreeAsync(base, st);
+  return err == cudaSuccess && ferr == cudaSuccess ? SS_OK : SS_ERR_CUDA;
 }
 
 SS_API ss_status_t ss_selective_scan_plan(int64_t batch, int64_t dim, int64_t dstate,

@@ -26,7 +26,8 @@ def declared_functions():
 
 
 def test_header_declares_the_entry_points():
-    assert declared_functions() == ["ss_selective_scan_check", "ss_selective_scan_fwd",
+    assert declared_functions() == ["ss_selective_scan_bwd", "ss_selective_scan_check",
+                                    "ss_selective_scan_fwd",
                                     "ss_selective_scan_fwd_h0", "ss_selective_scan_fwd_noalloc",
                                     "ss_selective_scan_plan", "ss_selective_state_update",
                                     "ss_status_string"]
@@ -121,6 +122,28 @@ def test_validation_of_the_decode_step(lib):
     assert call(y=state + 8) == ss.SS_ERR_INVALID_ARGUMENT     # output over the state
     assert call(state=state + 2) == ss.SS_ERR_INVALID_ARGUMENT  # misaligned fp32 state
     assert call(x=x + 1, dtype=ss.SS_BF16) == ss.SS_ERR_INVALID_ARGUMENT
+
+
+def test_validation_of_the_backward(lib):
+    bufs = [ctypes.create_string_buffer(4096) for _ in range(19)]
+    p = [ctypes.addressof(b) for b in bufs]
+    names = ["u", "delta", "A", "B", "C", "D", "z", "delta_bias", "dy", "dlast_state", "du",
+             "ddelta", "dA", "dB", "dC", "dD", "dz", "dbias"]
+    ok = dict(zip(names, p), delta_softplus=1, batch=1, dim=2, dstate=4, seqlen=8,
+              dtype=ss.SS_F32, stream=None)
+
+    def call(**kw):
+        return ss.ss_selective_scan_bwd(**dict(ok, **kw))
+
+    assert call(dy=None) == ss.SS_ERR_INVALID_ARGUMENT
+    assert call(dB=None) == ss.SS_ERR_INVALID_ARGUMENT
+    assert call(dz=None) == ss.SS_ERR_INVALID_ARGUMENT          # z given, dz missing
+    assert call(dstate=17) == ss.SS_ERR_UNSUPPORTED             # backward: dstate <= 16
+    assert call(seqlen=0) == ss.SS_ERR_INVALID_ARGUMENT
+    assert call(dtype=3) == ss.SS_ERR_UNSUPPORTED
+    assert call(du=ok["u"]) == ss.SS_ERR_INVALID_ARGUMENT       # output over an input
+    assert call(dC=ok["dB"] + 8) == ss.SS_ERR_INVALID_ARGUMENT  # two outputs overlap
+    assert call(dA=ok["dA"] + 2) == ss.SS_ERR_INVALID_ARGUMENT  # misaligned fp32 output
 
 
 def test_plan_is_host_only_and_consistent(lib, monkeypatch):
