@@ -20,6 +20,9 @@ workload, and prints the same metric.
 --op decode measures the one-token step instead (ss_selective_state_update,
 default workload: 64 sequences of a dim-5120, 16-state bf16 layer), with the
 state of every call taken from a rotating set larger than twice the L2.
+
+--op bwd measures the backward pass (ss_selective_scan_bwd) on a forward
+workload (default: the Mamba-2.8B-shaped layer).
 """
 from __future__ import annotations
 
@@ -50,8 +53,9 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=None,
                     help="workload key (inputs.WORKLOADS; with --op decode, inputs.DECODE_WORKLOADS)")
-    ap.add_argument("--op", choices=["fwd", "decode"], default="fwd",
-                    help="fwd: the forward scan (default); decode: one token per call")
+    ap.add_argument("--op", choices=["fwd", "decode", "bwd"], default="fwd",
+                    help="fwd: the forward scan (default); decode: one token per call; "
+                         "bwd: the backward pass")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-baseline-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -611,6 +615,141 @@ def run_decode(args, world, rank, local):
     }), flush=True)
 
 
+BWD_METRIC = "selective-scan bwd state-updates/s (B*D*L*N/s) at 1 GB300; % of roofline"
+# algorithmic work of the backward per state update: one forward recompute
+# (1 ex2, 2 FP32 lane-ops) and the reverse step (1 ex2, 10 FP32 lane-ops: the
+# g update and the dC, dB, dA, d(dt) and du terms)
+BWD_EX2_PER_UPDATE, BWD_FP32_PER_UPDATE = 2, 12
+
+
+def run_bwd(args, world, rank, local):
+    """The backward on a forward workload: inputs and dy resident in HBM."""
+    import torch
+    import mamba_selective_scan_ss_gb300 as ss
+    from mamba_selective_scan_ss_gb300 import _build
+    from mamba_selective_scan_ss_gb300.inputs import WORKLOADS, make_inputs
+
+    w = WORKLOADS[args.workload]
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py: no CUDA device (the selective scan runs only on the GPU)")
+    if rank == 0:
+        _build.build_all()
+    barrier(world)
+    ss.load_library()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(dev)
+    inp = make_inputs(w)
+    d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    g = torch.Generator().manual_seed(w.seed + 1000)
+    dy = torch.randn(d["u"].shape, generator=g).to(d["u"].dtype).to(dev)
+    elt = w.elt
+    x_bytes = w.batch * w.dim * w.seqlen * elt
+    # u, delta, dy (+ z) read once; du, ddelta (+ dz) written once
+    nbytes = (3 + int(w.has_z)) * x_bytes + (2 + int(w.has_z)) * x_bytes
+    nbytes += 2 * w.batch * w.dstate * w.seqlen * (elt + 4)          # B, C in; dB, dC out (fp32)
+    nbytes += 2 * 4 * w.dim * w.dstate + 4 * 4 * w.dim               # A, dA; D, bias, dD, dbias
+
+    def step():
+        ss.selective_scan_bwd(d["u"], d["delta"], d["A"], d["B"], d["C"], d["D"], d["z"],
+                              d["delta_bias"], d["delta_softplus"], dy=dy, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    torch.cuda.synchronize(dev)
+    sampler = ClockSampler(gpu_id_for(dev.index))
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    sampler.start()
+    t_wall0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step()
+        ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    t_wall = time.perf_counter() - t_wall0
+    clocks = sampler.stop()
+    barrier(world)
+    ms_max = max_over_ranks(ev0.elapsed_time(ev1), world)
+    ms_step = ms_max / args.steps
+    value = w.updates * args.steps * world / (ms_max * 1e-3)
+    if rank != 0:
+        return
+    pk = measured_peaks()
+    rates = unit_rates()
+    mhz = clocks["sm_mhz"] or rates["probe_mhz"]
+    r_sfu = rates["ex2_per_clk_sm"] * rates["sms"] * mhz * 1e6
+    r_fp32 = rates["fp32_per_clk_sm"] * rates["sms"] * mhz * 1e6
+    t_hbm = nbytes / (pk["hbm_gbs"] * 1e9)
+    t_sfu = BWD_EX2_PER_UPDATE * w.updates / r_sfu
+    t_fp32 = BWD_FP32_PER_UPDATE * w.updates / r_fp32
+    t_step = ms_step * 1e-3
+    if t_hbm >= max(t_sfu, t_fp32):
+        achieved = nbytes / t_step / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / pk["hbm_gbs"], "peak_source": pk["source"]}
+    else:
+        alu_peak = w.updates / max(t_sfu, t_fp32)
+        roof = {"bound": "alu", "achieved": w.updates / t_step / 1e9, "peak": alu_peak / 1e9,
+                "unit": "Gupdate/s", "frac": max(t_sfu, t_fp32) / t_step,
+                "peak_source": (f"{BWD_EX2_PER_UPDATE} ex2 and {BWD_FP32_PER_UPDATE} fp32 "
+                                f"lane-ops per update at the probes' {rates['ex2_per_clk_sm']:.1f} "
+                                f"and {rates['fp32_per_clk_sm']:.1f} /clk/SM x {rates['sms']} SMs "
+                                f"x {mhz:.0f} MHz sampled")}
+    roof.update({"traffic": None, "algorithmic_bytes_per_step": nbytes,
+                 "updates_per_step": w.updates, "t_hbm_us": t_hbm * 1e6,
+                 "t_sfu_us": t_sfu * 1e6, "t_fp32_us": t_fp32 * 1e6,
+                 "measured_step_us": t_step * 1e6,
+                 "scope": "one ss_selective_scan_bwd call = 3 kernels"})
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        cpu = bwd_oracle_rate(w, inp, dy.cpu(), min(args.cpu_baseline_seconds, 8.0))
+    print(json.dumps({
+        "metric": BWD_METRIC, "value": value, "unit": "state-updates/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic", "op": "bwd",
+        "config": {"workload": w.name, "batch": w.batch, "dim": w.dim, "dstate": w.dstate,
+                   "seqlen": w.seqlen, "io_dtype": w.dtype, "z_gate": w.has_z,
+                   "l2": "inputs larger than L2" if 4 * x_bytes > 2 * L2_BYTES else
+                         "inputs partly L2-resident between calls",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": roof, "cpu_baseline": cpu, "e2e": None,
+        "gpu_launches": 3 * args.steps, "clocks": clocks, "wall_s_timed_region": t_wall,
+    }), flush=True)
+
+
+def bwd_oracle_rate(w, inp, dy, budget_s: float) -> dict:
+    """The oracle's backward on the first channels of every batch row, repeated."""
+    import oracle
+
+    orc = oracle.default()
+    ch = max(1, min(w.dim, int(4e6 // max(1, w.batch * w.seqlen * w.dstate))))
+    sub = {k: (v[:, :ch].contiguous() if k in ("u", "delta", "z") and v is not None else v)
+           for k, v in inp.items()}
+    sub["A"] = inp["A"][:ch].contiguous()
+    sub["D"] = None if inp["D"] is None else inp["D"][:ch].contiguous()
+    sub["delta_bias"] = None if inp["delta_bias"] is None else inp["delta_bias"][:ch].contiguous()
+    dys = dy[:, :ch].contiguous()
+    cores = os.cpu_count() or 1
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        orc.bwd(sub["u"], sub["delta"], sub["A"], sub["B"], sub["C"], sub["D"], sub["z"],
+                sub["delta_bias"], sub["delta_softplus"], dy=dys, dtype=w.dtype, nthreads=cores)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    upd = w.batch * ch * w.seqlen * w.dstate
+    return {"value": upd * reps / el, "unit": "state-updates/s", "cores": cores, "kind": "oracle",
+            "sample": f"{reps} backward pass(es) over the first {ch} of {w.dim} channels of every "
+                      f"batch row, full seqlen {w.seqlen}: {upd} updates each, {el:.1f} s"}
+
+
 def decode_oracle_rate(w, inp, budget_s: float) -> dict:
     """The oracle's one-step forward from the state, repeated for about budget_s."""
     import oracle
@@ -639,11 +778,16 @@ def decode_oracle_rate(w, inp, budget_s: float) -> dict:
 def main():
     args = parse_args()
     if args.workload is None:
-        args.workload = "decode_64" if args.op == "decode" else "1"
+        args.workload = {"decode": "decode_64", "bwd": "2"}.get(args.op, "1")
     world, rank, local = dist_setup(args)
     try:
         if args.op == "decode":
             run_decode(args, world, rank, local)
+        elif args.op == "bwd":
+            if args.impl == "reference":
+                raise SystemExit("bench.py: --op bwd has no reference arm; its cpu_baseline "
+                                 "times the oracle's backward")
+            run_bwd(args, world, rank, local)
         elif args.impl == "reference":
             run_reference(args, world, rank)
         else:

@@ -560,6 +560,18 @@ SS_API ss_status_t ss_selective_scan_bwd(
   p.part_dd = reinterpret_cast<float*>(cur);
   p.batch = batch; p.dim = dim; p.dstate = dstate; p.seqlen = seqlen;
   p.dtiles = dtiles; p.nblk = nblk;
+  p.vec = seqlen % (16 / elt) == 0 && aligned(u, 16) && aligned(delta, 16) && aligned(dy, 16) &&
+          (!z || aligned(z, 16));
+  // the backward is latency-bound: the whole shared memory for resident CTAs
+  static const bool carveout = [] {
+    for (auto k : {(const void*)ss::ss_bwd_main<float, true>, (const void*)ss::ss_bwd_main<float, false>,
+                   (const void*)ss::ss_bwd_main<__nv_bfloat16, true>,
+                   (const void*)ss::ss_bwd_main<__nv_bfloat16, false>})
+      cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    return true;
+  }();
+  (void)carveout;
+  (void)cudaGetLastError();
   if (dtype == SS_F32) {
     if (z) ss::ss_bwd_main<float, true><<<(unsigned)ctas, ss::kBwdThreads, 0, st>>>(p);
     else ss::ss_bwd_main<float, false><<<(unsigned)ctas, ss::kBwdThreads, 0, st>>>(p);

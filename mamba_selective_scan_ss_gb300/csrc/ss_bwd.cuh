@@ -12,22 +12,23 @@
 //   du_t = dy'_t D + sum_n g_t[n] dt_t B[n,t]
 //   ddelta_t = d(dt_t) sigmoid(delta_t + bias)   (1 without softplus),  dbias += ddelta_t
 //
-// Layout: one lane per (row, state), 16 lanes per row, so the sums over the
-// states of a row are butterflies of four shuffles and the sums of dB/dC over
-// the rows of a CTA start with one shuffle between the two rows of a warp.
-// A CTA holds 64 rows (1024 threads).
+// Layout: one thread per row with all (up to 16) states in registers, as in
+// the forward, so the row's scalars (dt, du, the gate) and its sums over the
+// states (d(dt), du, the pre-gate read-out) stay inside the thread.  A CTA
+// holds 64 rows; the B/C values of each block of kBwdBlock steps are staged
+// once in shared memory and read as broadcasts.  The one exchange between
+// threads is the sum of dB/dC over the CTA's rows, step by step: every thread
+// writes its 32 contributions to a padded table and 32 threads add its
+// columns in row order.
 //
 // Time: a forward pass stores the state every kBwdBlock steps (checkpoints in
 // scratch); the reverse pass then, block by block from the end, recomputes the
-// block's states and decays from its checkpoint into registers and runs the
-// reverse recurrence over them.  One lane per step computes dt (softplus) and
-// the step's scalars and broadcasts them to the row's lanes by shuffle.
+// block's states from its checkpoint into shared memory and runs the reverse
+// recurrence over them (decays recomputed with ex2).
 //
-// Reductions are deterministic: dB/dC are summed over the CTA's warps in shared
-// memory in a fixed order and written as per-CTA partials, which
-// ss_bwd_reduce_bc adds over the CTAs of a batch in order; dA, dD and dbias
-// are written per (batch, channel) and ss_bwd_reduce_rows adds them over the
-// batch in order.
+// Reductions are deterministic: dB/dC per CTA in row order, then
+// ss_bwd_reduce_bc over the CTAs of a batch row in order; dA, dD and dbias
+// per (batch, channel), then ss_bwd_reduce_rows over the batch in order.
 #pragma once
 
 #include "ss_device.cuh"
@@ -35,9 +36,9 @@
 namespace ss {
 
 constexpr int kBwdBlock = 8;       // steps per recomputed block (and checkpoint spacing)
-constexpr int kBwdRows = 64;       // rows per CTA
-constexpr int kBwdLanes = 16;      // lanes (states) per row
-constexpr int kBwdThreads = kBwdRows * kBwdLanes;
+constexpr int kBwdRows = 64;       // rows per CTA (one thread each)
+constexpr int kBwdLanes = 16;      // states per group (dstate <= 16)
+constexpr int kBwdThreads = kBwdRows;
 
 struct BwdParams {
   const void* u;
@@ -54,7 +55,7 @@ struct BwdParams {
   void* du;             // [b,d,L] dtype
   void* ddelta;         // [b,d,L] dtype
   void* dz;             // [b,d,L] dtype (z present)
-  float* ckpt;          // [ctas][64][nblk][16] states at the end of each block
+  float* ckpt;          // [ctas][nblk][16][64] states at the end of each block
   float* part_bc;       // [ctas][2][16][L] per-CTA sums of dB, dC
   float* part_a;        // [b][d][16] per-row sums of dA
   float* part_dd;       // [b][d][2] per-row sums of dD, dbias
@@ -66,183 +67,205 @@ struct BwdParams {
   int64_t batch, dim, dstate, seqlen;
   int64_t dtiles;       // CTAs per batch row: ceil(dim / 64)
   int64_t nblk;         // ceil(seqlen / kBwdBlock)
+  int vec;              // rows 16-byte aligned: a block's row values load as 16-byte vectors
 };
+
+// Steps [t0, t0 + kBwdBlock) of one row as floats: 16-byte loads when the
+// block is whole and the row aligned (vec), else one element at a time.
+template <typename T>
+__device__ __forceinline__ void load_block(const T* row, int64_t t0, int cnt, bool vec,
+                                           float (&out)[kBwdBlock]) {
+  constexpr int V = Elem<T>::kVec;  // elements per 16 bytes (4 or 8)
+  if (vec && cnt == kBwdBlock) {
+#pragma unroll
+    for (int q = 0; q < kBwdBlock / V; ++q) {
+      const Vec16<T> v = *reinterpret_cast<const Vec16<T>*>(row + t0 + q * V);
+#pragma unroll
+      for (int e = 0; e < V; ++e) out[q * V + e] = Elem<T>::to_f32(v.e[e]);
+    }
+  } else {
+#pragma unroll
+    for (int st = 0; st < kBwdBlock; ++st) out[st] = st < cnt ? Elem<T>::to_f32(row[t0 + st]) : 0.f;
+  }
+}
 
 __device__ __forceinline__ float sigmoid_f(float x) { return rcp_approx(1.f + ex2(-x * kLog2e)); }
 
 template <typename T, bool HAS_Z>
-__global__ void __launch_bounds__(kBwdThreads, 1) ss_bwd_main(const BwdParams p) {
-  __shared__ float red[kBwdBlock][kBwdThreads / 32][2][kBwdLanes];
+__global__ void __launch_bounds__(kBwdThreads, 6) ss_bwd_main(const BwdParams p) {
+  constexpr int S = kBwdBlock, NT = kBwdLanes;
+  __shared__ float bc[2][S][NT];                 // B, C of the block's steps
+  __shared__ float hp[S][NT][kBwdRows];          // state before each step of the block
+  __shared__ float red[kBwdRows][2 * NT + 1];    // one step's dC (0..15), dB (16..31) per row
 
   const int tid = threadIdx.x;
-  const int warp = tid >> 5, lane = tid & 31;
-  const int half = lane & 16;                // 0 or 16: the row's lanes within the warp
-  const int n = lane & 15;                   // state of this lane; also the step it serves
-  const int rloc = warp * 2 + (lane >> 4);   // row within the CTA
   const int64_t cta = blockIdx.x;
   const int64_t b = cta / p.dtiles;
-  const int64_t d = (cta - b * p.dtiles) * kBwdRows + rloc;
+  const int64_t d = (cta - b * p.dtiles) * kBwdRows + tid;
   const bool valid = d < p.dim;
   const int64_t dc = valid ? d : p.dim - 1;
   const int64_t L = p.seqlen, N = p.dstate;
   const int64_t row = b * p.dim + dc;
-  const bool has_n = n < N;
 
-  const T* __restrict__ ug = static_cast<const T*>(p.u);
-  const T* __restrict__ dg = static_cast<const T*>(p.delta);
-  const T* __restrict__ zg = static_cast<const T*>(p.z);
-  const T* __restrict__ yg = static_cast<const T*>(p.dy);
-  const T* __restrict__ Bn = static_cast<const T*>(p.B) + (b * N + (has_n ? n : 0)) * L;
-  const T* __restrict__ Cn = static_cast<const T*>(p.C) + (b * N + (has_n ? n : 0)) * L;
-  const float An = has_n ? p.A[dc * N + n] : 0.f;
-  const float A2 = An * kLog2e;
+  const T* __restrict__ ug = static_cast<const T*>(p.u) + row * L;
+  const T* __restrict__ dg = static_cast<const T*>(p.delta) + row * L;
+  const T* __restrict__ zg = static_cast<const T*>(p.z) + row * L;
+  const T* __restrict__ yg = static_cast<const T*>(p.dy) + row * L;
+  const T* __restrict__ Bg = static_cast<const T*>(p.B) + b * N * L;
+  const T* __restrict__ Cg = static_cast<const T*>(p.C) + b * N * L;
+  float A2[NT];
+#pragma unroll
+  for (int n = 0; n < NT; ++n) A2[n] = n < N ? p.A[dc * N + n] * kLog2e : 0.f;
   const float bias = p.bias ? p.bias[dc] : 0.f;
   const float Dd = p.D ? p.D[dc] : 0.f;
-  float* __restrict__ ck = p.ckpt + ((cta * kBwdRows + rloc) * p.nblk) * kBwdLanes + n;
-
-  auto load_b = [&](int64_t t) { return has_n ? Elem<T>::to_f32(Bn[t]) : 0.f; };
-  auto load_c = [&](int64_t t) { return has_n ? Elem<T>::to_f32(Cn[t]) : 0.f; };
-  // dt of the step this lane serves (lane n serves step t0 + n of the block)
-  auto step_dt = [&](int64_t t, float& x, float& dtv) {
-    x = Elem<T>::to_f32(dg[row * L + t]) + bias;
-    dtv = p.softplus ? lo_of(softplus2(splat(x))) : x;
+  auto ck = [&](int64_t blk, int n) -> float& {
+    return p.ckpt[((cta * p.nblk + blk) * NT + n) * kBwdRows + tid];
   };
+  // B (and C) of steps [t0, t0 + cnt) into shared memory, zero past dstate
+  auto stage = [&](int64_t t0, int cnt, int tensors) {
+    for (int i = tid; i < tensors * NT * S; i += kBwdThreads) {
+      const int m = i / (NT * S), n = (i / S) % NT, st = i % S;
+      const T* src = m == 0 ? Bg : Cg;
+      bc[m][st][n] = (st < cnt && n < N) ? Elem<T>::to_f32(src[(int64_t)n * L + t0 + st]) : 0.f;
+    }
+  };
+  const bool vec = p.vec != 0;
+  auto dt_of = [&](float x) { return p.softplus ? lo_of(softplus2(splat(x))) : x; };
 
   // ---- forward: checkpoints at the end of every block but the last ----
-  float h = 0.f;
-  for (int64_t blk = 0; blk < p.nblk; ++blk) {
-    const int64_t t0 = blk * kBwdBlock;
-    const int cnt = (int)min((int64_t)kBwdBlock, L - t0);
-    float my_dt = 0.f, my_du = 0.f;
-    if (n < cnt) {
-      float x, dtv;
-      step_dt(t0 + n, x, dtv);
-      my_dt = dtv;
-      my_du = dtv * Elem<T>::to_f32(ug[row * L + t0 + n]);
-    }
+  {
+    float h[NT];
 #pragma unroll
-    for (int s = 0; s < kBwdBlock; ++s) {
-      if (s < cnt) {
-        const float dts = __shfl_sync(0xffffffffu, my_dt, half | s);
-        const float dus = __shfl_sync(0xffffffffu, my_du, half | s);
-        h = fmaf(ex2(dts * A2), h, dus * load_b(t0 + s));
+    for (int n = 0; n < NT; ++n) h[n] = 0.f;
+    for (int64_t blk = 0; blk < p.nblk; ++blk) {
+      const int64_t t0 = blk * S;
+      const int cnt = (int)min((int64_t)S, L - t0);
+      stage(t0, cnt, 1);
+      float xs[S], us[S];
+      load_block<T>(dg, t0, cnt, vec, xs);
+      load_block<T>(ug, t0, cnt, vec, us);
+      __syncthreads();
+#pragma unroll
+      for (int st = 0; st < S; ++st) {
+        if (st < cnt) {
+          const float dtv = dt_of(xs[st] + bias);
+          const float du = dtv * us[st];
+#pragma unroll
+          for (int n = 0; n < NT; ++n) h[n] = fmaf(ex2(dtv * A2[n]), h[n], du * bc[0][st][n]);
+        }
       }
+      if (blk + 1 < p.nblk) {
+#pragma unroll
+        for (int n = 0; n < NT; ++n) ck(blk, n) = h[n];
+      }
+      __syncthreads();  // bc is restaged by the next block
     }
-    if (blk + 1 < p.nblk) ck[blk * kBwdLanes] = h;
   }
 
   // ---- reverse, block by block ----
-  float g = (valid && has_n && p.dlast) ? p.dlast[row * N + n] : 0.f;
-  float dA_acc = 0.f, dD_acc = 0.f, dbias_acc = 0.f;
+  float g[NT], dA_acc[NT];
+#pragma unroll
+  for (int n = 0; n < NT; ++n) {
+    g[n] = (valid && n < N && p.dlast) ? p.dlast[row * N + n] : 0.f;
+    dA_acc[n] = 0.f;
+  }
+  float dD_acc = 0.f, dbias_acc = 0.f;
   for (int64_t blk = p.nblk - 1; blk >= 0; --blk) {
-    const int64_t t0 = blk * kBwdBlock;
-    const int cnt = (int)min((int64_t)kBwdBlock, L - t0);
-    // the scalars of step t0 + n, on lane n of the row
-    float my_x = 0.f, my_dt = 0.f, my_u = 0.f, my_dyp = 0.f, my_dy = 0.f, my_z = 0.f, my_sig = 0.f;
-    if (n < cnt) {
-      const int64_t t = t0 + n;
-      step_dt(t, my_x, my_dt);
-      my_u = Elem<T>::to_f32(ug[row * L + t]);
-      my_dy = valid ? Elem<T>::to_f32(yg[row * L + t]) : 0.f;
-      my_dyp = my_dy;
+    const int64_t t0 = blk * S;
+    const int cnt = (int)min((int64_t)S, L - t0);
+    stage(t0, cnt, 2);
+    // the row's scalars of the block's steps
+    float xs[S], dts[S], us[S], dys[S], zs[S];
+    load_block<T>(dg, t0, cnt, vec, xs);
+    load_block<T>(ug, t0, cnt, vec, us);
+    load_block<T>(yg, t0, cnt, vec, dys);
+    if (HAS_Z) load_block<T>(zg, t0, cnt, vec, zs);
+#pragma unroll
+    for (int st = 0; st < S; ++st) {
+      xs[st] += bias;
+      dts[st] = dt_of(xs[st]);
+      if (!valid) dys[st] = 0.f;
+      if (!HAS_Z) zs[st] = 0.f;
+    }
+    __syncthreads();
+    // recompute the block's states from its checkpoint
+    {
+      float h[NT];
+#pragma unroll
+      for (int n = 0; n < NT; ++n) h[n] = blk > 0 ? ck(blk - 1, n) : 0.f;
+#pragma unroll
+      for (int st = 0; st < S; ++st) {
+        if (st < cnt) {
+          const float du = dts[st] * us[st];
+#pragma unroll
+          for (int n = 0; n < NT; ++n) {
+            hp[st][n][tid] = h[n];
+            h[n] = fmaf(ex2(dts[st] * A2[n]), h[n], du * bc[0][st][n]);
+          }
+        }
+      }
+    }
+    // reverse over the block's steps
+#pragma unroll
+    for (int st = S - 1; st >= 0; --st) {
+      if (st >= cnt) continue;
+      const int64_t t = t0 + st;
+      float dyp = dys[st], sig = 0.f;
       if (HAS_Z) {
-        my_z = Elem<T>::to_f32(zg[row * L + t]);
-        my_sig = sigmoid_f(my_z);
-        my_dyp = my_dy * my_z * my_sig;
+        sig = sigmoid_f(zs[st]);
+        dyp = dys[st] * zs[st] * sig;
       }
-    }
-    // recompute the block's states and decays from its checkpoint
-    float hs = blk > 0 ? ck[(blk - 1) * kBwdLanes] : 0.f;
-    float hp[kBwdBlock], av[kBwdBlock];
+      const float dtv = dts[st], u = us[st], du = dtv * u;
+      float ddt_a[2] = {0.f, 0.f}, ddt_b[2] = {0.f, 0.f}, dsum[2] = {0.f, 0.f},
+            ysum[2] = {0.f, 0.f};
 #pragma unroll
-    for (int s = 0; s < kBwdBlock; ++s) {
-      hp[s] = hs;
-      av[s] = 1.f;
-      if (s < cnt) {
-        const float dts = __shfl_sync(0xffffffffu, my_dt, half | s);
-        const float us = __shfl_sync(0xffffffffu, my_u, half | s);
-        av[s] = ex2(dts * A2);
-        hs = fmaf(av[s], hs, dts * us * load_b(t0 + s));
+      for (int n = 0; n < NT; ++n) {
+        const float prev = hp[st][n][tid];
+        const float a = ex2(dtv * A2[n]);
+        const float bb = bc[0][st][n], cc = bc[1][st][n];
+        const float ap = a * prev;
+        const float ht = fmaf(du, bb, ap);
+        const float gn = fmaf(cc, dyp, g[n]);
+        const float gd = gn * dtv;
+        red[tid][n] = dyp * ht;           // dC
+        red[tid][NT + n] = gd * u;        // dB
+        dA_acc[n] = fmaf(gd, ap, dA_acc[n]);
+        ddt_a[n & 1] = fmaf(gn * A2[n], ap, ddt_a[n & 1]);
+        ddt_b[n & 1] = fmaf(gn, bb, ddt_b[n & 1]);
+        dsum[n & 1] = fmaf(gd, bb, dsum[n & 1]);
+        ysum[n & 1] = fmaf(cc, ht, ysum[n & 1]);
+        g[n] = a * gn;
       }
-    }
-    float out_ddt = 0.f, out_du = 0.f, out_yp = 0.f;
-#pragma unroll
-    for (int s = kBwdBlock - 1; s >= 0; --s) {
-      if (s < cnt) {
-        const int64_t t = t0 + s;
-        const float dts = __shfl_sync(0xffffffffu, my_dt, half | s);
-        const float us = __shfl_sync(0xffffffffu, my_u, half | s);
-        const float dyp = __shfl_sync(0xffffffffu, my_dyp, half | s);
-        const float bb = load_b(t), cc = load_c(t);
-        const float prev = hp[s], a = av[s];
-        const float ht = s + 1 < cnt ? hp[s + 1] : hs;   // state after step t
-        const float gn = fmaf(cc, dyp, g);
-        const float cC = dyp * ht;
-        const float cB = gn * dts * us;
-        dA_acc = fmaf(gn * dts, a * prev, dA_acc);
-        float r_ddt = gn * fmaf(An * a, prev, bb * us);
-        float r_du = gn * dts * bb;
-        float r_y = cc * ht;
-        g = a * gn;
-#pragma unroll
-        for (int off = 8; off > 0; off >>= 1) {
-          r_ddt += __shfl_xor_sync(0xffffffffu, r_ddt, off);
-          r_du += __shfl_xor_sync(0xffffffffu, r_du, off);
-          r_y += __shfl_xor_sync(0xffffffffu, r_y, off);
-        }
-        if (n == s) {
-          out_ddt = r_ddt;
-          out_du = r_du;
-          out_yp = r_y;
-        }
-        const float sB = cB + __shfl_xor_sync(0xffffffffu, cB, 16);
-        const float sC = cC + __shfl_xor_sync(0xffffffffu, cC, 16);
-        if (lane < 16) {
-          red[s][warp][0][n] = sB;
-          red[s][warp][1][n] = sC;
-        }
-      }
-    }
-    // the row's per-step outputs of the block: lane n writes step t0 + n
-    if (n < cnt) {
-      const int64_t xi = row * L + t0 + n;
-      const float dx = p.softplus ? out_ddt * sigmoid_f(my_x) : out_ddt;
+      const float ddt = (ddt_a[0] + ddt_a[1]) * kLn2 + (ddt_b[0] + ddt_b[1]) * u;
+      const float dx = p.softplus ? ddt * sigmoid_f(xs[st]) : ddt;
       dbias_acc += dx;
-      dD_acc = fmaf(my_dyp, my_u, dD_acc);
+      dD_acc = fmaf(dyp, u, dD_acc);
       if (valid) {
+        const int64_t xi = row * L + t;
         static_cast<T*>(p.ddelta)[xi] = Elem<T>::from_f32(dx);
-        static_cast<T*>(p.du)[xi] = Elem<T>::from_f32(fmaf(my_dyp, Dd, out_du));
+        static_cast<T*>(p.du)[xi] = Elem<T>::from_f32(fmaf(dyp, Dd, dsum[0] + dsum[1]));
         if (HAS_Z) {
-          const float yp = fmaf(Dd, my_u, out_yp);
-          const float dz = my_dy * yp * my_sig * fmaf(my_z, 1.f - my_sig, 1.f);
+          const float yp = fmaf(Dd, u, ysum[0] + ysum[1]);
+          const float dz = dys[st] * yp * sig * fmaf(zs[st], 1.f - sig, 1.f);
           static_cast<T*>(p.dz)[xi] = Elem<T>::from_f32(dz);
         }
       }
-    }
-    __syncthreads();
-    // sums of dB/dC over the CTA's rows, step by step, warps in order
-    if (tid < kBwdBlock * 2 * kBwdLanes) {
-      const int s = tid / (2 * kBwdLanes), m = (tid / kBwdLanes) & 1, nn = tid & 15;
-      if (s < cnt) {
+      __syncthreads();
+      // dB/dC of step t over the CTA's rows, in row order
+      if (tid < 2 * NT) {
         float acc = 0.f;
-        for (int w = 0; w < kBwdThreads / 32; ++w) acc += red[s][w][m][nn];
-        p.part_bc[((cta * 2 + m) * kBwdLanes + nn) * L + t0 + s] = acc;
+        for (int r = 0; r < kBwdRows; ++r) acc += red[r][tid];
+        const int m = tid < NT ? 1 : 0, nn = tid & (NT - 1);
+        p.part_bc[((cta * 2 + m) * NT + nn) * L + t] = acc;
       }
+      __syncthreads();
     }
-    __syncthreads();
-  }
-  // per-row totals
-#pragma unroll
-  for (int off = 8; off > 0; off >>= 1) {
-    dD_acc += __shfl_xor_sync(0xffffffffu, dD_acc, off);
-    dbias_acc += __shfl_xor_sync(0xffffffffu, dbias_acc, off);
   }
   if (valid) {
-    p.part_a[(b * p.dim + d) * kBwdLanes + n] = dA_acc;
-    if (n == 0) {
-      p.part_dd[(b * p.dim + d) * 2 + 0] = dD_acc;
-      p.part_dd[(b * p.dim + d) * 2 + 1] = dbias_acc;
-    }
+#pragma unroll
+    for (int n = 0; n < NT; ++n) p.part_a[(b * p.dim + d) * NT + n] = dA_acc[n];
+    p.part_dd[(b * p.dim + d) * 2 + 0] = dD_acc;
+    p.part_dd[(b * p.dim + d) * 2 + 1] = dbias_acc;
   }
 }
 
