@@ -95,6 +95,8 @@ class Oracle:
             ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
             ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
             ctypes.c_int, ctypes.c_int]
+        lib.ss_oracle_fwd_pc.restype = ctypes.c_int
+        lib.ss_oracle_fwd_pc.argtypes = list(lib.ss_oracle_fwd.argtypes)
         lib.ss_oracle_bwd.restype = ctypes.c_int
         lib.ss_oracle_bwd.argtypes = [ctypes.c_void_p] * 8 + [ctypes.c_int] + \
             [ctypes.c_void_p] * 12 + [ctypes.c_int64] * 4 + [ctypes.c_int, ctypes.c_int]
@@ -104,18 +106,22 @@ class Oracle:
 
     def fwd(self, u, delta, A, B, C, D=None, z=None, delta_bias=None,
             delta_softplus=True, h0=None, dtype: str = "f32",
-            nthreads: int | None = None):
-        """Sequential fp64 forward; returns (y [b,d,L], last_state [b,d,N])."""
+            nthreads: int | None = None, bc_per_channel: bool = False):
+        """Sequential fp64 forward; returns (y [b,d,L], last_state [b,d,N]).
+
+        bc_per_channel: B and C are [b,d,N,L], one row per channel (the task
+        spec's kernel sketch layout), instead of [b,N,L]."""
         u_, dl_, B_, C_, z_ = (_as_input(t, dtype) for t in (u, delta, B, C, z))
         A_ = _as_input(A, "f32")
         D_ = _as_input(D, "f32")
         bias_ = _as_input(delta_bias, "f32")
         batch, dim, seqlen = u_.shape
         dstate = A_.shape[1]
+        bc_shape = (batch, dim, dstate, seqlen) if bc_per_channel else (batch, dstate, seqlen)
         for name, arr, shape in (("delta", dl_, (batch, dim, seqlen)),
                                  ("A", A_, (dim, dstate)),
-                                 ("B", B_, (batch, dstate, seqlen)),
-                                 ("C", C_, (batch, dstate, seqlen))):
+                                 ("B", B_, bc_shape),
+                                 ("C", C_, bc_shape)):
             if tuple(arr.shape) != shape:
                 raise ValueError(f"{name} has shape {arr.shape}, expected {shape}")
         if z_ is not None and tuple(z_.shape) != (batch, dim, seqlen):
@@ -128,7 +134,8 @@ class Oracle:
         y = np.empty((batch, dim, seqlen), dtype=np.float64)
         last = np.empty((batch, dim, dstate), dtype=np.float64)
         nt = nthreads if nthreads is not None else (os.cpu_count() or 1)
-        rc = self.lib.ss_oracle_fwd(
+        fn = self.lib.ss_oracle_fwd_pc if bc_per_channel else self.lib.ss_oracle_fwd
+        rc = fn(
             _ptr(u_), _ptr(dl_), _ptr(A_), _ptr(B_), _ptr(C_), _ptr(D_), _ptr(z_),
             _ptr(bias_), int(bool(delta_softplus)), _ptr(h0_), _ptr(y), _ptr(last),
             batch, dim, dstate, seqlen, DTYPES[dtype], nt)

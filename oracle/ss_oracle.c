@@ -41,8 +41,8 @@
  *     log(1 + e^x) for every x without overflow;
  *   - no clamp is applied to A.
  *
- * Inputs are read in the ABI layouts (u/delta/z [b,d,L], B/C [b,N,L],
- * A [d,N], D and bias [d]); dtype 0 means float32 values, dtype 1 means
+ * Inputs are read in the ABI layouts (u/delta/z [b,d,L], B/C [b,N,L] or, for
+ * ss_oracle_fwd_pc, [b,d,N,L], A [d,N], D and bias [d]); dtype 0 means float32 values, dtype 1 means
  * bfloat16 bit patterns, widened exactly to double.  Outputs are double.
  * Rows are split over nthreads POSIX threads; each row is independent.
  */
@@ -70,6 +70,7 @@ typedef struct {
   double* last_state;
   int64_t batch, dim, dstate, seqlen;
   int dtype;
+  int bc_per_channel; /* B, C are [b,d,N,L] (one row per channel) instead of [b,N,L] */
   int64_t row_begin, row_end;
   int status;
 } oracle_job;
@@ -100,6 +101,7 @@ static void run_rows(oracle_job* j) {
   }
   for (int64_t row = j->row_begin; row < j->row_end; ++row) {
     const int64_t b = row / dim, d = row % dim;
+    const int64_t bc = j->bc_per_channel ? row : b;  /* B/C row of this channel */
     for (int64_t n = 0; n < N; ++n) h[n] = j->h0 ? j->h0[row * N + n] : 0.0;
     const double bias = j->bias ? (double)j->bias[d] : 0.0;
     const double Dd = j->D ? (double)j->D[d] : 0.0;
@@ -111,9 +113,9 @@ static void run_rows(oracle_job* j) {
       double y = 0.0;
       for (int64_t n = 0; n < N; ++n) {
         const double a_bar = exp(dt * (double)j->A[d * N + n]);
-        const double b_bar = dt * load_elem(j->B, (b * N + n) * L + t, j->dtype);
+        const double b_bar = dt * load_elem(j->B, (bc * N + n) * L + t, j->dtype);
         h[n] = a_bar * h[n] + b_bar * u;
-        y += load_elem(j->C, (b * N + n) * L + t, j->dtype) * h[n];
+        y += load_elem(j->C, (bc * N + n) * L + t, j->dtype) * h[n];
       }
       y += Dd * u;
       if (j->z) y *= silu(load_elem(j->z, x_idx, j->dtype));
@@ -132,12 +134,15 @@ static void* thread_main(void* arg) {
 
 /* Returns 0 on success, 1 on a bad argument, 2 on an allocation or thread
  * failure.  h0 and last_state are [b,d,N] doubles and may be NULL; D, z and
- * delta_bias may be NULL (zero skip, no gate, zero bias). */
-int ss_oracle_fwd(const void* u, const void* delta, const float* A, const void* B,
-                  const void* C, const float* D, const void* z, const float* delta_bias,
-                  int delta_softplus, const double* h0, double* y, double* last_state,
-                  int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, int dtype,
-                  int nthreads) {
+ * delta_bias may be NULL (zero skip, no gate, zero bias).  bc_per_channel:
+ * B and C are [b,d,N,L], one row per channel (the task spec's kernel sketch
+ * layout), instead of [b,N,L] shared by the channels of a batch row. */
+static int oracle_fwd_impl(const void* u, const void* delta, const float* A, const void* B,
+                           const void* C, const float* D, const void* z,
+                           const float* delta_bias, int delta_softplus, const double* h0,
+                           double* y, double* last_state, int64_t batch, int64_t dim,
+                           int64_t dstate, int64_t seqlen, int dtype, int nthreads,
+                           int bc_per_channel) {
   if (!u || !delta || !A || !B || !C || !y) return 1;
   if (batch <= 0 || dim <= 0 || dstate <= 0 || seqlen <= 0) return 1;
   if (dtype != ORACLE_F32 && dtype != ORACLE_BF16) return 1;
@@ -162,6 +167,7 @@ int ss_oracle_fwd(const void* u, const void* delta, const float* A, const void* 
     j->y = y; j->last_state = last_state;
     j->batch = batch; j->dim = dim; j->dstate = dstate; j->seqlen = seqlen;
     j->dtype = dtype;
+    j->bc_per_channel = bc_per_channel;
     j->row_begin = rows * i / nthreads;
     j->row_end = rows * (i + 1) / nthreads;
     if (nthreads == 1) {
@@ -180,6 +186,25 @@ int ss_oracle_fwd(const void* u, const void* delta, const float* A, const void* 
   free(tids);
   free(created);
   return status;
+}
+
+int ss_oracle_fwd(const void* u, const void* delta, const float* A, const void* B,
+                  const void* C, const float* D, const void* z, const float* delta_bias,
+                  int delta_softplus, const double* h0, double* y, double* last_state,
+                  int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, int dtype,
+                  int nthreads) {
+  return oracle_fwd_impl(u, delta, A, B, C, D, z, delta_bias, delta_softplus, h0, y, last_state,
+                         batch, dim, dstate, seqlen, dtype, nthreads, 0);
+}
+
+/* The forward with B and C given per channel, [b,d,N,L]. */
+int ss_oracle_fwd_pc(const void* u, const void* delta, const float* A, const void* B,
+                     const void* C, const float* D, const void* z, const float* delta_bias,
+                     int delta_softplus, const double* h0, double* y, double* last_state,
+                     int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, int dtype,
+                     int nthreads) {
+  return oracle_fwd_impl(u, delta, A, B, C, D, z, delta_bias, delta_softplus, h0, y, last_state,
+                         batch, dim, dstate, seqlen, dtype, nthreads, 1);
 }
 
 /* The associative operator of "Mamba CUDA 实现解析", section

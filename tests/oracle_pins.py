@@ -372,6 +372,40 @@ def pin_backward_finite_differences(orc, seed=22):
             _close(g[gname], fd, rtol=1e-6, atol=1e-7, what=f"{gname} (softplus={softplus})")
 
 
+# --------------------------------------------------------------------------
+# Per-channel B/C (the task spec's kernel sketch keeps B and C per [b,d,t]):
+# with every channel given the same rows the result equals the shared layout
+# bit for bit, and every channel equals the shared-layout oracle run alone on
+# that channel (batch 1, dim 1) with its own rows, bit for bit.
+def pin_per_channel_bc(orc, seed=23):
+    rng = np.random.default_rng(seed)
+    b, d, n, L = 2, 3, 4, 7
+    p = _rand_problem(rng, b, d, n, L)
+    y_s, s_s = orc.fwd(**p)
+    q = dict(p)
+    q["B"] = np.ascontiguousarray(np.broadcast_to(p["B"][:, None], (b, d, n, L)))
+    q["C"] = np.ascontiguousarray(np.broadcast_to(p["C"][:, None], (b, d, n, L)))
+    y_b, s_b = orc.fwd(**q, bc_per_channel=True)
+    assert np.array_equal(y_b, y_s) and np.array_equal(s_b, s_s), "broadcast rows differ"
+    q["B"] = rng.standard_normal((b, d, n, L)).astype(np.float32)
+    q["C"] = rng.standard_normal((b, d, n, L)).astype(np.float32)
+    y_pc, s_pc = orc.fwd(**q, bc_per_channel=True)
+    for bi in range(b):
+        for di in range(d):
+            one = {k: (None if v is None else v) for k, v in q.items()}
+            one["u"] = q["u"][bi:bi + 1, di:di + 1].copy()
+            one["delta"] = q["delta"][bi:bi + 1, di:di + 1].copy()
+            one["z"] = q["z"][bi:bi + 1, di:di + 1].copy()
+            one["A"] = q["A"][di:di + 1].copy()
+            one["D"] = q["D"][di:di + 1].copy()
+            one["delta_bias"] = q["delta_bias"][di:di + 1].copy()
+            one["B"] = q["B"][bi, di][None].copy()
+            one["C"] = q["C"][bi, di][None].copy()
+            y1, s1 = orc.fwd(**one)
+            assert np.array_equal(y1[0, 0], y_pc[bi, di]), f"channel ({bi},{di}) y"
+            assert np.array_equal(s1[0, 0], s_pc[bi, di]), f"channel ({bi},{di}) state"
+
+
 ALL_PINS = [
     pin_unrolled_sum,
     pin_zero_A_is_cumsum,
@@ -385,4 +419,5 @@ ALL_PINS = [
     pin_invariances,
     pin_bf16_widening,
     pin_backward_finite_differences,
+    pin_per_channel_bc,
 ]

@@ -30,13 +30,17 @@ MUTANTS = {
     "softplus_missing_abs": ("log1p(exp(-fabs(x)))", "log1p(exp(-x))"),
     "bias_ignored": ("load_elem(j->delta, x_idx, j->dtype) + bias;",
                      "load_elem(j->delta, x_idx, j->dtype);"),
-    "B_layout_b_L_N": ("load_elem(j->B, (b * N + n) * L + t, j->dtype)",
-                       "load_elem(j->B, (b * L + t) * N + n, j->dtype)"),
-    "C_time_reversed": ("load_elem(j->C, (b * N + n) * L + t, j->dtype)",
-                        "load_elem(j->C, (b * N + n) * L + (L - 1 - t), j->dtype)"),
+    "B_layout_b_L_N": ("load_elem(j->B, (bc * N + n) * L + t, j->dtype)",
+                       "load_elem(j->B, (bc * L + t) * N + n, j->dtype)"),
+    "C_time_reversed": ("load_elem(j->C, (bc * N + n) * L + t, j->dtype)",
+                        "load_elem(j->C, (bc * N + n) * L + (L - 1 - t), j->dtype)"),
+    "per_channel_BC_row_of_batch": ("const int64_t bc = j->bc_per_channel ? row : b;",
+                                    "const int64_t bc = b;"),
+    "per_channel_BC_row_swapped": ("const int64_t bc = j->bc_per_channel ? row : b;",
+                                   "const int64_t bc = j->bc_per_channel ? d * j->batch + b : b;"),
     "readout_before_update": (
-        "        h[n] = a_bar * h[n] + b_bar * u;\n        y += load_elem(j->C, (b * N + n) * L + t, j->dtype) * h[n];\n",
-        "        y += load_elem(j->C, (b * N + n) * L + t, j->dtype) * h[n];\n        h[n] = a_bar * h[n] + b_bar * u;\n"),
+        "        h[n] = a_bar * h[n] + b_bar * u;\n        y += load_elem(j->C, (bc * N + n) * L + t, j->dtype) * h[n];\n",
+        "        y += load_elem(j->C, (bc * N + n) * L + t, j->dtype) * h[n];\n        h[n] = a_bar * h[n] + b_bar * u;\n"),
     "h0_ignored": ("h[n] = j->h0 ? j->h0[row * N + n] : 0.0;", "h[n] = 0.0;"),
     "channel_from_wrong_axis": ("const int64_t b = row / dim, d = row % dim;",
                                 "const int64_t b = row % j->batch, d = row / j->batch;"),
