@@ -236,9 +236,13 @@ def oracle_rate(w, budget_s: float, inp_cpu=None) -> dict:
         sub["A"] = inp["A"][:ch].contiguous()
         sub["D"] = inp["D"][:ch].contiguous() if inp["D"] is not None else None
         sub["delta_bias"] = inp["delta_bias"][:ch].contiguous() if inp["delta_bias"] is not None else None
+        if w.bc_per_channel:
+            sub["B"] = inp["B"][:, :ch].contiguous()
+            sub["C"] = inp["C"][:, :ch].contiguous()
         t0 = time.perf_counter()
         orc.fwd(sub["u"], sub["delta"], sub["A"], sub["B"], sub["C"], sub["D"], sub["z"],
-                sub["delta_bias"], sub["delta_softplus"], dtype=w.dtype, nthreads=cores)
+                sub["delta_bias"], sub["delta_softplus"], dtype=w.dtype, nthreads=cores,
+                bc_per_channel=w.bc_per_channel)
         return time.perf_counter() - t0
 
     probe_ch = min(w.dim, max(1, cores))
@@ -320,8 +324,11 @@ def run_ours(args, world, rank, local):
         st = torch.empty((w.batch, w.dim, w.dstate), device=dev, dtype=torch.float32)
         sets.append((d, y, st))
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    plan = ss.ss_selective_scan_plan(w.batch, w.dim, w.dstate, w.seqlen,
-                                     ss.SS_F32 if w.dtype == "f32" else ss.SS_BF16, True, sms)
+    if w.bc_per_channel:  # ss_selective_scan_fwd_pc: one kernel, no chunks
+        plan = {"nchunks": 1, "kernel_launches": 1}
+    else:
+        plan = ss.ss_selective_scan_plan(w.batch, w.dim, w.dstate, w.seqlen,
+                                         ss.SS_F32 if w.dtype == "f32" else ss.SS_BF16, True, sms)
 
     def step(i):
         d, y, st = sets[i % nsets]
@@ -413,8 +420,9 @@ def run_ours(args, world, rank, local):
     t_sfu = w.updates / r_sfu
     t_fp32 = 4 * w.updates / r_fp32
     t_step = ms_step * 1e-3 / world * world  # per-rank step time
-    kernel_src = [REPO / "mamba_selective_scan_ss_gb300" / "csrc" / f
-                  for f in ("ss_fwd.cuh", "ss_sched.cuh", "ss_device.cuh", "ss_api.cu")]
+    srcs = (("ss_pc.cuh", "ss_device.cuh", "ss_api.cu") if w.bc_per_channel else
+            ("ss_fwd.cuh", "ss_sched.cuh", "ss_device.cuh", "ss_api.cu"))
+    kernel_src = [REPO / "mamba_selective_scan_ss_gb300" / "csrc" / f for f in srcs]
     traffic, traffic_src = traffic_record(kernel_src, w.name)
     if t_hbm >= max(t_sfu, t_fp32):
         achieved = nbytes / t_step / 1e9
@@ -432,7 +440,8 @@ def run_ours(args, world, rank, local):
                  "algorithmic_bytes_per_step": nbytes, "updates_per_step": w.updates,
                  "t_hbm_us": t_hbm * 1e6, "t_sfu_us": t_sfu * 1e6, "t_fp32_us": t_fp32 * 1e6,
                  "measured_step_us": t_step * 1e6,
-                 "scope": f"one ss_selective_scan_fwd call = {plan['kernel_launches']} kernel(s)"})
+                 "scope": (f"one ss_selective_scan_fwd{'_pc' if w.bc_per_channel else ''} call"
+                           f" = {plan['kernel_launches']} kernel(s)")})
 
     cpu = None
     if world == 1 and not args.no_cpu_baseline:

@@ -197,6 +197,28 @@ SS_API ss_status_t ss_selective_scan_bwd(
     float* dC, float* dD, void* dz, float* dbias,
     int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, ss_dtype_t dtype, void* stream);
 
+/*
+ * ss_selective_scan_fwd_pc -- the forward with B and C given per channel:
+ * the layout of "ТЕХНИЧЕСКОЕ ЗАДАНИЕ: Реализовать selective scan (Mamba)",
+ * Этап 2 step 3 (the base kernel signature indexes B and C by batch, channel
+ * and step), taken to dstate states.
+ *
+ * Arguments: those of ss_selective_scan_fwd, except
+ *   B, C       [batch, dim, dstate, seqlen]   dtype   one row per channel
+ *
+ * Limits: dstate <= 128 (else SS_ERR_UNSUPPORTED); zero initial state.
+ * Behaviour: validated on the host (errors launch nothing and write
+ * nothing); one kernel is enqueued on `stream`; no scratch, no device-side
+ * wait, no synchronisation.  y and last_state must not overlap any input or
+ * each other.
+ */
+SS_API ss_status_t ss_selective_scan_fwd_pc(
+    const void* u, const void* delta, const float* A, const void* B, const void* C,
+    const float* D, const void* z, const float* delta_bias, int delta_softplus,
+    void* y, float* last_state,
+    int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
+    ss_dtype_t dtype, void* stream);
+
 /* Human-readable name of a status code (static storage, never NULL). */
 SS_API const char* ss_status_string(ss_status_t status);
 

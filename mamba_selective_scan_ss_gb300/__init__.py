@@ -7,7 +7,7 @@ raise: there is no fallback implementation.
 
 Low-level names mirror the C ABI exactly (raw device pointers as ints):
     ss_selective_scan_fwd, ss_selective_scan_fwd_h0, ss_selective_state_update,
-    ss_selective_scan_bwd,
+    ss_selective_scan_bwd, ss_selective_scan_fwd_pc,
     ss_status_string, ss_selective_scan_check, ss_selective_scan_plan,
     ss_selective_scan_fwd_noalloc
 plus convenience wrappers for torch CUDA tensors:
@@ -28,7 +28,8 @@ __all__ = [
     "SS_ERR_CUDA", "SS_ERR_TIMEOUT", "SS_ERR_SCRATCH_LIMIT", "SelectiveScanError", "library_path", "load_library",
     "ss_selective_scan_fwd", "ss_status_string", "ss_selective_scan_check",
     "ss_selective_scan_plan", "ss_selective_scan_fwd_noalloc", "ss_selective_scan_fwd_h0",
-    "ss_selective_state_update", "ss_selective_scan_bwd", "selective_scan_fwd",
+    "ss_selective_state_update", "ss_selective_scan_bwd", "ss_selective_scan_fwd_pc",
+    "selective_scan_fwd",
     "selective_state_update", "selective_scan_bwd",
 ]
 
@@ -77,6 +78,8 @@ def load_library():
         lib.ss_selective_state_update.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                                   ctypes.c_int, vp, i64, i64, i64,
                                                   ctypes.c_int, vp]
+        lib.ss_selective_scan_fwd_pc.restype = ctypes.c_int
+        lib.ss_selective_scan_fwd_pc.argtypes = list(lib.ss_selective_scan_fwd.argtypes)
         lib.ss_selective_scan_bwd.restype = ctypes.c_int
         lib.ss_selective_scan_bwd.argtypes = [vp] * 8 + [ctypes.c_int] + [vp] * 10 + \
             [i64, i64, i64, i64, ctypes.c_int, vp]
@@ -141,6 +144,14 @@ def ss_selective_state_update(state, x, dt, A, B, C, D, z, dt_bias, dt_softplus,
         int(dtype), stream)
 
 
+def ss_selective_scan_fwd_pc(u, delta, A, B, C, D, z, delta_bias, delta_softplus, y, last_state,
+                             batch, dim, dstate, seqlen, dtype, stream) -> int:
+    """The forward with B and C per channel ([batch, dim, dstate, seqlen])."""
+    return load_library().ss_selective_scan_fwd_pc(
+        u, delta, A, B, C, D, z, delta_bias, int(delta_softplus), y, last_state,
+        batch, dim, dstate, seqlen, int(dtype), stream)
+
+
 def ss_selective_scan_bwd(u, delta, A, B, C, D, z, delta_bias, delta_softplus, dy, dlast_state,
                           du, ddelta, dA, dB, dC, dD, dz, dbias, batch, dim, dstate, seqlen,
                           dtype, stream) -> int:
@@ -199,7 +210,8 @@ def selective_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None,
                        y=None, last_state=None, stream=None, h0=None):
     """Run the forward on torch CUDA tensors in the ABI layouts.
 
-    u, delta, z: [batch, dim, seqlen]; B, C: [batch, dstate, seqlen]; A:
+    u, delta, z: [batch, dim, seqlen]; B, C: [batch, dstate, seqlen] (or
+    [batch, dim, dstate, seqlen]: one row per channel, ss_selective_scan_fwd_pc); A:
     [dim, dstate] fp32; D, delta_bias: [dim] fp32.  u, delta, B, C, z share one
     dtype (float32 or bfloat16), which is also y's dtype.  Returns y, or
     (y, last_state) with last_state [batch, dim, dstate] fp32.  Outputs are
@@ -224,12 +236,18 @@ def selective_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None,
             delta_softplus)
     outs = (_ptr(y), _ptr(last_state) if return_last_state else None,
             batch, dim, dstate, seqlen, dt, s)
-    if h0 is None:
+    per_channel = B.dim() == 4
+    if per_channel:
+        if h0 is not None:
+            raise ValueError("per-channel B/C take no initial state")
+        status = ss_selective_scan_fwd_pc(*args, *outs)
+    elif h0 is None:
         status = ss_selective_scan_fwd(*args, *outs)
     else:
         status = ss_selective_scan_fwd_h0(*args, _ptr(h0), *outs)
     if status != SS_OK:
-        raise SelectiveScanError(status, "ss_selective_scan_fwd" + ("" if h0 is None else "_h0"))
+        what = "_pc" if per_channel else ("" if h0 is None else "_h0")
+        raise SelectiveScanError(status, "ss_selective_scan_fwd" + what)
     return (y, last_state) if return_last_state else y
 
 

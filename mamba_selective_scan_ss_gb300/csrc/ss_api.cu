@@ -15,6 +15,7 @@
 
 #include "ss_bwd.cuh"
 #include "ss_decode.cuh"
+#include "ss_pc.cuh"
 #include "ss_sched.cuh"
 #include "ss_selective_scan.h"
 
@@ -588,6 +589,73 @@ SS_API ss_status_t ss_selective_scan_bwd(
   const cudaError_t err = cudaGetLastError();
   const cudaError_t ferr = cudaFreeAsync(base, st);
   return err == cudaSuccess && ferr == cudaSuccess ? SS_OK : SS_ERR_CUDA;
+}
+
+SS_API ss_status_t ss_selective_scan_fwd_pc(
+    const void* u, const void* delta, const float* A, const void* B, const void* C,
+    const float* D, const void* z, const float* delta_bias, int delta_softplus,
+    void* y, float* last_state,
+    int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
+    ss_dtype_t dtype, void* stream) {
+  // ---- validation: nothing is enqueued or written on error ----
+  if (dtype != SS_F32 && dtype != SS_BF16) return SS_ERR_UNSUPPORTED;
+  if (!u || !delta || !A || !B || !C || !y) return SS_ERR_INVALID_ARGUMENT;
+  if (batch <= 0 || dim <= 0 || dstate <= 0 || seqlen <= 0) return SS_ERR_INVALID_ARGUMENT;
+  if (dstate > 128) return SS_ERR_UNSUPPORTED;
+  const int64_t elt = dtype == SS_F32 ? 4 : 2;
+  Sizes sz;
+  int64_t bc_bytes;
+  if (!sizes_ok(batch, dim, dstate, seqlen, elt, &sz) || !mul_ok(sz.x_bytes, dstate, &bc_bytes))
+    return SS_ERR_UNSUPPORTED;
+  const uintptr_t ea = (uintptr_t)elt;
+  if (!aligned(u, ea) || !aligned(delta, ea) || !aligned(B, ea) || !aligned(C, ea) ||
+      !aligned(y, ea) || (z && !aligned(z, ea)) || !aligned(A, 4) || (D && !aligned(D, 4)) ||
+      (delta_bias && !aligned(delta_bias, 4)) || (last_state && !aligned(last_state, 4)))
+    return SS_ERR_INVALID_ARGUMENT;
+  const void* ins[] = {u, delta, B, C, z, A, D, delta_bias};
+  const int64_t in_bytes[] = {sz.x_bytes, sz.x_bytes, bc_bytes, bc_bytes, z ? sz.x_bytes : 0,
+                              sz.a_elems * 4, D ? dim * 4 : 0, delta_bias ? dim * 4 : 0};
+  for (int i = 0; i < 8; ++i) {
+    if (range_overlap(y, sz.x_bytes, ins[i], in_bytes[i])) return SS_ERR_INVALID_ARGUMENT;
+    if (last_state && range_overlap(last_state, sz.st_elems * 4, ins[i], in_bytes[i]))
+      return SS_ERR_INVALID_ARGUMENT;
+  }
+  if (last_state && range_overlap(last_state, sz.st_elems * 4, y, sz.x_bytes))
+    return SS_ERR_INVALID_ARGUMENT;
+
+  ss::PcParams p{};
+  p.u = u; p.delta = delta; p.A = A; p.B = B; p.C = C; p.D = D; p.z = z; p.bias = delta_bias;
+  p.softplus = delta_softplus ? 1 : 0;
+  p.y = y; p.last_state = last_state;
+  p.rows = batch * dim; p.dim = dim; p.dstate = dstate; p.seqlen = seqlen;
+  const int quads = (int)((dstate + 3) / 4);
+  p.seg_shift = 0;
+  while ((1 << p.seg_shift) < quads) ++p.seg_shift;
+  const int64_t blocks = ((p.rows << p.seg_shift) + 255) / 256;
+  if (blocks > INT_MAX) return SS_ERR_UNSUPPORTED;
+  const bool vec = seqlen % (32 / elt) == 0 && aligned(u, 16) && aligned(delta, 16) &&
+                   aligned(B, 16) && aligned(C, 16) && aligned(y, 16) && (!z || aligned(z, 16));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  (void)cudaGetLastError();
+  const unsigned g = (unsigned)blocks;
+  if (dtype == SS_F32) {
+    if (z) {
+      if (vec) ss::ss_fwd_pc<float, true, true><<<g, 256, 0, st>>>(p);
+      else ss::ss_fwd_pc<float, true, false><<<g, 256, 0, st>>>(p);
+    } else {
+      if (vec) ss::ss_fwd_pc<float, false, true><<<g, 256, 0, st>>>(p);
+      else ss::ss_fwd_pc<float, false, false><<<g, 256, 0, st>>>(p);
+    }
+  } else {
+    if (z) {
+      if (vec) ss::ss_fwd_pc<__nv_bfloat16, true, true><<<g, 256, 0, st>>>(p);
+      else ss::ss_fwd_pc<__nv_bfloat16, true, false><<<g, 256, 0, st>>>(p);
+    } else {
+      if (vec) ss::ss_fwd_pc<__nv_bfloat16, false, true><<<g, 256, 0, st>>>(p);
+      else ss::ss_fwd_pc<__nv_bfloat16, false, false><<<g, 256, 0, st>>>(p);
+    }
+  }
+  return cudaGetLastError() == cudaSuccess ? SS_OK : SS_ERR_CUDA;
 }
 
 SS_API ss_status_t ss_selective_scan_plan(int64_t batch, int64_t dim, int64_t dstate,

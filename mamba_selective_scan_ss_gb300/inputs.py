@@ -10,6 +10,7 @@ Workload shapes (batch, dim, dstate, seqlen) and value distributions:
     i.e. the inverse of softplus, so softplus(0 + delta_bias) = dt
   * A[d, n] = -(n + 1)                       (the real diagonal init of Mamba)
   * B, C ~ N(0, 1), layout [batch, dstate, seqlen], shared by all channels
+    (bc_per_channel workloads: [batch, dim, dstate, seqlen], one row per channel)
   * D ~ N(0, 1), layout [dim]
 Draw order is u, delta_raw, dt, B, C, D, z from one torch CPU generator seeded
 with the workload's seed.  For bf16 workloads u, delta_raw, B, C and z are
@@ -39,6 +40,7 @@ class ScanWorkload:
     dt_lo: float = 1e-3
     dt_hi: float = 1e-1
     seed: int = 0
+    bc_per_channel: bool = False  # B, C [batch, dim, dstate, seqlen] instead of shared
 
     @property
     def updates(self) -> int:
@@ -58,7 +60,8 @@ class ScanWorkload:
         bdl = self.batch * self.dim * self.seqlen
         streams = 3 + (1 if self.has_z else 0)          # u, delta, y (+ z)
         b = streams * bdl * self.elt
-        b += 2 * self.batch * self.dstate * self.seqlen * self.elt
+        b += 2 * self.batch * self.dstate * self.seqlen * self.elt * (
+            self.dim if self.bc_per_channel else 1)
         b += 4 * self.dim * self.dstate
         b += 4 * self.dim * (int(self.has_D) + int(self.has_bias))
         b += 4 * self.batch * self.dim * self.dstate
@@ -86,6 +89,9 @@ WORKLOADS = {
     "4_1024": _cfg4(1024),
     "4_4096": _cfg4(4096),
     "4_16384": _cfg4(16384),
+    # per-channel B/C (one row per channel): a Mamba-2.8B-shaped layer at L=512
+    "pc_2": ScanWorkload("per-channel-bc-b8-d5120-n16-L512-bf16", 8, 5120, 16, 512, "bf16",
+                         has_z=True, seed=9, bc_per_channel=True),
 }
 
 
@@ -100,8 +106,9 @@ def make_inputs(w: ScanWorkload) -> dict:
     delta = torch.randn((b, d, L), generator=g, dtype=torch.float32)
     lo, hi = math.log(w.dt_lo), math.log(w.dt_hi)
     dt = torch.exp(torch.rand((d,), generator=g, dtype=torch.float64) * (hi - lo) + lo)
-    Bm = torch.randn((b, n, L), generator=g, dtype=torch.float32)
-    Cm = torch.randn((b, n, L), generator=g, dtype=torch.float32)
+    bc_shape = (b, d, n, L) if w.bc_per_channel else (b, n, L)
+    Bm = torch.randn(bc_shape, generator=g, dtype=torch.float32)
+    Cm = torch.randn(bc_shape, generator=g, dtype=torch.float32)
     D = torch.randn((d,), generator=g, dtype=torch.float32)
     z = torch.randn((b, d, L), generator=g, dtype=torch.float32) if w.has_z else None
 

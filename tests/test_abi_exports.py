@@ -29,6 +29,7 @@ def test_header_declares_the_entry_points():
     assert declared_functions() == ["ss_selective_scan_bwd", "ss_selective_scan_check",
                                     "ss_selective_scan_fwd",
                                     "ss_selective_scan_fwd_h0", "ss_selective_scan_fwd_noalloc",
+                                    "ss_selective_scan_fwd_pc",
                                     "ss_selective_scan_plan", "ss_selective_state_update",
                                     "ss_status_string"]
 

@@ -1,0 +1,109 @@
+"""Forward with B and C per channel against the oracle, through the C ABI.
+
+ss_selective_scan_fwd_pc takes B and C as [batch, dim, dstate, seqlen] (one
+row per channel); the oracle's forward reads the same layout
+(bc_per_channel).  Tolerances are those of the forward: fp32 I/O
+|err| <= 1e-5 + 1e-4*|ref|, bf16 I/O |err| <= 1e-2*(1 + |ref|), on y and
+last_state.
+"""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import mamba_selective_scan_ss_gb300 as ss
+import oracle
+from mamba_selective_scan_ss_gb300 import _build
+from mamba_selective_scan_ss_gb300.inputs import ScanWorkload, make_inputs
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"f32": (1e-5, 1e-4), "bf16": (1e-2, 1e-2)}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    _build.build_all()
+    ss.load_library()
+
+
+@pytest.fixture(scope="module")
+def orc():
+    return oracle.default()
+
+
+def close(got, ref, dtype, what):
+    atol, rtol = TOL[dtype]
+    g = got.float().cpu().numpy().astype(np.float64)
+    err = np.abs(g - ref)
+    bound = atol + rtol * np.abs(ref)
+    assert np.all(err <= bound), f"{what}: max |err|/bound {np.max(err / bound):.3g}"
+
+
+def check(orc, w):
+    inp = make_inputs(w)
+    if not w.softplus:
+        # without softplus dt = delta + bias must stay positive: shift delta
+        inp["delta"] = (inp["delta"].float().abs() * 0.05 + 0.01).to(inp["delta"].dtype)
+        inp["delta_bias"] = None
+    d = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    y, last = ss.selective_scan_fwd(d["u"], d["delta"], d["A"], d["B"], d["C"], d["D"], d["z"],
+                                    d["delta_bias"], d["delta_softplus"])
+    torch.cuda.synchronize()
+    y_ref, last_ref = orc.fwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"],
+                              inp["z"], inp["delta_bias"], inp["delta_softplus"],
+                              dtype=w.dtype, bc_per_channel=True)
+    close(y, y_ref, w.dtype, "y")
+    close(last, last_ref, w.dtype, "last_state")
+
+
+def W(b, d, n, L, dtype="f32", **kw):
+    return ScanWorkload(f"pc-b{b}-d{d}-n{n}-L{L}-{dtype}", b, d, n, L, dtype,
+                        bc_per_channel=True, seed=kw.pop("seed", 81), **kw)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("shape", [(2, 33, 16, 64), (1, 5, 16, 37), (3, 70, 16, 200),
+                                   (1, 1, 16, 1), (2, 300, 16, 24)])
+def test_per_channel_forward(orc, dtype, shape):
+    check(orc, W(*shape, dtype=dtype))
+
+
+@pytest.mark.parametrize("dstate", [1, 3, 4, 5, 8, 12, 17, 32, 64, 100, 128])
+def test_per_channel_dstate(orc, dstate):
+    check(orc, W(2, 9, dstate, 40, seed=82))
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("opts", [dict(has_z=False), dict(has_D=False), dict(has_bias=False),
+                                  dict(softplus=False)])
+def test_per_channel_optional_inputs(orc, dtype, opts):
+    check(orc, W(2, 20, 16, 48, dtype=dtype, seed=83, **opts))
+
+
+def test_per_channel_with_shared_rows_equals_shared_layout():
+    """Every channel given its batch row's B/C: the shared-layout forward's result."""
+    w = ScanWorkload("pc-shared-b2-d40-n16-L64-f32", 2, 40, 16, 64, "f32", seed=84)
+    inp = make_inputs(w)
+    d = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    y_s, s_s = ss.selective_scan_fwd(d["u"], d["delta"], d["A"], d["B"], d["C"], d["D"], d["z"],
+                                     d["delta_bias"], True)
+    Bp = d["B"][:, None].expand(-1, w.dim, -1, -1).contiguous()
+    Cp = d["C"][:, None].expand(-1, w.dim, -1, -1).contiguous()
+    y_p, s_p = ss.selective_scan_fwd(d["u"], d["delta"], d["A"], Bp, Cp, d["D"], d["z"],
+                                     d["delta_bias"], True)
+    torch.cuda.synchronize()
+    atol, rtol = TOL["f32"]
+    assert torch.allclose(y_p, y_s, atol=atol, rtol=rtol)
+    assert torch.allclose(s_p, s_s, atol=atol, rtol=rtol)
+
+
+def test_per_channel_rejects_more_than_128_states():
+    w = W(1, 2, 129, 8, seed=85)
+    inp = make_inputs(w)
+    d = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    with pytest.raises(ss.SelectiveScanError):
+        ss.selective_scan_fwd(d["u"], d["delta"], d["A"], d["B"], d["C"], d["D"], d["z"],
+                              d["delta_bias"], True)
