@@ -15,6 +15,9 @@ Functions and the passages they follow:
   * ``Oracle.bwd``      -- the exact derivative of ``fwd`` in reverse mode (the
     backward that the Russian task spec asks to verify with gradcheck, Этап 3
     step 4 and section 5; the Blelloch article, section 5.3).
+  * ``Oracle.ssd``      -- the Mamba-2 recurrence with one scalar decay per head
+    (the Mamba-2 cuTile news page, "Технические детали оптимизации"), run
+    sequentially per (batch, head).
 
 Parity status: pinned.  The pins (closed forms, the unrolled sum of eq (8) by
 brute force, composition under eq (10)-(12), special cases) live in
@@ -100,6 +103,9 @@ class Oracle:
         lib.ss_oracle_bwd.restype = ctypes.c_int
         lib.ss_oracle_bwd.argtypes = [ctypes.c_void_p] * 8 + [ctypes.c_int] + \
             [ctypes.c_void_p] * 12 + [ctypes.c_int64] * 4 + [ctypes.c_int, ctypes.c_int]
+        lib.ss_oracle_ssd.restype = ctypes.c_int
+        lib.ss_oracle_ssd.argtypes = [ctypes.c_void_p] * 7 + [ctypes.c_int] + \
+            [ctypes.c_void_p] * 2 + [ctypes.c_int64] * 6 + [ctypes.c_int, ctypes.c_int]
         lib.ss_oracle_combine.restype = None
         lib.ss_oracle_combine.argtypes = [ctypes.c_void_p] * 6 + [ctypes.c_int64]
         self.lib = lib
@@ -180,6 +186,32 @@ class Oracle:
         if rc != 0:
             raise RuntimeError(f"ss_oracle_bwd failed with status {rc}")
         return out
+
+    def ssd(self, x, dt, A, B, C, D=None, dt_bias=None, dt_softplus=True,
+            dtype: str = "f32", nthreads: int | None = None):
+        """Sequential fp64 Mamba-2 forward; returns (y [b,L,H,P], final_state [b,H,P,N]).
+
+        x [b,L,H,P], dt [b,L,H], A [H], B and C [b,L,G,N], D and dt_bias [H]."""
+        x_, dt_, B_, C_ = (_as_input(t, dtype) for t in (x, dt, B, C))
+        A_, D_, bias_ = (_as_input(t, "f32") for t in (A, D, dt_bias))
+        batch, seqlen, nheads, headdim = x_.shape
+        ngroups, dstate = B_.shape[2], B_.shape[3]
+        for name, arr, shape in (("dt", dt_, (batch, seqlen, nheads)), ("A", A_, (nheads,)),
+                                 ("B", B_, (batch, seqlen, ngroups, dstate)),
+                                 ("C", C_, (batch, seqlen, ngroups, dstate)),
+                                 ("D", D_, (nheads,)), ("dt_bias", bias_, (nheads,))):
+            if arr is not None and tuple(arr.shape) != shape:
+                raise ValueError(f"{name} has shape {arr.shape}, expected {shape}")
+        y = np.empty((batch, seqlen, nheads, headdim), dtype=np.float64)
+        final = np.empty((batch, nheads, headdim, dstate), dtype=np.float64)
+        nt = nthreads if nthreads is not None else (os.cpu_count() or 1)
+        rc = self.lib.ss_oracle_ssd(
+            _ptr(x_), _ptr(dt_), _ptr(A_), _ptr(B_), _ptr(C_), _ptr(D_), _ptr(bias_),
+            int(bool(dt_softplus)), _ptr(y), _ptr(final),
+            batch, seqlen, nheads, headdim, ngroups, dstate, DTYPES[dtype], nt)
+        if rc != 0:
+            raise RuntimeError(f"ss_oracle_ssd failed with status {rc}")
+        return y, final
 
     def combine(self, a1, v1, a2, c2):
         """Elementwise (a1, v1) (+) (a2, c2) of eq (10); returns (a, v)."""

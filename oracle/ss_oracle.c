@@ -421,3 +421,133 @@ done:
   free(fj); free(bj); free(tids); free(created); free(partial);
   return status;
 }
+
+/* ---------------------------------------------------------------------------
+ * Mamba-2 forward (one scalar decay per head), the recurrence that the Mamba-2
+ * cuTile news page ("Прорыв в оптимизации SSM-моделей", section
+ * "Технические детали оптимизации") writes for the state of a head:
+ *
+ *   h_t = exp(A * dt_t) * h_{t-1} + dt_t * B_t * x_t
+ *
+ * with h the head's state [P, N] (P = head dim, N = dstate), x_t [P] the
+ * head's slice of token t, B_t and C_t [N] the token's rows for the head's
+ * group, and the read-out with the skip connection that the page's
+ * compute_out kernel fuses:
+ *
+ *   y_t[p] = sum_n C_t[n] * h_t[p,n] + D * x_t[p]
+ *
+ * dt_t = softplus(dt[b,t,h] + dt_bias[h]) when dt_softplus is set, else
+ * dt + bias.  The state starts at zero.  Layouts: x, y [b,L,H,P]; dt [b,L,H];
+ * B, C [b,L,G,N] (head h reads group h / (H/G)); A, D, dt_bias [H];
+ * final_state [b,H,P,N].  Units (b, h) are independent and are split over
+ * the threads.
+ */
+typedef struct {
+  const void* x;
+  const void* dt;
+  const float* A;
+  const void* B;
+  const void* C;
+  const float* D;
+  const float* bias;
+  int softplus;
+  double* y;
+  double* final_state;
+  int64_t batch, seqlen, nheads, headdim, ngroups, dstate;
+  int dtype;
+  int64_t unit_begin, unit_end;
+  int status;
+} oracle_ssd_job;
+
+static void ssd_units(oracle_ssd_job* j) {
+  const int64_t L = j->seqlen, H = j->nheads, P = j->headdim, G = j->ngroups, N = j->dstate;
+  double* h = (double*)malloc(sizeof(double) * (size_t)(P * N));
+  if (!h) {
+    j->status = 2;
+    return;
+  }
+  for (int64_t unit = j->unit_begin; unit < j->unit_end; ++unit) {
+    const int64_t b = unit / H, hd = unit % H;
+    const int64_t g = hd / (H / G);  /* the head's group */
+    for (int64_t i = 0; i < P * N; ++i) h[i] = 0.0;
+    const double A = (double)j->A[hd];
+    const double bias = j->bias ? (double)j->bias[hd] : 0.0;
+    const double Dh = j->D ? (double)j->D[hd] : 0.0;
+    for (int64_t t = 0; t < L; ++t) {
+      double dt = load_elem(j->dt, (b * L + t) * H + hd, j->dtype) + bias;
+      if (j->softplus) dt = softplus(dt);
+      const double decay = exp(A * dt);
+      const int64_t xrow = ((b * L + t) * H + hd) * P;   /* x_t, y_t of this head */
+      const int64_t bcrow = ((b * L + t) * G + g) * N;   /* B_t, C_t of its group */
+      for (int64_t p = 0; p < P; ++p) {
+        const double xp = load_elem(j->x, xrow + p, j->dtype);
+        double y = 0.0;
+        for (int64_t n = 0; n < N; ++n) {
+          h[p * N + n] = decay * h[p * N + n] + dt * load_elem(j->B, bcrow + n, j->dtype) * xp;
+          y += load_elem(j->C, bcrow + n, j->dtype) * h[p * N + n];
+        }
+        j->y[xrow + p] = y + Dh * xp;
+      }
+    }
+    if (j->final_state)
+      for (int64_t i = 0; i < P * N; ++i) j->final_state[unit * P * N + i] = h[i];
+  }
+  free(h);
+}
+
+static void* ssd_thread_main(void* arg) {
+  ssd_units((oracle_ssd_job*)arg);
+  return NULL;
+}
+
+/* Returns 0 on success, 1 on a bad argument (a null required pointer, a size
+ * <= 0, nheads not a multiple of ngroups, an unknown dtype), 2 on an
+ * allocation failure.  y is [b,L,H,P] doubles; final_state [b,H,P,N] doubles
+ * or NULL; D and dt_bias may be NULL (no skip, zero bias). */
+int ss_oracle_ssd(const void* x, const void* dt, const float* A, const void* B, const void* C,
+                  const float* D, const float* dt_bias, int dt_softplus, double* y,
+                  double* final_state, int64_t batch, int64_t seqlen, int64_t nheads,
+                  int64_t headdim, int64_t ngroups, int64_t dstate, int dtype, int nthreads) {
+  if (!x || !dt || !A || !B || !C || !y) return 1;
+  if (batch <= 0 || seqlen <= 0 || nheads <= 0 || headdim <= 0 || ngroups <= 0 || dstate <= 0)
+    return 1;
+  if (nheads % ngroups != 0) return 1;
+  if (dtype != ORACLE_F32 && dtype != ORACLE_BF16) return 1;
+  const int64_t units = batch * nheads;
+  if (nthreads < 1) nthreads = 1;
+  if ((int64_t)nthreads > units) nthreads = (int)units;
+  oracle_ssd_job* jobs = (oracle_ssd_job*)calloc((size_t)nthreads, sizeof(oracle_ssd_job));
+  pthread_t* tids = (pthread_t*)calloc((size_t)nthreads, sizeof(pthread_t));
+  char* created = (char*)calloc((size_t)nthreads, 1);
+  if (!jobs || !tids || !created) {
+    free(jobs);
+    free(tids);
+    free(created);
+    return 2;
+  }
+  for (int i = 0; i < nthreads; ++i) {
+    oracle_ssd_job* j = &jobs[i];
+    j->x = x; j->dt = dt; j->A = A; j->B = B; j->C = C; j->D = D; j->bias = dt_bias;
+    j->softplus = dt_softplus; j->y = y; j->final_state = final_state;
+    j->batch = batch; j->seqlen = seqlen; j->nheads = nheads; j->headdim = headdim;
+    j->ngroups = ngroups; j->dstate = dstate; j->dtype = dtype;
+    j->unit_begin = units * i / nthreads;
+    j->unit_end = units * (i + 1) / nthreads;
+    if (nthreads == 1) {
+      ssd_units(j);
+    } else if (pthread_create(&tids[i], NULL, ssd_thread_main, j) == 0) {
+      created[i] = 1;
+    } else {
+      ssd_units(j);
+    }
+  }
+  int status = 0;
+  for (int i = 0; i < nthreads; ++i)
+    if (created[i]) pthread_join(tids[i], NULL);
+  for (int i = 0; i < nthreads; ++i)
+    if (jobs[i].status) status = jobs[i].status;
+  free(jobs);
+  free(tids);
+  free(created);
+  return status;
+}

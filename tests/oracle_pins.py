@@ -406,6 +406,109 @@ def pin_per_channel_bc(orc, seed=23):
             assert np.array_equal(s1[0, 0], s_pc[bi, di]), f"channel ({bi},{di}) state"
 
 
+# --------------------------------------------------------------------------
+# Mamba-2 (one scalar decay per head; the Mamba-2 cuTile news page,
+# "Технические детали оптимизации"):  h_t = exp(A dt_t) h_{t-1} + dt_t B_t x_t,
+# y_t = C_t . h_t + D x_t, per (batch, head), B and C shared by a group of heads.
+def _ssd_problem(rng, b, L, H, P, G, N, *, D=True, bias=True):
+    f = np.float32
+    return dict(
+        x=rng.standard_normal((b, L, H, P)).astype(f),
+        dt=(rng.standard_normal((b, L, H)) * 0.5).astype(f),
+        A=(-rng.uniform(0.3, 2.0, H)).astype(f),
+        B=rng.standard_normal((b, L, G, N)).astype(f),
+        C=rng.standard_normal((b, L, G, N)).astype(f),
+        D=rng.standard_normal(H).astype(f) if D else None,
+        dt_bias=(rng.standard_normal(H) * 0.5 - 1.0).astype(f) if bias else None)
+
+
+def _ssd_dt(p, softplus):
+    x = p["dt"].astype(np.float64)
+    if p["dt_bias"] is not None:
+        x = x + p["dt_bias"].astype(np.float64)[None, None, :]
+    return _softplus(x) if softplus else x
+
+
+# The quadratic ("dual") form of the same recurrence: with cum_t = sum_{r<=t} A dt_r,
+#   y_t = sum_{s<=t} (C_t . B_s) exp(cum_t - cum_s) dt_s x_s + D x_t
+#   h_L = sum_s exp(cum_{L-1} - cum_s) dt_s x_s B_s^T
+# evaluated by brute force over every (t, s) pair under an explicit causal mask.
+def pin_ssd_quadratic_form(orc, seed=24):
+    rng = np.random.default_rng(seed)
+    cases = [(2, 9, 4, 3, 2, 5, True, True), (1, 6, 3, 2, 1, 4, False, True),
+             (1, 1, 2, 2, 2, 3, True, False), (2, 12, 6, 2, 3, 2, True, True)]
+    for b, L, H, P, G, N, softplus, with_d in cases:
+        p = _ssd_problem(rng, b, L, H, P, G, N, D=with_d)
+        dt = _ssd_dt(p, softplus)                                   # [b,L,H]
+        cum = np.cumsum(dt * p["A"].astype(np.float64)[None, None, :], axis=1)
+        grp = np.arange(H) // (H // G)
+        Bh = p["B"].astype(np.float64)[:, :, grp, :]                # [b,L,H,N]
+        Ch = p["C"].astype(np.float64)[:, :, grp, :]
+        x = p["x"].astype(np.float64)
+        cb = np.einsum("bthn,bshn->bhts", Ch, Bh)
+        ct = cum.transpose(0, 2, 1)                                 # [b,H,L]
+        causal = np.tril(np.ones((L, L), dtype=bool))
+        seg = np.where(causal, ct[:, :, :, None] - ct[:, :, None, :], 0.0)
+        w = np.where(causal, np.exp(seg), 0.0) * cb * dt.transpose(0, 2, 1)[:, :, None, :]
+        y = np.einsum("bhts,bshp->bthp", w, x)
+        if with_d:
+            y = y + p["D"].astype(np.float64)[None, None, :, None] * x
+        wl = np.exp(cum[:, -1:, :] - cum) * dt                      # [b,L,H]
+        final = np.einsum("bsh,bshp,bshn->bhpn", wl, x, Bh)
+        y_o, f_o = orc.ssd(**p, dt_softplus=softplus)
+        _close(y_o, y, rtol=1e-11, atol=1e-12, what="ssd quadratic form y")
+        _close(f_o, final, rtol=1e-11, atol=1e-12, what="ssd quadratic form state")
+
+
+# A head of the Mamba-2 recurrence is the Mamba-1 scan (already pinned above)
+# with the head's P channels as the scan's channels, A[d,n] = A_h for every
+# state, dt the same for every channel, and B, C the head group's rows.
+def pin_ssd_is_mamba1_with_scalar_decay(orc, seed=25):
+    rng = np.random.default_rng(seed)
+    b, L, H, P, G, N = 2, 11, 4, 3, 2, 5
+    for softplus in (True, False):
+        p = _ssd_problem(rng, b, L, H, P, G, N)
+        y_o, f_o = orc.ssd(**p, dt_softplus=softplus)
+        for h in range(H):
+            g = h // (H // G)
+            q = dict(u=np.ascontiguousarray(p["x"][:, :, h, :].transpose(0, 2, 1)),
+                     delta=np.ascontiguousarray(np.broadcast_to(
+                         p["dt"][:, None, :, h], (b, P, L))),
+                     A=np.full((P, N), p["A"][h], np.float32),
+                     B=np.ascontiguousarray(p["B"][:, :, g, :].transpose(0, 2, 1)),
+                     C=np.ascontiguousarray(p["C"][:, :, g, :].transpose(0, 2, 1)),
+                     D=np.full(P, p["D"][h], np.float32), z=None,
+                     delta_bias=np.full(P, p["dt_bias"][h], np.float32))
+            y1, s1 = orc.fwd(**q, delta_softplus=softplus)
+            _close(y_o[:, :, h, :], y1.transpose(0, 2, 1), rtol=1e-14, atol=1e-15,
+                   what=f"ssd head {h} y")
+            _close(f_o[:, h], s1, rtol=1e-14, atol=1e-15, what=f"ssd head {h} state")
+
+
+# The page's chunked evaluation ("jump formula"): the state after a chunk is the
+# incoming state decayed over the chunk plus the chunk's own state from zero,
+# and each output of the chunk adds C_t . (exp(cum_t) h_in) to its zero-state
+# output, cum_t the decay accumulated inside the chunk up to t.
+def pin_ssd_jump_formula(orc, seed=26):
+    rng = np.random.default_rng(seed)
+    b, L, H, P, G, N, L1 = 2, 13, 4, 2, 2, 3, 5
+    p = _ssd_problem(rng, b, L, H, P, G, N)
+    y_all, f_all = orc.ssd(**p)
+    part = lambda sl: {k: (np.ascontiguousarray(v[:, sl]) if k in ("x", "dt", "B", "C") else v)
+                       for k, v in p.items()}
+    y1, f1 = orc.ssd(**part(slice(0, L1)))
+    p2 = part(slice(L1, L))
+    y2, f2 = orc.ssd(**p2)
+    cum2 = np.cumsum(_ssd_dt(p2, True) * p["A"].astype(np.float64)[None, None, :], axis=1)
+    grp = np.arange(H) // (H // G)
+    C2 = p2["C"].astype(np.float64)[:, :, grp, :]                     # [b,L2,H,N]
+    carry = np.einsum("bthn,bth,bhpn->bthp", C2, np.exp(cum2), f1)
+    _close(y_all[:, :L1], y1, rtol=1e-13, atol=1e-14, what="ssd first chunk")
+    _close(y_all[:, L1:], y2 + carry, rtol=1e-11, atol=1e-12, what="ssd second chunk y")
+    _close(f_all, np.exp(cum2[:, -1])[:, :, None, None] * f1 + f2, rtol=1e-11, atol=1e-12,
+           what="ssd state after both chunks")
+
+
 ALL_PINS = [
     pin_unrolled_sum,
     pin_zero_A_is_cumsum,
@@ -420,4 +523,7 @@ ALL_PINS = [
     pin_bf16_widening,
     pin_backward_finite_differences,
     pin_per_channel_bc,
+    pin_ssd_quadratic_form,
+    pin_ssd_is_mamba1_with_scalar_decay,
+    pin_ssd_jump_formula,
 ]

@@ -62,6 +62,20 @@ MUTANTS = {
     "bwd_dB_without_u": ("j->dB[(b * N + n) * L + t] += gn * dt * u;",
                          "j->dB[(b * N + n) * L + t] += gn * dt;"),
     "bwd_dlast_ignored": ("g[n] = j->dlast ? j->dlast[row * N + n] : 0.0;", "g[n] = 0.0;"),
+    # the Mamba-2 forward
+    "ssd_group_by_modulo": ("const int64_t g = hd / (H / G);", "const int64_t g = hd % G;"),
+    "ssd_decay_missing_dt": ("const double decay = exp(A * dt);", "const double decay = exp(A);"),
+    "ssd_input_missing_dt": ("decay * h[p * N + n] + dt * load_elem(j->B, bcrow + n, j->dtype) * xp;",
+                             "decay * h[p * N + n] + load_elem(j->B, bcrow + n, j->dtype) * xp;"),
+    "ssd_readout_from_B": ("y += load_elem(j->C, bcrow + n, j->dtype) * h[p * N + n];",
+                           "y += load_elem(j->B, bcrow + n, j->dtype) * h[p * N + n];"),
+    "ssd_skip_dropped": ("j->y[xrow + p] = y + Dh * xp;", "j->y[xrow + p] = y;"),
+    "ssd_bias_ignored": ("load_elem(j->dt, (b * L + t) * H + hd, j->dtype) + bias;",
+                         "load_elem(j->dt, (b * L + t) * H + hd, j->dtype);"),
+    "ssd_x_head_major": ("const int64_t xrow = ((b * L + t) * H + hd) * P;",
+                         "const int64_t xrow = ((b * H + hd) * L + t) * P;"),
+    "ssd_state_transposed": ("j->final_state[unit * P * N + i] = h[i];",
+                             "j->final_state[unit * P * N + (i % N) * P + i / N] = h[i];"),
 }
 
 
