@@ -198,6 +198,43 @@ SS_API ss_status_t ss_selective_scan_bwd(
     int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, ss_dtype_t dtype, void* stream);
 
 /*
+ * ss_mamba2_fwd -- the Mamba-2 forward (one scalar decay per head), the
+ * recurrence of the Mamba-2 cuTile news page ("Прорыв в оптимизации
+ * SSM-моделей", section "Технические детали оптимизации"), evaluated in
+ * chunks with the page's jump formula on the tensor cores (tcgen05):
+ *   dt_t = softplus(dt[b,t,h] + dt_bias[h])   (or dt + dt_bias when dt_softplus == 0)
+ *   h_t  = exp(A[h] dt_t) h_{t-1} + dt_t x_t B_t^T       state [headdim, dstate], zero at t = 0
+ *   y_t  = h_t C_t + D[h] x_t
+ * for every batch b and head h; B_t and C_t are the rows of the head's group
+ * g = h / (nheads / ngroups).
+ *
+ * Arguments (device pointers, dense row-major):
+ *   x           [batch, seqlen, nheads, headdim]   bf16
+ *   dt          [batch, seqlen, nheads]            bf16
+ *   A           [nheads]                           float32
+ *   B, C        [batch, seqlen, ngroups, dstate]   bf16
+ *   D, dt_bias  [nheads]                           float32, or NULL (0)
+ *   y           [batch, seqlen, nheads, headdim]   bf16 (written)
+ *   final_state [batch, nheads, headdim, dstate]   float32 (written), or NULL
+ * Limits: dtype SS_BF16, headdim 64 and dstate 128 (else SS_ERR_UNSUPPORTED);
+ * nheads a multiple of ngroups, x, B, C and y 16-byte aligned (else
+ * SS_ERR_INVALID_ARGUMENT).  Precision: the products run on bf16 operands
+ * with fp32 accumulation; the decayed C.B weights, the decayed inputs and the
+ * state carried into a chunk are rounded to bf16 where they enter a product
+ * (the state itself stays fp32).
+ * Behaviour: validated on the host (errors launch nothing and write
+ * nothing); one kernel is enqueued on `stream`, one CTA per (batch, head);
+ * no scratch, no synchronisation; its waits on the tensor cores are bounded
+ * (SS_ERR_TIMEOUT from ss_selective_scan_check).  y and final_state must not
+ * overlap any input or each other.
+ */
+SS_API ss_status_t ss_mamba2_fwd(
+    const void* x, const void* dt, const float* A, const void* B, const void* C,
+    const float* D, const float* dt_bias, int dt_softplus, void* y, float* final_state,
+    int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim, int64_t ngroups,
+    int64_t dstate, ss_dtype_t dtype, void* stream);
+
+/*
  * ss_selective_scan_fwd_pc -- the forward with B and C given per channel:
  * the layout of "ТЕХНИЧЕСКОЕ ЗАДАНИЕ: Реализовать selective scan (Mamba)",
  * Этап 2 step 3 (the base kernel signature indexes B and C by batch, channel

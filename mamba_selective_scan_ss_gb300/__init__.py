@@ -7,7 +7,7 @@ raise: there is no fallback implementation.
 
 Low-level names mirror the C ABI exactly (raw device pointers as ints):
     ss_selective_scan_fwd, ss_selective_scan_fwd_h0, ss_selective_state_update,
-    ss_selective_scan_bwd, ss_selective_scan_fwd_pc,
+    ss_selective_scan_bwd, ss_selective_scan_fwd_pc, ss_mamba2_fwd,
     ss_status_string, ss_selective_scan_check, ss_selective_scan_plan,
     ss_selective_scan_fwd_noalloc
 plus convenience wrappers for torch CUDA tensors:
@@ -17,6 +17,7 @@ plus convenience wrappers for torch CUDA tensors:
                            dt_softplus=True, y=None)
     selective_scan_bwd(u, delta, A, B, C, D, z, delta_bias, delta_softplus, dy,
                        dlast_state=None)
+    mamba2_fwd(x, dt, A, B, C, D=None, dt_bias=None, dt_softplus=True, ...)
 """
 from __future__ import annotations
 
@@ -29,8 +30,8 @@ __all__ = [
     "ss_selective_scan_fwd", "ss_status_string", "ss_selective_scan_check",
     "ss_selective_scan_plan", "ss_selective_scan_fwd_noalloc", "ss_selective_scan_fwd_h0",
     "ss_selective_state_update", "ss_selective_scan_bwd", "ss_selective_scan_fwd_pc",
-    "selective_scan_fwd",
-    "selective_state_update", "selective_scan_bwd",
+    "ss_mamba2_fwd", "selective_scan_fwd",
+    "selective_state_update", "selective_scan_bwd", "mamba2_fwd",
 ]
 
 SS_F32, SS_BF16 = 0, 1
@@ -83,6 +84,9 @@ def load_library():
         lib.ss_selective_scan_bwd.restype = ctypes.c_int
         lib.ss_selective_scan_bwd.argtypes = [vp] * 8 + [ctypes.c_int] + [vp] * 10 + \
             [i64, i64, i64, i64, ctypes.c_int, vp]
+        lib.ss_mamba2_fwd.restype = ctypes.c_int
+        lib.ss_mamba2_fwd.argtypes = [vp] * 7 + [ctypes.c_int, vp, vp] + [i64] * 6 + \
+            [ctypes.c_int, vp]
         lib.ss_selective_scan_plan.restype = ctypes.c_int
         lib.ss_selective_scan_plan.argtypes = [i64, i64, i64, i64, ctypes.c_int, ctypes.c_int,
                                                ctypes.c_int, ctypes.POINTER(_Plan)]
@@ -159,6 +163,14 @@ def ss_selective_scan_bwd(u, delta, A, B, C, D, z, delta_bias, delta_softplus, d
     return load_library().ss_selective_scan_bwd(
         u, delta, A, B, C, D, z, delta_bias, int(delta_softplus), dy, dlast_state, du, ddelta,
         dA, dB, dC, dD, dz, dbias, batch, dim, dstate, seqlen, int(dtype), stream)
+
+
+def ss_mamba2_fwd(x, dt, A, B, C, D, dt_bias, dt_softplus, y, final_state, batch, seqlen,
+                  nheads, headdim, ngroups, dstate, dtype, stream) -> int:
+    """The Mamba-2 forward (scalar decay per head) on the tensor cores."""
+    return load_library().ss_mamba2_fwd(
+        x, dt, A, B, C, D, dt_bias, int(dt_softplus), y, final_state, batch, seqlen, nheads,
+        headdim, ngroups, dstate, int(dtype), stream)
 
 
 def ss_status_string(status: int) -> str:
@@ -308,3 +320,34 @@ def selective_scan_bwd(u, delta, A, B, C, D=None, z=None, delta_bias=None,
     if status != SS_OK:
         raise SelectiveScanError(status, "ss_selective_scan_bwd")
     return g
+
+
+def mamba2_fwd(x, dt, A, B, C, D=None, dt_bias=None, dt_softplus: bool = True,
+               return_final_state: bool = True, y=None, final_state=None, stream=None):
+    """The Mamba-2 forward on torch CUDA tensors (ss_mamba2_fwd).
+
+    x: [batch, seqlen, nheads, headdim] bf16; dt: [batch, seqlen, nheads] bf16;
+    A, D, dt_bias: [nheads] fp32; B, C: [batch, seqlen, ngroups, dstate] bf16.
+    Returns y (like x), or (y, final_state) with final_state [batch, nheads,
+    headdim, dstate] fp32.
+    """
+    import torch
+
+    io = _io_dtype(x)
+    _check_tensors(x, (("x", x), ("dt", dt), ("B", B), ("C", C)),
+                   (("A", A), ("D", D), ("dt_bias", dt_bias)))
+    batch, seqlen, nheads, headdim = x.shape
+    ngroups, dstate = B.shape[2], B.shape[3]
+    if y is None:
+        y = torch.empty_like(x)
+    if final_state is None and return_final_state:
+        final_state = torch.empty((batch, nheads, headdim, dstate), device=x.device,
+                                  dtype=torch.float32)
+    status = ss_mamba2_fwd(_ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(dt_bias),
+                           dt_softplus, _ptr(y),
+                           _ptr(final_state) if return_final_state else None,
+                           batch, seqlen, nheads, headdim, ngroups, dstate, io,
+                           _stream(stream, x.device))
+    if status != SS_OK:
+        raise SelectiveScanError(status, "ss_mamba2_fwd")
+    return (y, final_state) if return_final_state else y

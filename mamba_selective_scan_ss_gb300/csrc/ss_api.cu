@@ -18,6 +18,7 @@
 #include "ss_pc.cuh"
 #include "ss_sched.cuh"
 #include "ss_selective_scan.h"
+#include "ss_ssd.cuh"
 
 namespace {
 
@@ -655,6 +656,69 @@ SS_API ss_status_t ss_selective_scan_fwd_pc(
       else ss::ss_fwd_pc<__nv_bfloat16, false, false><<<g, 256, 0, st>>>(p);
     }
   }
+  return cudaGetLastError() == cudaSuccess ? SS_OK : SS_ERR_CUDA;
+}
+
+SS_API ss_status_t ss_mamba2_fwd(
+    const void* x, const void* dt, const float* A, const void* B, const void* C,
+    const float* D, const float* dt_bias, int dt_softplus, void* y, float* final_state,
+    int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim, int64_t ngroups,
+    int64_t dstate, ss_dtype_t dtype, void* stream) {
+  // ---- validation: nothing is enqueued or written on error ----
+  if (dtype != SS_F32 && dtype != SS_BF16) return SS_ERR_UNSUPPORTED;
+  if (!x || !dt || !A || !B || !C || !y) return SS_ERR_INVALID_ARGUMENT;
+  if (batch <= 0 || seqlen <= 0 || nheads <= 0 || headdim <= 0 || ngroups <= 0 || dstate <= 0)
+    return SS_ERR_INVALID_ARGUMENT;
+  if (nheads % ngroups != 0) return SS_ERR_INVALID_ARGUMENT;
+  if (dtype != SS_BF16 || headdim != ss::kSsdP || dstate != ss::kSsdN) return SS_ERR_UNSUPPORTED;
+  int64_t tokens, x_elems, bc_elems, dt_elems, units, st_elems;
+  if (!mul_ok(batch, seqlen, &tokens) || !mul_ok(tokens, nheads, &dt_elems) ||
+      !mul_ok(dt_elems, headdim, &x_elems) || !mul_ok(tokens, ngroups, &bc_elems) ||
+      !mul_ok(bc_elems, dstate, &bc_elems) || !mul_ok(batch, nheads, &units) ||
+      !mul_ok(units, headdim * dstate, &st_elems) || x_elems > INT64_MAX / 4 ||
+      bc_elems > INT64_MAX / 4 || st_elems > INT64_MAX / 4)
+    return SS_ERR_UNSUPPORTED;
+  if (units > INT_MAX) return SS_ERR_UNSUPPORTED;
+  if (!aligned(x, 16) || !aligned(B, 16) || !aligned(C, 16) || !aligned(y, 16) ||
+      !aligned(dt, 2) || !aligned(A, 4) || (D && !aligned(D, 4)) ||
+      (dt_bias && !aligned(dt_bias, 4)) || (final_state && !aligned(final_state, 4)))
+    return SS_ERR_INVALID_ARGUMENT;
+  const void* ins[] = {x, dt, B, C, A, D, dt_bias};
+  const int64_t in_bytes[] = {x_elems * 2, dt_elems * 2, bc_elems * 2, bc_elems * 2,
+                              nheads * 4, D ? nheads * 4 : 0, dt_bias ? nheads * 4 : 0};
+  for (int i = 0; i < 7; ++i) {
+    if (range_overlap(y, x_elems * 2, ins[i], in_bytes[i])) return SS_ERR_INVALID_ARGUMENT;
+    if (final_state && range_overlap(final_state, st_elems * 4, ins[i], in_bytes[i]))
+      return SS_ERR_INVALID_ARGUMENT;
+  }
+  if (final_state && range_overlap(final_state, st_elems * 4, y, x_elems * 2))
+    return SS_ERR_INVALID_ARGUMENT;
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SS_ERR_CUDA;
+  static std::once_flag smem_once[64];
+  cudaError_t attr = cudaSuccess;
+  std::call_once(smem_once[dev], [&] {
+    attr = cudaFuncSetAttribute(ss::ss_ssd_fwd, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)ss::kSsdSmemBytes);
+  });
+  if (attr != cudaSuccess) return SS_ERR_CUDA;
+
+  ss::SsdParams p{};
+  p.x = static_cast<const __nv_bfloat16*>(x);
+  p.dt = static_cast<const __nv_bfloat16*>(dt);
+  p.A = A;
+  p.B = static_cast<const __nv_bfloat16*>(B);
+  p.C = static_cast<const __nv_bfloat16*>(C);
+  p.D = D;
+  p.bias = dt_bias;
+  p.softplus = dt_softplus ? 1 : 0;
+  p.y = static_cast<__nv_bfloat16*>(y);
+  p.final_state = final_state;
+  p.batch = batch; p.seqlen = seqlen; p.nheads = nheads; p.ngroups = ngroups;
+  (void)cudaGetLastError();
+  ss::ss_ssd_fwd<<<(unsigned)units, ss::kSsdThreads, ss::kSsdSmemBytes,
+                   static_cast<cudaStream_t>(stream)>>>(p);
   return cudaGetLastError() == cudaSuccess ? SS_OK : SS_ERR_CUDA;
 }
 

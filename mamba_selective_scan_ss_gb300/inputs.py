@@ -208,3 +208,95 @@ def make_decode_inputs(w: DecodeWorkload) -> dict:
         "dt_bias": bias if w.has_bias else None,
         "dt_softplus": True,
     }
+
+
+# ---------------------------------------------------------------- Mamba-2
+@dataclass(frozen=True)
+class Mamba2Workload:
+    """A Mamba-2 forward (one scalar decay per head): x [b, L, H, P], dt
+    [b, L, H], B and C [b, L, G, N], A, D and dt_bias [H]."""
+    name: str
+    batch: int
+    seqlen: int
+    nheads: int
+    headdim: int
+    ngroups: int
+    dstate: int
+    dtype: str = "bf16"
+    has_D: bool = True
+    has_bias: bool = True
+    seed: int = 0
+
+    @property
+    def updates(self) -> int:
+        """State updates of one call: batch * seqlen * nheads * headdim * dstate."""
+        return self.batch * self.seqlen * self.nheads * self.headdim * self.dstate
+
+    @property
+    def elt(self) -> int:
+        return 4 if self.dtype == "f32" else 2
+
+    def algorithmic_bytes(self) -> int:
+        """x, dt, B, C read once, y written once, the final state written once,
+        A, D and the bias read once."""
+        tok = self.batch * self.seqlen
+        b = 2 * tok * self.nheads * self.headdim * self.elt     # x, y
+        b += tok * self.nheads * self.elt                       # dt
+        b += 2 * tok * self.ngroups * self.dstate * self.elt    # B, C
+        b += 4 * self.batch * self.nheads * self.headdim * self.dstate  # final state
+        b += 4 * self.nheads * (1 + int(self.has_D) + int(self.has_bias))
+        return b
+
+    def chunk_flops(self, chunk: int) -> int:
+        """Multiply-add flops of the chunked evaluation with chunks of ``chunk``
+        steps: per (batch, chunk, group) C B^T; per (batch, chunk, head) the
+        masked product with x, the read-out of the incoming state and the
+        chunk's own state."""
+        nch = -(-self.seqlen // chunk)
+        q, p, n = chunk, self.headdim, self.dstate
+        per_head = 2 * q * q * p + 2 * q * n * p + 2 * q * n * p
+        per_group = 2 * q * q * n
+        return self.batch * nch * (self.nheads * per_head + self.ngroups * per_group)
+
+
+MAMBA2_WORKLOADS = {
+    # a Mamba-2-2.7B-shaped layer: d_inner 5120 = 80 heads of 64, 128 states, one group
+    "m2_2.7b": Mamba2Workload("mamba2-2.7b-layer-b8-L2048-h80-p64-n128-bf16", 8, 2048, 80, 64, 1,
+                              128, "bf16", seed=12),
+    # small case the oracle finishes in seconds: three chunks (the last ragged), two groups
+    "m2_small": Mamba2Workload("mamba2-small-b2-L300-h4-p64-n128-g2-bf16", 2, 300, 4, 64, 2, 128,
+                               "bf16", seed=11),
+}
+
+
+def make_mamba2_inputs(w: Mamba2Workload) -> dict:
+    """Draw a Mamba-2 workload's inputs on the CPU (torch tensors, ABI layouts).
+
+    x, dt_raw ~ N(0, 1); per-head step dt ~ LogUniform[1e-3, 1e-1] and dt_bias =
+    log(expm1(dt)); A[h] = -U[1, 16] (the Mamba-2 initialisation range);
+    B, C ~ N(0, 1) [b, L, G, N]; D ~ N(0, 1) [H].  Draw order x, dt_raw, dt, A,
+    B, C, D.  bf16 workloads round x, dt_raw, B and C to bf16.
+    """
+    g = torch.Generator(device="cpu")
+    g.manual_seed(w.seed)
+    b, L, H, P, G, N = w.batch, w.seqlen, w.nheads, w.headdim, w.ngroups, w.dstate
+    io = torch.float32 if w.dtype == "f32" else torch.bfloat16
+    x = torch.randn((b, L, H, P), generator=g, dtype=torch.float32)
+    dt_raw = torch.randn((b, L, H), generator=g, dtype=torch.float32)
+    lo, hi = math.log(1e-3), math.log(1e-1)
+    dt = torch.exp(torch.rand((H,), generator=g, dtype=torch.float64) * (hi - lo) + lo)
+    A = -(1.0 + 15.0 * torch.rand((H,), generator=g, dtype=torch.float32))
+    Bm = torch.randn((b, L, G, N), generator=g, dtype=torch.float32)
+    Cm = torch.randn((b, L, G, N), generator=g, dtype=torch.float32)
+    D = torch.randn((H,), generator=g, dtype=torch.float32)
+    bias = torch.log(torch.expm1(dt)).to(torch.float32)
+    return {
+        "x": x.to(io).contiguous(),
+        "dt": dt_raw.to(io).contiguous(),
+        "A": A.contiguous(),
+        "B": Bm.to(io).contiguous(),
+        "C": Cm.to(io).contiguous(),
+        "D": D if w.has_D else None,
+        "dt_bias": bias if w.has_bias else None,
+        "dt_softplus": True,
+    }

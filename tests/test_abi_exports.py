@@ -26,7 +26,7 @@ def declared_functions():
 
 
 def test_header_declares_the_entry_points():
-    assert declared_functions() == ["ss_selective_scan_bwd", "ss_selective_scan_check",
+    assert declared_functions() == ["ss_mamba2_fwd", "ss_selective_scan_bwd", "ss_selective_scan_check",
                                     "ss_selective_scan_fwd",
                                     "ss_selective_scan_fwd_h0", "ss_selective_scan_fwd_noalloc",
                                     "ss_selective_scan_fwd_pc",
@@ -146,6 +146,28 @@ def test_validation_of_the_backward(lib):
     assert call(dC=ok["dB"] + 8) == ss.SS_ERR_INVALID_ARGUMENT  # two outputs overlap
     assert call(dA=ok["dA"] + 2) == ss.SS_ERR_INVALID_ARGUMENT  # misaligned fp32 output
 
+
+
+def test_validation_of_the_mamba2_forward(lib):
+    bufs = [ctypes.create_string_buffer(4096) for _ in range(10)]
+    p = [ctypes.addressof(b) for b in bufs]
+    names = ["x", "dt", "A", "B", "C", "D", "dt_bias", "y", "final_state"]
+    ok = dict(zip(names, p), dt_softplus=1, batch=1, seqlen=8, nheads=2, headdim=64,
+              ngroups=1, dstate=128, dtype=ss.SS_BF16, stream=None)
+
+    def call(**kw):
+        return ss.ss_mamba2_fwd(**dict(ok, **kw))
+
+    assert call(x=None) == ss.SS_ERR_INVALID_ARGUMENT
+    assert call(y=None) == ss.SS_ERR_INVALID_ARGUMENT
+    assert call(seqlen=0) == ss.SS_ERR_INVALID_ARGUMENT
+    assert call(nheads=3, ngroups=2) == ss.SS_ERR_INVALID_ARGUMENT  # heads not a multiple of groups
+    assert call(dtype=ss.SS_F32) == ss.SS_ERR_UNSUPPORTED           # bf16 only
+    assert call(dtype=7) == ss.SS_ERR_UNSUPPORTED
+    assert call(headdim=32) == ss.SS_ERR_UNSUPPORTED                # head dim 64 only
+    assert call(dstate=64) == ss.SS_ERR_UNSUPPORTED                 # 128 states only
+    assert call(x=ok["x"] + 2) == ss.SS_ERR_INVALID_ARGUMENT        # rows not 16-byte aligned
+    assert call(y=ok["x"]) == ss.SS_ERR_INVALID_ARGUMENT            # output over an input
 
 def test_plan_is_host_only_and_consistent(lib, monkeypatch):
     monkeypatch.delenv("SS_NCHUNKS", raising=False)
