@@ -43,6 +43,7 @@ sys.path.insert(0, str(REPO))
 METRIC = "selective-scan fwd state-updates/s (B*D*L*N/s) at 1 GB300; % of roofline"
 L2_BYTES = 129 * 2**20
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 
 
 def parse_args():
@@ -53,9 +54,9 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=None,
                     help="workload key (inputs.WORKLOADS; with --op decode, inputs.DECODE_WORKLOADS)")
-    ap.add_argument("--op", choices=["fwd", "decode", "bwd"], default="fwd",
+    ap.add_argument("--op", choices=["fwd", "decode", "bwd", "mamba2"], default="fwd",
                     help="fwd: the forward scan (default); decode: one token per call; "
-                         "bwd: the backward pass")
+                         "bwd: the backward pass; mamba2: the Mamba-2 forward (tensor cores)")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-baseline-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -183,10 +184,11 @@ def measured_peaks() -> dict:
     if p.exists():
         try:
             d = json.loads(p.read_text())
-            return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+            return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                    "source": "measured"}
         except (ValueError, KeyError):
             pass
-    return {"hbm_gbs": FALLBACK_HBM_GBS, "source": "fallback"}
+    return {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops": FALLBACK_BF16_TFLOPS, "source": "fallback"}
 
 
 def unit_rates() -> dict:
@@ -784,14 +786,197 @@ def decode_oracle_rate(w, inp, budget_s: float) -> dict:
                       f"in {el:.1f} s"}
 
 
+M2_METRIC = "Mamba-2 fwd state-updates/s (B*L*H*P*N/s) at 1 GB300; % of roofline"
+M2_CHUNK = 128  # steps per chunk of the kernel (the tensor-core MMA's M)
+
+
+def m2_oracle_rate(w, inp, budget_s: float) -> dict:
+    """The oracle's Mamba-2 forward on the first heads of every batch row, repeated."""
+    import oracle
+
+    orc = oracle.default()
+    per_head = w.batch * w.seqlen * w.headdim * w.dstate
+    hpg = w.nheads // w.ngroups
+    heads = min(w.nheads, max(1, int(4e8 // per_head)))
+    if heads >= hpg:
+        heads -= heads % hpg  # whole groups, so the sub-problem maps heads to the same groups
+    groups = max(1, heads // hpg)
+    sub = {"x": inp["x"][:, :, :heads].contiguous(), "dt": inp["dt"][:, :, :heads].contiguous(),
+           "A": inp["A"][:heads].contiguous(),
+           "B": inp["B"][:, :, :groups].contiguous(), "C": inp["C"][:, :, :groups].contiguous(),
+           "D": None if inp["D"] is None else inp["D"][:heads].contiguous(),
+           "dt_bias": None if inp["dt_bias"] is None else inp["dt_bias"][:heads].contiguous()}
+    cores = os.cpu_count() or 1
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        orc.ssd(sub["x"], sub["dt"], sub["A"], sub["B"], sub["C"], sub["D"], sub["dt_bias"], True,
+                dtype=w.dtype, nthreads=cores)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    upd = per_head * heads
+    return {"value": upd * reps / el, "reps": reps, "seconds": el,
+            "cores": min(cores, w.batch * heads),
+            "sample": f"{reps} pass(es) over the first {heads} of {w.nheads} heads of every batch "
+                      f"row, full seqlen {w.seqlen}: {upd} updates each, {el:.1f} s"}
+
+
+def run_mamba2(args, world, rank, local):
+    """The Mamba-2 forward (ss_mamba2_fwd, one kernel per call on the tensor
+    cores); inputs resident in HBM and larger than 2x L2."""
+    import torch
+    import mamba_selective_scan_ss_gb300 as ss
+    from mamba_selective_scan_ss_gb300 import _build
+    from mamba_selective_scan_ss_gb300.inputs import MAMBA2_WORKLOADS, make_mamba2_inputs
+
+    w = MAMBA2_WORKLOADS[args.workload]
+    inp = make_mamba2_inputs(w)
+    config = {"workload": w.name, "batch": w.batch, "seqlen": w.seqlen, "nheads": w.nheads,
+              "headdim": w.headdim, "ngroups": w.ngroups, "dstate": w.dstate,
+              "io_dtype": w.dtype, "chunk": M2_CHUNK}
+    if args.impl == "reference":
+        if rank == 0:
+            r = m2_oracle_rate(w, inp, max(1.0, args.reference_seconds / 10))
+            print(json.dumps({
+                "metric": M2_METRIC, "value": r["value"], "unit": "state-updates/s",
+                "n_gpus": args.gpus, "steps": r["reps"], "warmup": 0,
+                "ms_per_step": 1e3 * r["seconds"] / r["reps"], "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "impl": "reference", "op": "mamba2", "config": config,
+                "cpu_baseline": {"value": r["value"], "unit": "state-updates/s",
+                                 "cores": r["cores"], "kind": "oracle", "sample": r["sample"]},
+                "e2e": {"value": r["value"], "unit": "state-updates/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}), flush=True)
+        return
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py: no CUDA device (the Mamba-2 forward runs only on the GPU)")
+    if rank == 0:
+        _build.build_all()
+    barrier(world)
+    ss.load_library()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(dev)
+    d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    y = torch.empty_like(d["x"])
+    fs = torch.empty((w.batch, w.nheads, w.headdim, w.dstate), device=dev, dtype=torch.float32)
+    nbytes = w.algorithmic_bytes()
+    flops = w.chunk_flops(M2_CHUNK)
+
+    def step():
+        ss.mamba2_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["dt_bias"], True,
+                      y=y, final_state=fs, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    torch.cuda.synchronize(dev)
+    sampler = ClockSampler(gpu_id_for(dev.index))
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    sampler.start()
+    t_wall0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step()
+        ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    t_wall = time.perf_counter() - t_wall0
+    clocks = sampler.stop()
+    barrier(world)
+    if ss.ss_selective_scan_check(stream.cuda_stream) != ss.SS_OK:
+        raise SystemExit("bench.py: the Mamba-2 kernel reported a device-side error")
+    ms_max = max_over_ranks(ev0.elapsed_time(ev1), world)
+    ms_step = ms_max / args.steps
+    value = w.updates * args.steps * world / (ms_max * 1e-3)
+
+    e2e = None
+    if args.e2e_steps > 0:
+        keys = ["x", "dt", "B", "C"]
+        host = {k: inp[k].pin_memory() for k in keys}
+        y_host = torch.empty(y.shape, dtype=y.dtype).pin_memory()
+        h2d = sum(v.numel() * v.element_size() for v in host.values())
+        d2h = y_host.numel() * y_host.element_size()
+
+        def e2e_step():
+            with torch.cuda.stream(stream):
+                for k, v in host.items():
+                    d[k].copy_(v, non_blocking=True)
+                ss.mamba2_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["dt_bias"], True,
+                              y=y, final_state=fs, stream=stream)
+                y_host.copy_(y, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        e_ms = max_over_ranks(e0.elapsed_time(e1), world)
+        e2e = {"value": w.updates * args.e2e_steps * world / (e_ms * 1e-3),
+               "unit": "state-updates/s", "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(d2h), "ms_per_step": e_ms / args.e2e_steps}
+    if rank != 0:
+        return
+    pk = measured_peaks()
+    t_hbm = nbytes / (pk["hbm_gbs"] * 1e9)
+    t_tc = flops / (pk["bf16_tflops"] * 1e12)
+    t_step = ms_step * 1e-3
+    kernel_src = [REPO / "mamba_selective_scan_ss_gb300" / "csrc" / f
+                  for f in ("ss_ssd.cuh", "ss_device.cuh", "ss_api.cu")]
+    traffic, traffic_src = traffic_record(kernel_src, w.name)
+    if t_hbm >= t_tc:
+        achieved = nbytes / t_step / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / pk["hbm_gbs"], "peak_source": pk["source"]}
+    else:
+        achieved = flops / t_step / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"],
+                "peak_source": pk["source"] + " bf16 burst"}
+    roof.update({"traffic": traffic, "traffic_source": traffic_src,
+                 "algorithmic_bytes_per_step": nbytes, "chunk_flops_per_step": flops,
+                 "tensor_tflops_achieved": flops / t_step / 1e12,
+                 "updates_per_step": w.updates, "t_hbm_us": t_hbm * 1e6,
+                 "t_tensor_us": t_tc * 1e6, "measured_step_us": t_step * 1e6,
+                 "scope": "one ss_mamba2_fwd call = 1 kernel"})
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        r = m2_oracle_rate(w, inp, min(args.cpu_baseline_seconds, 10.0))
+        cpu = {"value": r["value"], "unit": "state-updates/s", "cores": r["cores"],
+               "kind": "oracle", "sample": r["sample"]}
+    in_bytes = nbytes // 2  # x, dt, B, C: about half of the call's traffic
+    config["l2"] = ("inputs larger than L2" if in_bytes > L2_BYTES else
+                    "inputs partly L2-resident between calls")
+    config["parallelism"] = f"replicas x{world}"
+    print(json.dumps({
+        "metric": M2_METRIC, "value": value, "unit": "state-updates/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic", "op": "mamba2", "config": config,
+        "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": int(args.steps), "clocks": clocks, "wall_s_timed_region": t_wall,
+    }), flush=True)
+
+
 def main():
     args = parse_args()
     if args.workload is None:
-        args.workload = {"decode": "decode_64", "bwd": "2"}.get(args.op, "1")
+        args.workload = {"decode": "decode_64", "bwd": "2", "mamba2": "m2_2.7b"}.get(args.op, "1")
     world, rank, local = dist_setup(args)
     try:
         if args.op == "decode":
             run_decode(args, world, rank, local)
+        elif args.op == "mamba2":
+            run_mamba2(args, world, rank, local)
         elif args.op == "bwd":
             if args.impl == "reference":
                 raise SystemExit("bench.py: --op bwd has no reference arm; its cpu_baseline "

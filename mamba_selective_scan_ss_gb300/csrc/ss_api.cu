@@ -5,6 +5,7 @@
 // device, allocate stream-ordered scratch for chunk carries when the sequence
 // is split, and enqueue the kernels on the caller's stream.
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 
 #include <climits>
 #include <cstdint>
@@ -35,6 +36,29 @@ bool range_overlap(const void* a, int64_t a_bytes, const void* b, int64_t b_byte
 }
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// A TMA descriptor of a bf16 tensor [d2][d1][d0] (d0 contiguous) read in boxes
+// of 8 x 128 x 1 elements, without swizzle; elements past d1 read as zero.
+bool tma_map_rows(CUtensorMap* map, const void* base, int64_t d0, int64_t d1, int64_t d2) {
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      fn = nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }();
+  if (!encode) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)d0, (cuuint64_t)d1, (cuuint64_t)d2};
+  const cuuint64_t strides[2] = {(cuuint64_t)d0 * 2, (cuuint64_t)(d0 * d1) * 2};
+  const cuuint32_t box[3] = {8, 128, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 bool mul_ok(int64_t a, int64_t b, int64_t* out) { return !__builtin_mul_overflow(a, b, out); }
 
@@ -694,6 +718,9 @@ SS_API ss_status_t ss_mamba2_fwd(
   if (final_state && range_overlap(final_state, st_elems * 4, y, x_elems * 2))
     return SS_ERR_INVALID_ARGUMENT;
 
+  if (seqlen > INT_MAX || batch > INT_MAX || nheads * headdim > INT_MAX ||
+      ngroups * dstate > INT_MAX)
+    return SS_ERR_UNSUPPORTED;  // TMA coordinates are 32-bit
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SS_ERR_CUDA;
   static std::once_flag smem_once[64];
@@ -705,6 +732,11 @@ SS_API ss_status_t ss_mamba2_fwd(
   if (attr != cudaSuccess) return SS_ERR_CUDA;
 
   ss::SsdParams p{};
+  // x as [batch, seqlen, nheads*headdim], B and C as [batch, seqlen, ngroups*dstate]
+  if (!tma_map_rows(&p.tx, x, nheads * headdim, seqlen, batch) ||
+      !tma_map_rows(&p.tb, B, ngroups * dstate, seqlen, batch) ||
+      !tma_map_rows(&p.tc, C, ngroups * dstate, seqlen, batch))
+    return SS_ERR_CUDA;
   p.x = static_cast<const __nv_bfloat16*>(x);
   p.dt = static_cast<const __nv_bfloat16*>(dt);
   p.A = A;

@@ -29,6 +29,8 @@
 // the state product's A operand (MN-major, K = s) from the same bytes.
 #pragma once
 
+#include <cuda.h>
+
 #include "ss_device.cuh"
 #include "ss_sched.cuh"
 
@@ -37,7 +39,7 @@ namespace ss {
 constexpr int kSsdQ = 128;  // steps per chunk (the MMA's M)
 constexpr int kSsdP = 64;   // head dim
 constexpr int kSsdN = 128;  // dstate
-constexpr int kSsdThreads = 128;
+constexpr int kSsdThreads = 256;
 
 // shared-memory map (bytes from the 1024-aligned dynamic base)
 constexpr uint32_t kSsdOffC = 0;           // C [t][n] K-major, then M [t][s] K-major
@@ -46,11 +48,15 @@ constexpr uint32_t kSsdOffX = 65536;       // x [s][p] MN-major
 constexpr uint32_t kSsdOffH = 81920;       // H [n][p] MN-major, then w.x [s][p]
 constexpr uint32_t kSsdOffCum = 98304;     // cum [Q] fp32
 constexpr uint32_t kSsdOffDt = 98816;      // dt [Q] fp32
-constexpr uint32_t kSsdOffMisc = 99328;    // warp sums, mbarrier, tensor-memory address
-constexpr uint32_t kSsdSmemBytes = 99328 + 64;
+constexpr uint32_t kSsdOffG = 99328;       // block factors [Q] fp32
+constexpr uint32_t kSsdOffMisc = 99840;    // warp sums, mbarrier, tensor-memory address
+constexpr uint32_t kSsdSmemBytes = 99840 + 64;
 constexpr uint32_t kSsdTmemCols = 256;     // CB / S [0,128), Y_in [128,192), Y_dg [192,256)
 
 struct SsdParams {
+  // TMA descriptors (3-D: columns, steps, batch; boxes of 8 columns x 128
+  // steps, zero past the sequence's end) of x [b,L,H*P] and B, C [b,L,G*N]
+  CUtensorMap tx, tb, tc;
   const __nv_bfloat16* x;   // [b,L,H,P]
   const __nv_bfloat16* dt;  // [b,L,H]
   const float* A;           // [H]
@@ -140,10 +146,18 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// 16 bytes global -> shared, zero-filled when !valid (the source is then not read).
-__device__ __forceinline__ void cp_async16_zfill(uint32_t smem, const void* gmem, bool valid) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem), "l"(gmem),
-               "r"(valid ? 16 : 0)
+// One TMA box (8 columns x 128 steps of one batch row) into shared memory:
+// 128 rows of 16 bytes, one 2 KB slab of the no-swizzle operand layout.
+__device__ __forceinline__ void tma_load3(uint32_t dst, const CUtensorMap* map, int c0, int c1,
+                                          int c2, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
                : "memory");
 }
 
@@ -155,30 +169,40 @@ __device__ __forceinline__ uint32_t bf16x2(float lo, float hi) {
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
-// grid = batch * nheads CTAs (one per (b, h)), block = 128, dynamic shared
+// grid = batch * nheads CTAs (one per (b, h)), block = 256, dynamic shared
 // memory kSsdSmemBytes.  Requires P = 64, N = 128 and 16-byte aligned rows.
-__global__ void __launch_bounds__(kSsdThreads, 2) ss_ssd_fwd(const SsdParams p) {
+//
+// Thread i works on row r = 32 (w % 4) + lane of every Q x * matrix (warp w
+// may read only tensor-memory lanes 32 (w % 4) ..), half hf = w / 4 of its
+// columns.  The next chunk's copies are issued as soon as the second pair of
+// products has consumed the shared operands, so they overlap the epilogue.
+__global__ void __launch_bounds__(kSsdThreads, 2) ss_ssd_fwd(const __grid_constant__ SsdParams p) {
   extern __shared__ __align__(1024) unsigned char smem[];
   constexpr int Q = kSsdQ, P = kSsdP, N = kSsdN;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int q4 = warp & 3, hf = warp >> 2;
+  const int r = q4 * 32 + lane;  // row (t, s or n) of this thread
   const int64_t H = p.nheads, G = p.ngroups, L = p.seqlen;
   const int64_t b = blockIdx.x / H, h = blockIdx.x % H;
   const int64_t g = h / (H / G);
 
   unsigned char* sC = smem + kSsdOffC;
-  unsigned char* sB = smem + kSsdOffB;
   unsigned char* sX = smem + kSsdOffX;
   unsigned char* sH = smem + kSsdOffH;
   float* cum = reinterpret_cast<float*>(smem + kSsdOffCum);
   float* dts = reinterpret_cast<float*>(smem + kSsdOffDt);
+  float* gs = reinterpret_cast<float*>(smem + kSsdOffG);
   float* wsum = reinterpret_cast<float*>(smem + kSsdOffMisc);
-  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kSsdOffMisc + 32);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kSsdOffMisc + 32);   // products
+  uint64_t* lbar = reinterpret_cast<uint64_t*>(smem + kSsdOffMisc + 40);  // copies
   uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + kSsdOffMisc + 48);
-  const uint32_t uC = smem_u32(sC), uB = smem_u32(sB), uX = smem_u32(sX), uH = smem_u32(sH);
-  const uint32_t ubar = smem_u32(bar);
+  const uint32_t uC = smem_u32(sC), uB = smem_u32(smem + kSsdOffB), uX = smem_u32(sX),
+                 uH = smem_u32(sH);
+  const uint32_t ubar = smem_u32(bar), ulbar = smem_u32(lbar);
 
   if (tid == 0) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(ubar));
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(ulbar));
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 0) {
@@ -191,63 +215,70 @@ __global__ void __launch_bounds__(kSsdThreads, 2) ss_ssd_fwd(const SsdParams p) 
   __syncthreads();
   tc_fence_after();
   const uint32_t tm = *tslot;
-  const uint32_t tlane = tm + ((uint32_t)(warp * 32) << 16);  // this warp's lanes
+  const uint32_t tlane = tm + ((uint32_t)(q4 * 32) << 16);  // this warp's lanes
 
   const float A2 = p.A[h] * kLog2e;
   const float bias = p.bias ? p.bias[h] : 0.f;
   const float Dh = p.D ? p.D[h] : 0.f;
-  float hs[P];  // state row n = tid: hs[p] = H[p][n]
+  float hs[P / 2];  // state row n = r, columns p in [32 hf, 32 hf + 32)
 #pragma unroll
-  for (int i = 0; i < P; ++i) hs[i] = 0.f;
+  for (int i = 0; i < P / 2; ++i) hs[i] = 0.f;
+
+  // chunk c's rows of C, B and x by TMA (thread 0; completes on lbar), and
+  // its dt (warps 0-3, row r)
+  auto issue = [&](int64_t c, float& dt_raw) {
+    const int64_t t0 = c * Q;
+    if (tid == 0) {
+      mbar_expect_tx(ulbar, (2 * (N / 8) + P / 8) * Q * 16);
+#pragma unroll
+      for (int j = 0; j < N / 8; ++j) {
+        tma_load3(uC + j * (Q * 16), &p.tc, (int)(g * N + 8 * j), (int)t0, (int)b, ulbar);
+        tma_load3(uB + j * (Q * 16), &p.tb, (int)(g * N + 8 * j), (int)t0, (int)b, ulbar);
+      }
+#pragma unroll
+      for (int j = 0; j < P / 8; ++j)
+        tma_load3(uX + j * (Q * 16), &p.tx, (int)(h * P + 8 * j), (int)t0, (int)b, ulbar);
+    }
+    const bool valid = hf == 0 && t0 + r < L;
+    dt_raw = valid ? __bfloat162float(p.dt[(b * L + t0 + r) * H + h]) : 0.f;
+  };
 
   constexpr uint32_t kIdCB = umma_idesc(128, 0, 0);
   constexpr uint32_t kIdY = umma_idesc(64, 0, 1);
   constexpr uint32_t kIdS = umma_idesc(64, 1, 1);
-  uint32_t parity = 0;
+  uint32_t parity = 0, lparity = 0;
   bool ok = true;
   const int64_t nchunks = (L + Q - 1) / Q;
+  float dt_raw;
+  issue(0, dt_raw);
   for (int64_t c = 0; c < nchunks && ok; ++c) {
     const int64_t t0 = c * Q;
     const int len = (int)(L - t0 < Q ? L - t0 : Q);
-    const int s = tid;  // the row this thread stages: step t0 + s
-    const bool valid = s < len;
-    const int64_t tok = b * L + t0 + (valid ? s : 0);
 
-    // ---- stage: x, B, C rows (zero past the end) and the in-chunk decay sums
-    {
-      const __nv_bfloat16* crow = p.C + (tok * G + g) * N;
-      const __nv_bfloat16* brow = p.B + (tok * G + g) * N;
-      const __nv_bfloat16* xrow = p.x + (tok * H + h) * P;
-#pragma unroll
-      for (int j = 0; j < N / 8; ++j) {
-        cp_async16_zfill(uC + j * (Q * 16) + s * 16, crow + j * 8, valid);
-        cp_async16_zfill(uB + j * (Q * 16) + s * 16, brow + j * 8, valid);
+    // ---- in-chunk decay sums (warps 0-3, row s = r): cum_s = sum_{r<=s} dt_r A log2e
+    if (hf == 0) {
+      float dtv = 0.f;
+      if (r < len) {
+        const float xdt = dt_raw + bias;
+        dtv = p.softplus ? softplus(xdt) : xdt;
       }
+      float run = dtv * A2;
 #pragma unroll
-      for (int j = 0; j < P / 8; ++j) cp_async16_zfill(uX + j * (Q * 16) + s * 16, xrow + j * 8, valid);
-      cp_async_commit();
-    }
-    float dtv = 0.f;
-    if (valid) {
-      const float xdt = __bfloat162float(p.dt[tok * H + h]) + bias;
-      dtv = p.softplus ? softplus(xdt) : xdt;
-    }
-    float run = dtv * A2;  // inclusive scan of dt*A*log2e over the chunk's steps
+      for (int o = 1; o < 32; o <<= 1) {
+        const float v = __shfl_up_sync(0xffffffffu, run, o);
+        if (lane >= o) run += v;
+      }
+      if (lane == 31) wsum[warp] = run;
+      dts[r] = dtv;
+      asm volatile("bar.sync 1, 128;" ::: "memory");  // warps 0-3 only
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const float v = __shfl_up_sync(0xffffffffu, run, o);
-      if (lane >= o) run += v;
+      for (int w = 0; w < 3; ++w)
+        if (w < warp) run += wsum[w];
+      cum[r] = run;
     }
-    if (lane == 31) wsum[warp] = run;
-    __syncthreads();
-#pragma unroll
-    for (int w = 0; w < 4; ++w)
-      if (w < warp) run += wsum[w];
-    cum[s] = run;
-    dts[s] = dtv;
-    cp_async_wait<0>();
-    fence_async_smem();
-    __syncthreads();
+    ok = __syncthreads_and(mbar_wait(ulbar, lparity));  // chunk c's copies have landed
+    lparity ^= 1;
+    if (!ok) break;
 
     // ---- CB = C B^T, Y_in = C H^T
     if (tid == 0) {
@@ -264,36 +295,65 @@ __global__ void __launch_bounds__(kSsdThreads, 2) ss_ssd_fwd(const SsdParams p) 
       }
       umma_commit(ubar);
     }
+    // factors of the below-diagonal 32 x 32 blocks: exp2(cum_t - cum_s) =
+    // exp2(cum_t - cum_e) exp2(cum_e - cum_s), e the block's last column; both
+    // exponents are <= 0 there (the decay only shrinks), so neither overflows
+    if (hf == 0) gs[r] = ex2(cum[r | 31] - cum[r]) * dts[r];
     ok = __syncthreads_and(mbar_wait(ubar, parity));
     parity ^= 1;
     tc_fence_after();
     if (!ok) break;
 
-    // ---- M from CB (row t = tid) into C's buffer; w.x (row s = tid) into H's
+    // ---- M (row t = r) into C's buffer: D on the diagonal, zero above it
     {
-      const int t = tid;
+      const int t = r;
       const float ct = cum[t];
-#pragma unroll
-      for (int q = 0; q < Q / 32; ++q) {
+      auto store8 = [&](int jb, const float (&m)[8]) {
+        *reinterpret_cast<uint4*>(sC + jb * (Q * 16) + t * 16) =
+            make_uint4(bf16x2(m[0], m[1]), bf16x2(m[2], m[3]), bf16x2(m[4], m[5]),
+                       bf16x2(m[6], m[7]));
+      };
+      if (hf == 0) {  // the diagonal block q4: exp2(cum_t - cum_s) per element
         float cb[32];
-        tmem_ld32(tlane + q * 32, cb);
+        tmem_ld32(tlane + q4 * 32, cb);
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          uint32_t w4[4];
+          float m[8];
 #pragma unroll
-          for (int e = 0; e < 8; e += 2) {
-            const int s0 = q * 32 + k * 8 + e;
-            const float m0 = s0 <= t ? cb[k * 8 + e] * ex2(ct - cum[s0]) * dts[s0] : 0.f;
-            const float m1 = s0 + 1 <= t ? cb[k * 8 + e + 1] * ex2(ct - cum[s0 + 1]) * dts[s0 + 1] : 0.f;
-            w4[e / 2] = bf16x2(m0, m1);
+          for (int e = 0; e < 8; ++e) {
+            const int s = q4 * 32 + k * 8 + e;
+            const float v = cb[k * 8 + e] * ex2(ct - cum[s]) * dts[s];
+            m[e] = s < t ? v : (s == t ? v + Dh : 0.f);
           }
-          *reinterpret_cast<uint4*>(sC + (q * 4 + k) * (Q * 16) + t * 16) =
-              make_uint4(w4[0], w4[1], w4[2], w4[3]);
+          store8(q4 * 4 + k, m);
+        }
+      } else {  // blocks q < q4 factorised, blocks q > q4 zero
+#pragma unroll
+        for (int q = 0; q < Q / 32; ++q) {
+          if (q < q4) {
+            float cb[32];
+            tmem_ld32(tlane + q * 32, cb);
+            const float et = ex2(ct - cum[q * 32 + 31]);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              float m[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) m[e] = cb[k * 8 + e] * et * gs[q * 32 + k * 8 + e];
+              store8(q * 4 + k, m);
+            }
+          } else if (q > q4) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              *reinterpret_cast<uint4*>(sC + (q * 4 + k) * (Q * 16) + t * 16) = make_uint4(0, 0, 0, 0);
+          }
         }
       }
+      // w.x (row s = r, columns [32 hf, 32 hf + 32)) into H's buffer
+      const int s = r;
       const float ws = ex2(cum[Q - 1] - cum[s]) * dts[s];
 #pragma unroll
-      for (int j = 0; j < P / 8; ++j) {
+      for (int jj = 0; jj < P / 16; ++jj) {
+        const int j = hf * (P / 16) + jj;
         const uint4 v = *reinterpret_cast<const uint4*>(sX + j * (Q * 16) + s * 16);
         *reinterpret_cast<uint4*>(sH + j * (Q * 16) + s * 16) =
             make_uint4(bf16x2(bf_lo(v.x) * ws, bf_hi(v.x) * ws), bf16x2(bf_lo(v.y) * ws, bf_hi(v.y) * ws),
@@ -304,7 +364,7 @@ __global__ void __launch_bounds__(kSsdThreads, 2) ss_ssd_fwd(const SsdParams p) 
     tc_fence_before();
     __syncthreads();
 
-    // ---- Y_dg = M X, S = B^T (w.x)
+    // ---- Y_dg = M X (with the skip), S = B^T (w.x)
     if (tid == 0) {
       tc_fence_after();
 #pragma unroll
@@ -320,54 +380,41 @@ __global__ void __launch_bounds__(kSsdThreads, 2) ss_ssd_fwd(const SsdParams p) 
     parity ^= 1;
     tc_fence_after();
     if (!ok) break;
+    // the shared operands are consumed: the next chunk's copies overlap the epilogue
+    if (c + 1 < nchunks) issue(c + 1, dt_raw);
 
-    // ---- state (row n = tid): H <- exp(cum_end) H + S^T, then its bf16 copy
+    // ---- state (row n = r): H <- exp(cum_end) H + S^T, then its bf16 copy
     {
-      const int n = tid;
+      const int n = r;
       const float decay = ex2(cum[Q - 1]);
+      float sv[32];
+      tmem_ld32(tlane + hf * 32, sv);
 #pragma unroll
-      for (int q = 0; q < P / 32; ++q) {
-        float sv[32];
-        tmem_ld32(tlane + q * 32, sv);
+      for (int i = 0; i < 32; ++i) hs[i] = fmaf(decay, hs[i], sv[i]);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) hs[q * 32 + i] = fmaf(decay, hs[q * 32 + i], sv[i]);
-      }
-#pragma unroll
-      for (int j = 0; j < P / 8; ++j)
-        *reinterpret_cast<uint4*>(sH + j * (N / 8 * 128) + n * 16) =
-            make_uint4(bf16x2(hs[j * 8 + 0], hs[j * 8 + 1]), bf16x2(hs[j * 8 + 2], hs[j * 8 + 3]),
-                       bf16x2(hs[j * 8 + 4], hs[j * 8 + 5]), bf16x2(hs[j * 8 + 6], hs[j * 8 + 7]));
+      for (int jj = 0; jj < 4; ++jj)
+        *reinterpret_cast<uint4*>(sH + (hf * 4 + jj) * (N / 8 * 128) + n * 16) =
+            make_uint4(bf16x2(hs[jj * 8 + 0], hs[jj * 8 + 1]), bf16x2(hs[jj * 8 + 2], hs[jj * 8 + 3]),
+                       bf16x2(hs[jj * 8 + 4], hs[jj * 8 + 5]), bf16x2(hs[jj * 8 + 6], hs[jj * 8 + 7]));
     }
-    // ---- output (row t = tid): y = exp(cum_t) Y_in + Y_dg + D x
+    // ---- output (row t = r, columns [32 hf, 32 hf + 32)): y = exp(cum_t) Y_in + Y_dg
     {
-      const int t = tid;
-      const float et = ex2(cum[t]);
-      __nv_bfloat16* yrow = p.y + ((b * L + t0 + t) * H + h) * P;
+      const int t = r;
+      float yd[32], yi[32];
+      tmem_ld32(tlane + 192 + hf * 32, yd);
+      if (c > 0) {
+        tmem_ld32(tlane + 128 + hf * 32, yi);
+        const float et = ex2(cum[t]);
 #pragma unroll
-      for (int q = 0; q < P / 32; ++q) {
-        float yd[32], yi[32];
-        tmem_ld32(tlane + 192 + q * 32, yd);
-        if (c > 0) {
-          tmem_ld32(tlane + 128 + q * 32, yi);
-        } else {
+        for (int i = 0; i < 32; ++i) yd[i] = fmaf(et, yi[i], yd[i]);
+      }
+      if (t < len) {
+        __nv_bfloat16* yrow = p.y + ((b * L + t0 + t) * H + h) * P + hf * 32;
 #pragma unroll
-          for (int i = 0; i < 32; ++i) yi[i] = 0.f;
-        }
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int j = q * 4 + k;  // p block of 8
-          const uint4 xv = *reinterpret_cast<const uint4*>(sX + j * (Q * 16) + t * 16);
-          const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
-          uint32_t o[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int i0 = k * 8 + 2 * e;
-            const float y0 = fmaf(et, yi[i0], fmaf(Dh, bf_lo(xw[e]), yd[i0]));
-            const float y1 = fmaf(et, yi[i0 + 1], fmaf(Dh, bf_hi(xw[e]), yd[i0 + 1]));
-            o[e] = bf16x2(y0, y1);
-          }
-          if (t < len) *reinterpret_cast<uint4*>(yrow + j * 8) = make_uint4(o[0], o[1], o[2], o[3]);
-        }
+        for (int k = 0; k < 4; ++k)
+          *reinterpret_cast<uint4*>(yrow + k * 8) =
+              make_uint4(bf16x2(yd[k * 8 + 0], yd[k * 8 + 1]), bf16x2(yd[k * 8 + 2], yd[k * 8 + 3]),
+                         bf16x2(yd[k * 8 + 4], yd[k * 8 + 5]), bf16x2(yd[k * 8 + 6], yd[k * 8 + 7]));
       }
     }
     fence_async_smem();
@@ -376,9 +423,9 @@ __global__ void __launch_bounds__(kSsdThreads, 2) ss_ssd_fwd(const SsdParams p) 
   }
 
   if (ok && p.final_state) {
-    float* fs = p.final_state + (b * H + h) * P * N;
+    float* fs = p.final_state + (b * H + h) * P * N + (int64_t)(hf * 32) * N;
 #pragma unroll
-    for (int i = 0; i < P; ++i) fs[i * N + tid] = hs[i];
+    for (int i = 0; i < P / 2; ++i) fs[i * N + r] = hs[i];
   }
   tc_fence_before();
   __syncthreads();
