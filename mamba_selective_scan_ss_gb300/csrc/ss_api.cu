@@ -38,7 +38,7 @@ bool range_overlap(const void* a, int64_t a_bytes, const void* b, int64_t b_byte
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 // A TMA descriptor of a bf16 tensor [d2][d1][d0] (d0 contiguous) read in boxes
-// of 8 x 128 x 1 elements, without swizzle; elements past d1 read as zero.
+// of 64 x 128 x 1 elements, 128-byte swizzled; elements past d1 read as zero.
 bool tma_map_rows(CUtensorMap* map, const void* base, int64_t d0, int64_t d1, int64_t d2) {
   static PFN_cuTensorMapEncodeTiled_v12000 encode = [] {
     void* fn = nullptr;
@@ -52,10 +52,10 @@ bool tma_map_rows(CUtensorMap* map, const void* base, int64_t d0, int64_t d1, in
   if (!encode) return false;
   const cuuint64_t dims[3] = {(cuuint64_t)d0, (cuuint64_t)d1, (cuuint64_t)d2};
   const cuuint64_t strides[2] = {(cuuint64_t)d0 * 2, (cuuint64_t)(d0 * d1) * 2};
-  const cuuint32_t box[3] = {8, 128, 1};
+  const cuuint32_t box[3] = {64, 128, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
-                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                 CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }

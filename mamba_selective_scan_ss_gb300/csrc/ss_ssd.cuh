@@ -21,12 +21,13 @@
 //
 // The four products are tcgen05.mma kind::f16 (bf16 operands from shared
 // memory, fp32 accumulators in tensor memory), issued by one thread and
-// completed through an mbarrier; thread i of the CTA owns tensor-memory lane i
-// (row t of CB and Y, row n of S).  Operands use the no-swizzle canonical
-// layouts: 16-byte rows of 8 elements, a row block of 8 rows at 128 bytes, so
-// a thread that owns a row writes one 16-byte chunk per 8 columns and a warp's
-// chunks are contiguous.  B serves as the CB operand (K-major, K = n) and as
-// the state product's A operand (MN-major, K = s) from the same bytes.
+// completed through an mbarrier; threads own tensor-memory lanes (rows t of CB
+// and Y, rows n of S).  Every operand uses the 128-byte-swizzle layout: rows of
+// 64 elements (128 bytes) whose 16-byte chunks are XOR-permuted by the row
+// index mod 8, 8-row groups 1024 bytes apart, which is what TMA writes for a
+// 64 x 128 box and what lets a warp write a chunk of 32 rows without bank
+// conflicts.  B serves as the CB operand (K-major, K = n) and as the state
+// product's A operand (MN-major, K = s) from the same bytes.
 #pragma once
 
 #include <cuda.h>
@@ -42,10 +43,11 @@ constexpr int kSsdN = 128;  // dstate
 constexpr int kSsdThreads = 256;
 
 // shared-memory map (bytes from the 1024-aligned dynamic base)
-constexpr uint32_t kSsdOffC = 0;           // C [t][n] K-major, then M [t][s] K-major
-constexpr uint32_t kSsdOffB = 32768;       // B [s][n]
-constexpr uint32_t kSsdOffX = 65536;       // x [s][p] MN-major
-constexpr uint32_t kSsdOffH = 81920;       // H [n][p] MN-major, then w.x [s][p]
+constexpr uint32_t kSsdOffC = 0;           // C [t][n], then M [t][s]: two 64-column halves
+constexpr uint32_t kSsdOffB = 32768;       // B [s][n]: two 64-column halves
+constexpr uint32_t kSsdOffX = 65536;       // x [s][p]
+constexpr uint32_t kSsdOffH = 81920;       // H [n][p], then w.x [s][p]
+constexpr uint32_t kSsdHalf = 16384;       // bytes of a 64-column half of a 128-row tile
 constexpr uint32_t kSsdOffCum = 98304;     // cum [Q] fp32
 constexpr uint32_t kSsdOffDt = 98816;      // dt [Q] fp32
 constexpr uint32_t kSsdOffG = 99328;       // block factors [Q] fp32
@@ -54,8 +56,9 @@ constexpr uint32_t kSsdSmemBytes = 99840 + 64;
 constexpr uint32_t kSsdTmemCols = 256;     // CB / S [0,128), Y_in [128,192), Y_dg [192,256)
 
 struct SsdParams {
-  // TMA descriptors (3-D: columns, steps, batch; boxes of 8 columns x 128
-  // steps, zero past the sequence's end) of x [b,L,H*P] and B, C [b,L,G*N]
+  // TMA descriptors (3-D: columns, steps, batch; 128-byte-swizzled boxes of
+  // 64 columns x 128 steps, zero past the sequence's end) of x [b,L,H*P] and
+  // B, C [b,L,G*N]
   CUtensorMap tx, tb, tc;
   const __nv_bfloat16* x;   // [b,L,H,P]
   const __nv_bfloat16* dt;  // [b,L,H]
@@ -74,12 +77,23 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-// Shared-memory matrix descriptor, no swizzle: start, leading-dimension byte
-// offset (between 8-element blocks along K), stride byte offset (between
-// 8-row blocks along M or N), descriptor version 1.
-__device__ __forceinline__ uint64_t umma_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+// Shared-memory matrix descriptor of a 128-byte-swizzled operand: start,
+// leading byte offset (MN-major: between 64-element atoms along M or N; unused
+// by K-major), stride byte offset (between 8-row groups: 1024), version 1,
+// layout 2 (128-byte swizzle).  A K-major operand steps through K inside an
+// atom by moving the start 32 bytes per 16 elements.
+__device__ __forceinline__ uint64_t umma_desc(uint32_t addr, uint32_t lbo) {
   return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
-         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46);
+         ((uint64_t)(1024 >> 4) << 32) | (1ull << 46) | (2ull << 61);
+}
+// start of K step ks (16 elements) of a K-major tile whose K = 128 is split in
+// two 64-column halves
+__device__ __forceinline__ uint32_t kmajor_step(uint32_t base, int ks) {
+  return base + (ks >> 2) * kSsdHalf + (ks & 3) * 32;
+}
+// byte offset of 16-byte chunk c (columns 8c..8c+7 of a 64-column half) of row r
+__device__ __forceinline__ uint32_t sw128(int r, int c) {
+  return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4));
 }
 
 // Instruction descriptor of kind::f16: fp32 accumulator, bf16 A and B, M = 128,
@@ -146,8 +160,8 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// One TMA box (8 columns x 128 steps of one batch row) into shared memory:
-// 128 rows of 16 bytes, one 2 KB slab of the no-swizzle operand layout.
+// One TMA box (64 columns x 128 steps of one batch row) into shared memory:
+// 128 rows of 128 bytes, 128-byte swizzled (16 KB).
 __device__ __forceinline__ void tma_load3(uint32_t dst, const CUtensorMap* map, int c0, int c1,
                                           int c2, uint32_t bar) {
   asm volatile(
@@ -200,6 +214,10 @@ __global__ void __launch_bounds__(kSsdThreads, 2) ss_ssd_fwd(const __grid_consta
                  uH = smem_u32(sH);
   const uint32_t ubar = smem_u32(bar), ulbar = smem_u32(lbar);
 
+  if (smem_u32(smem) & 1023u) {  // the swizzled TMA boxes need a 1024-byte aligned base
+    if (tid == 0) atomicOr(&g_ss_device_error, kErrTimeout);
+    return;
+  }
   if (tid == 0) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(ubar));
     asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(ulbar));
@@ -229,15 +247,13 @@ __global__ void __launch_bounds__(kSsdThreads, 2) ss_ssd_fwd(const __grid_consta
   auto issue = [&](int64_t c, float& dt_raw) {
     const int64_t t0 = c * Q;
     if (tid == 0) {
-      mbar_expect_tx(ulbar, (2 * (N / 8) + P / 8) * Q * 16);
+      mbar_expect_tx(ulbar, (2 * (N / 64) + P / 64) * kSsdHalf);
 #pragma unroll
-      for (int j = 0; j < N / 8; ++j) {
-        tma_load3(uC + j * (Q * 16), &p.tc, (int)(g * N + 8 * j), (int)t0, (int)b, ulbar);
-        tma_load3(uB + j * (Q * 16), &p.tb, (int)(g * N + 8 * j), (int)t0, (int)b, ulbar);
+      for (int a = 0; a < N / 64; ++a) {
+        tma_load3(uC + a * kSsdHalf, &p.tc, (int)(g * N + 64 * a), (int)t0, (int)b, ulbar);
+        tma_load3(uB + a * kSsdHalf, &p.tb, (int)(g * N + 64 * a), (int)t0, (int)b, ulbar);
       }
-#pragma unroll
-      for (int j = 0; j < P / 8; ++j)
-        tma_load3(uX + j * (Q * 16), &p.tx, (int)(h * P + 8 * j), (int)t0, (int)b, ulbar);
+      tma_load3(uX, &p.tx, (int)(h * P), (int)t0, (int)b, ulbar);
     }
     const bool valid = hf == 0 && t0 + r < L;
     dt_raw = valid ? __bfloat162float(p.dt[(b * L + t0 + r) * H + h]) : 0.f;
@@ -285,13 +301,13 @@ __global__ void __launch_bounds__(kSsdThreads, 2) ss_ssd_fwd(const __grid_consta
       tc_fence_after();
 #pragma unroll
       for (int ks = 0; ks < N / 16; ++ks)
-        umma(tm + 0, umma_desc(uC + ks * 2 * (Q * 16), Q * 16, 128),
-             umma_desc(uB + ks * 2 * (Q * 16), Q * 16, 128), kIdCB, ks > 0);
+        umma(tm + 0, umma_desc(kmajor_step(uC, ks), 16), umma_desc(kmajor_step(uB, ks), 16), kIdCB,
+             ks > 0);
       if (c > 0) {
 #pragma unroll
         for (int ks = 0; ks < N / 16; ++ks)
-          umma(tm + 128, umma_desc(uC + ks * 2 * (Q * 16), Q * 16, 128),
-               umma_desc(uH + ks * 2 * 128, 128, N / 8 * 128), kIdY, ks > 0);
+          umma(tm + 128, umma_desc(kmajor_step(uC, ks), 16), umma_desc(uH + ks * 2048, 16), kIdY,
+               ks > 0);
       }
       umma_commit(ubar);
     }
@@ -308,8 +324,8 @@ __global__ void __launch_bounds__(kSsdThreads, 2) ss_ssd_fwd(const __grid_consta
     {
       const int t = r;
       const float ct = cum[t];
-      auto store8 = [&](int jb, const float (&m)[8]) {
-        *reinterpret_cast<uint4*>(sC + jb * (Q * 16) + t * 16) =
+      auto store8 = [&](int jb, const float (&m)[8]) {  // columns 8 jb .. 8 jb + 7
+        *reinterpret_cast<uint4*>(sC + (jb >> 3) * kSsdHalf + sw128(t, jb & 7)) =
             make_uint4(bf16x2(m[0], m[1]), bf16x2(m[2], m[3]), bf16x2(m[4], m[5]),
                        bf16x2(m[6], m[7]));
       };
@@ -344,7 +360,8 @@ __global__ void __launch_bounds__(kSsdThreads, 2) ss_ssd_fwd(const __grid_consta
           } else if (q > q4) {
 #pragma unroll
             for (int k = 0; k < 4; ++k)
-              *reinterpret_cast<uint4*>(sC + (q * 4 + k) * (Q * 16) + t * 16) = make_uint4(0, 0, 0, 0);
+              *reinterpret_cast<uint4*>(sC + ((q * 4 + k) >> 3) * kSsdHalf + sw128(t, (q * 4 + k) & 7)) =
+                  make_uint4(0, 0, 0, 0);
           }
         }
       }
@@ -354,8 +371,8 @@ __global__ void __launch_bounds__(kSsdThreads, 2) ss_ssd_fwd(const __grid_consta
 #pragma unroll
       for (int jj = 0; jj < P / 16; ++jj) {
         const int j = hf * (P / 16) + jj;
-        const uint4 v = *reinterpret_cast<const uint4*>(sX + j * (Q * 16) + s * 16);
-        *reinterpret_cast<uint4*>(sH + j * (Q * 16) + s * 16) =
+        const uint4 v = *reinterpret_cast<const uint4*>(sX + sw128(s, j));
+        *reinterpret_cast<uint4*>(sH + sw128(s, j)) =
             make_uint4(bf16x2(bf_lo(v.x) * ws, bf_hi(v.x) * ws), bf16x2(bf_lo(v.y) * ws, bf_hi(v.y) * ws),
                        bf16x2(bf_lo(v.z) * ws, bf_hi(v.z) * ws), bf16x2(bf_lo(v.w) * ws, bf_hi(v.w) * ws));
       }
@@ -369,10 +386,10 @@ __global__ void __launch_bounds__(kSsdThreads, 2) ss_ssd_fwd(const __grid_consta
       tc_fence_after();
 #pragma unroll
       for (int ks = 0; ks < Q / 16; ++ks) {
-        umma(tm + 192, umma_desc(uC + ks * 2 * (Q * 16), Q * 16, 128),
-             umma_desc(uX + ks * 2 * 128, 128, Q / 8 * 128), kIdY, ks > 0);
-        umma(tm + 0, umma_desc(uB + ks * 2 * 128, 128, Q / 8 * 128),
-             umma_desc(uH + ks * 2 * 128, 128, Q / 8 * 128), kIdS, ks > 0);
+        umma(tm + 192, umma_desc(kmajor_step(uC, ks), 16), umma_desc(uX + ks * 2048, 16), kIdY,
+             ks > 0);
+        umma(tm + 0, umma_desc(uB + ks * 2048, kSsdHalf), umma_desc(uH + ks * 2048, 16), kIdS,
+             ks > 0);
       }
       umma_commit(ubar);
     }
@@ -393,7 +410,7 @@ __global__ void __launch_bounds__(kSsdThreads, 2) ss_ssd_fwd(const __grid_consta
       for (int i = 0; i < 32; ++i) hs[i] = fmaf(decay, hs[i], sv[i]);
 #pragma unroll
       for (int jj = 0; jj < 4; ++jj)
-        *reinterpret_cast<uint4*>(sH + (hf * 4 + jj) * (N / 8 * 128) + n * 16) =
+        *reinterpret_cast<uint4*>(sH + sw128(n, hf * 4 + jj)) =
             make_uint4(bf16x2(hs[jj * 8 + 0], hs[jj * 8 + 1]), bf16x2(hs[jj * 8 + 2], hs[jj * 8 + 3]),
                        bf16x2(hs[jj * 8 + 4], hs[jj * 8 + 5]), bf16x2(hs[jj * 8 + 6], hs[jj * 8 + 7]));
     }
