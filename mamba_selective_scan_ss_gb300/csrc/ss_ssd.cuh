@@ -48,11 +48,12 @@ constexpr uint32_t kSsdOffB = 32768;       // B [s][n]: two 64-column halves
 constexpr uint32_t kSsdOffX = 65536;       // x [s][p]
 constexpr uint32_t kSsdOffH = 81920;       // H [n][p], then w.x [s][p]
 constexpr uint32_t kSsdHalf = 16384;       // bytes of a 64-column half of a 128-row tile
-constexpr uint32_t kSsdOffCum = 98304;     // cum [Q] fp32
-constexpr uint32_t kSsdOffDt = 98816;      // dt [Q] fp32
-constexpr uint32_t kSsdOffG = 99328;       // block factors [Q] fp32
-constexpr uint32_t kSsdOffMisc = 99840;    // warp sums, mbarrier, tensor-memory address
-constexpr uint32_t kSsdSmemBytes = 99840 + 64;
+// per-step tables of two chunks (this one and the next): fp32 [2][Q] each
+constexpr uint32_t kSsdOffCum = 98304;     // decay sums cum
+constexpr uint32_t kSsdOffDt = 99328;      // dt
+constexpr uint32_t kSsdOffG = 100352;      // block factors
+constexpr uint32_t kSsdOffMisc = 101376;   // warp sums, mbarriers, tensor-memory address
+constexpr uint32_t kSsdSmemBytes = 101376 + 64;
 constexpr uint32_t kSsdTmemCols = 256;     // CB / S [0,128), Y_in [128,192), Y_dg [192,256)
 
 struct SsdParams {
@@ -133,9 +134,9 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
   return false;
 }
 
-// 32 consecutive fp32 columns of this warp's 32 tensor-memory lanes.
-__device__ __forceinline__ void tmem_ld32(uint32_t addr, float (&v)[32]) {
-  uint32_t r[32];
+// Start reading 32 consecutive fp32 columns of this warp's 32 tensor-memory
+// lanes; the values are valid after tmem_wait on the same array.
+__device__ __forceinline__ void tmem_ld32_async(uint32_t addr, uint32_t (&r)[32]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
       "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
@@ -145,10 +146,21 @@ __device__ __forceinline__ void tmem_ld32(uint32_t addr, float (&v)[32]) {
         "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
         "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
       : "r"(addr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
+// Wait for this thread's tensor-memory reads; the array is an operand so that
+// no use of it is scheduled before the wait.
+__device__ __forceinline__ void tmem_wait(uint32_t (&r)[32]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                 "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                 "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]),
+                 "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]),
+                 "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]),
+                 "+r"(r[30]), "+r"(r[31])
+               :
+               : "memory");
+}
+__device__ __forceinline__ float fu(uint32_t v) { return __uint_as_float(v); }
 
 __device__ __forceinline__ void fence_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -203,9 +215,9 @@ __global__ void __launch_bounds__(kSsdThreads, 2) ss_ssd_fwd(const __grid_consta
   unsigned char* sC = smem + kSsdOffC;
   unsigned char* sX = smem + kSsdOffX;
   unsigned char* sH = smem + kSsdOffH;
-  float* cum = reinterpret_cast<float*>(smem + kSsdOffCum);
-  float* dts = reinterpret_cast<float*>(smem + kSsdOffDt);
-  float* gs = reinterpret_cast<float*>(smem + kSsdOffG);
+  float* cum2 = reinterpret_cast<float*>(smem + kSsdOffCum);
+  float* dts2 = reinterpret_cast<float*>(smem + kSsdOffDt);
+  float* gs2 = reinterpret_cast<float*>(smem + kSsdOffG);
   float* wsum = reinterpret_cast<float*>(smem + kSsdOffMisc);
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kSsdOffMisc + 32);   // products
   uint64_t* lbar = reinterpret_cast<uint64_t*>(smem + kSsdOffMisc + 40);  // copies
@@ -244,19 +256,51 @@ __global__ void __launch_bounds__(kSsdThreads, 2) ss_ssd_fwd(const __grid_consta
 
   // chunk c's rows of C, B and x by TMA (thread 0; completes on lbar), and
   // its dt (warps 0-3, row r)
-  auto issue = [&](int64_t c, float& dt_raw) {
-    const int64_t t0 = c * Q;
-    if (tid == 0) {
-      mbar_expect_tx(ulbar, (2 * (N / 64) + P / 64) * kSsdHalf);
-#pragma unroll
-      for (int a = 0; a < N / 64; ++a) {
-        tma_load3(uC + a * kSsdHalf, &p.tc, (int)(g * N + 64 * a), (int)t0, (int)b, ulbar);
-        tma_load3(uB + a * kSsdHalf, &p.tb, (int)(g * N + 64 * a), (int)t0, (int)b, ulbar);
+  const unsigned short* dt_bits = reinterpret_cast<const unsigned short*>(p.dt);
+  auto load_dt = [&](int64_t c) -> uint32_t {  // raw bf16 bits of chunk c's dt (warps 0-3)
+    const int64_t t = c * Q + r;
+    return (hf == 0 && t < L) ? (uint32_t)dt_bits[(b * L + t) * H + h] : 0u;
+  };
+  // (lane 0 of warps 0-4 each issue one box; warp 0 also posts the byte count)
+  auto issue = [&](int64_t c) {
+    const int t0 = (int)(c * Q);
+    if (lane == 0 && warp < 5) {
+      if (warp == 0) mbar_expect_tx(ulbar, (2 * (N / 64) + P / 64) * kSsdHalf);
+      if (warp < 4) {
+        const int a = warp & 1;
+        tma_load3((warp < 2 ? uC : uB) + a * kSsdHalf, warp < 2 ? &p.tc : &p.tb,
+                  (int)(g * N + 64 * a), t0, (int)b, ulbar);
+      } else {
+        tma_load3(uX, &p.tx, (int)(h * P), t0, (int)b, ulbar);
       }
-      tma_load3(uX, &p.tx, (int)(h * P), (int)t0, (int)b, ulbar);
     }
-    const bool valid = hf == 0 && t0 + r < L;
-    dt_raw = valid ? __bfloat162float(p.dt[(b * L + t0 + r) * H + h]) : 0.f;
+  };
+  // decay sums, dt and block factors of chunk cc into table buf (warps 0-3,
+  // row s = r): cum_s = sum_{r<=s} dt_r A log2e, and the factors of the
+  // below-diagonal 32 x 32 blocks: exp2(cum_t - cum_s) = exp2(cum_t - cum_e)
+  // exp2(cum_e - cum_s), e the block's last column; both exponents are <= 0
+  // there (the decay only shrinks), so neither overflows
+  auto scan_chunk = [&](int64_t cc, uint32_t bits, int buf) {
+    float dtv = 0.f;
+    if (cc * Q + r < L) {
+      const float xdt = __uint_as_float(bits << 16) + bias;
+      dtv = p.softplus ? lo_of(softplus2(splat(xdt))) : xdt;
+    }
+    float run = dtv * A2;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float v = __shfl_up_sync(0xffffffffu, run, o);
+      if (lane >= o) run += v;
+    }
+    if (lane == 31) wsum[warp] = run;
+    dts2[buf * Q + r] = dtv;
+    asm volatile("bar.sync 1, 128;" ::: "memory");  // warps 0-3 only
+#pragma unroll
+    for (int w = 0; w < 3; ++w)
+      if (w < warp) run += wsum[w];
+    cum2[buf * Q + r] = run;
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+    gs2[buf * Q + r] = ex2(cum2[buf * Q + (r | 31)] - run) * dtv;
   };
 
   constexpr uint32_t kIdCB = umma_idesc(128, 0, 0);
@@ -265,33 +309,19 @@ __global__ void __launch_bounds__(kSsdThreads, 2) ss_ssd_fwd(const __grid_consta
   uint32_t parity = 0, lparity = 0;
   bool ok = true;
   const int64_t nchunks = (L + Q - 1) / Q;
-  float dt_raw;
-  issue(0, dt_raw);
+  issue(0);
+  // the tables of chunk 0 now; those of chunk c + 1 while the tensor cores run
+  // chunk c's second pair of products (dt is loaded a chunk before it is used)
+  if (hf == 0) scan_chunk(0, load_dt(0), 0);
+  uint32_t dt_nxt = load_dt(1);
   for (int64_t c = 0; c < nchunks && ok; ++c) {
     const int64_t t0 = c * Q;
     const int len = (int)(L - t0 < Q ? L - t0 : Q);
+    const int buf = (int)(c & 1);
+    const float* cum = cum2 + buf * Q;
+    const float* dts = dts2 + buf * Q;
+    const float* gs = gs2 + buf * Q;
 
-    // ---- in-chunk decay sums (warps 0-3, row s = r): cum_s = sum_{r<=s} dt_r A log2e
-    if (hf == 0) {
-      float dtv = 0.f;
-      if (r < len) {
-        const float xdt = dt_raw + bias;
-        dtv = p.softplus ? softplus(xdt) : xdt;
-      }
-      float run = dtv * A2;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const float v = __shfl_up_sync(0xffffffffu, run, o);
-        if (lane >= o) run += v;
-      }
-      if (lane == 31) wsum[warp] = run;
-      dts[r] = dtv;
-      asm volatile("bar.sync 1, 128;" ::: "memory");  // warps 0-3 only
-#pragma unroll
-      for (int w = 0; w < 3; ++w)
-        if (w < warp) run += wsum[w];
-      cum[r] = run;
-    }
     ok = __syncthreads_and(mbar_wait(ulbar, lparity));  // chunk c's copies have landed
     lparity ^= 1;
     if (!ok) break;
@@ -311,10 +341,6 @@ __global__ void __launch_bounds__(kSsdThreads, 2) ss_ssd_fwd(const __grid_consta
       }
       umma_commit(ubar);
     }
-    // factors of the below-diagonal 32 x 32 blocks: exp2(cum_t - cum_s) =
-    // exp2(cum_t - cum_e) exp2(cum_e - cum_s), e the block's last column; both
-    // exponents are <= 0 there (the decay only shrinks), so neither overflows
-    if (hf == 0) gs[r] = ex2(cum[r | 31] - cum[r]) * dts[r];
     ok = __syncthreads_and(mbar_wait(ubar, parity));
     parity ^= 1;
     tc_fence_after();
@@ -329,35 +355,52 @@ __global__ void __launch_bounds__(kSsdThreads, 2) ss_ssd_fwd(const __grid_consta
             make_uint4(bf16x2(m[0], m[1]), bf16x2(m[2], m[3]), bf16x2(m[4], m[5]),
                        bf16x2(m[6], m[7]));
       };
-      if (hf == 0) {  // the diagonal block q4: exp2(cum_t - cum_s) per element
-        float cb[32];
-        tmem_ld32(tlane + q4 * 32, cb);
+      // block q (columns 32 q .. 32 q + 31) below the diagonal, from its CB values
+      auto full_block = [&](int q, const uint32_t (&cb)[32]) {
+        const float et = ex2(ct - cum[q * 32 + 31]);
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          float m[8];
+          float m[8], gv[8];
+          *reinterpret_cast<float4*>(gv) = *reinterpret_cast<const float4*>(gs + q * 32 + k * 8);
+          *reinterpret_cast<float4*>(gv + 4) = *reinterpret_cast<const float4*>(gs + q * 32 + k * 8 + 4);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) m[e] = fu(cb[k * 8 + e]) * et * gv[e];
+          store8(q * 4 + k, m);
+        }
+      };
+      if (hf == 0) {  // the diagonal block q4: exp2(cum_t - cum_s) per element
+        uint32_t cb[32];
+        tmem_ld32_async(tlane + q4 * 32, cb);
+        tmem_wait(cb);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          float m[8], cv[8], dv[8];
+          const int s0 = q4 * 32 + k * 8;
+          *reinterpret_cast<float4*>(cv) = *reinterpret_cast<const float4*>(cum + s0);
+          *reinterpret_cast<float4*>(cv + 4) = *reinterpret_cast<const float4*>(cum + s0 + 4);
+          *reinterpret_cast<float4*>(dv) = *reinterpret_cast<const float4*>(dts + s0);
+          *reinterpret_cast<float4*>(dv + 4) = *reinterpret_cast<const float4*>(dts + s0 + 4);
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
-            const int s = q4 * 32 + k * 8 + e;
-            const float v = cb[k * 8 + e] * ex2(ct - cum[s]) * dts[s];
+            const int s = s0 + e;
+            const float v = fu(cb[k * 8 + e]) * ex2(ct - cv[e]) * dv[e];
             m[e] = s < t ? v : (s == t ? v + Dh : 0.f);
           }
           store8(q4 * 4 + k, m);
         }
       } else {  // blocks q < q4 factorised, blocks q > q4 zero
 #pragma unroll
-        for (int q = 0; q < Q / 32; ++q) {
+        for (int q = 0; q < Q / 32 - 1; ++q) {
           if (q < q4) {
-            float cb[32];
-            tmem_ld32(tlane + q * 32, cb);
-            const float et = ex2(ct - cum[q * 32 + 31]);
+            uint32_t cb[32];
+            tmem_ld32_async(tlane + q * 32, cb);
+            tmem_wait(cb);
+            full_block(q, cb);
+          }
+        }
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              float m[8];
-#pragma unroll
-              for (int e = 0; e < 8; ++e) m[e] = cb[k * 8 + e] * et * gs[q * 32 + k * 8 + e];
-              store8(q * 4 + k, m);
-            }
-          } else if (q > q4) {
+        for (int q = 1; q < Q / 32; ++q) {
+          if (q > q4) {
 #pragma unroll
             for (int k = 0; k < 4; ++k)
               *reinterpret_cast<uint4*>(sC + ((q * 4 + k) >> 3) * kSsdHalf + sw128(t, (q * 4 + k) & 7)) =
@@ -393,21 +436,25 @@ __global__ void __launch_bounds__(kSsdThreads, 2) ss_ssd_fwd(const __grid_consta
       }
       umma_commit(ubar);
     }
+    if (hf == 0 && c + 1 < nchunks) scan_chunk(c + 1, dt_nxt, buf ^ 1);
     ok = __syncthreads_and(mbar_wait(ubar, parity));
     parity ^= 1;
     tc_fence_after();
     if (!ok) break;
     // the shared operands are consumed: the next chunk's copies overlap the epilogue
-    if (c + 1 < nchunks) issue(c + 1, dt_raw);
+    if (c + 1 < nchunks) issue(c + 1);
+    dt_nxt = load_dt(c + 2);
 
     // ---- state (row n = r): H <- exp(cum_end) H + S^T, then its bf16 copy
+    uint32_t sv[32], yd[32];
+    tmem_ld32_async(tlane + hf * 32, sv);
+    tmem_ld32_async(tlane + 192 + hf * 32, yd);  // Y_dg, for the output below
     {
       const int n = r;
       const float decay = ex2(cum[Q - 1]);
-      float sv[32];
-      tmem_ld32(tlane + hf * 32, sv);
+      tmem_wait(sv);
 #pragma unroll
-      for (int i = 0; i < 32; ++i) hs[i] = fmaf(decay, hs[i], sv[i]);
+      for (int i = 0; i < 32; ++i) hs[i] = fmaf(decay, hs[i], fu(sv[i]));
 #pragma unroll
       for (int jj = 0; jj < 4; ++jj)
         *reinterpret_cast<uint4*>(sH + sw128(n, hf * 4 + jj)) =
@@ -417,21 +464,25 @@ __global__ void __launch_bounds__(kSsdThreads, 2) ss_ssd_fwd(const __grid_consta
     // ---- output (row t = r, columns [32 hf, 32 hf + 32)): y = exp(cum_t) Y_in + Y_dg
     {
       const int t = r;
-      float yd[32], yi[32];
-      tmem_ld32(tlane + 192 + hf * 32, yd);
-      if (c > 0) {
-        tmem_ld32(tlane + 128 + hf * 32, yi);
-        const float et = ex2(cum[t]);
+      tmem_wait(yd);
+      float yv[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) yd[i] = fmaf(et, yi[i], yd[i]);
+      for (int i = 0; i < 32; ++i) yv[i] = fu(yd[i]);
+      if (c > 0) {
+        uint32_t yi[32];
+        tmem_ld32_async(tlane + 128 + hf * 32, yi);
+        const float et = ex2(cum[t]);
+        tmem_wait(yi);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) yv[i] = fmaf(et, fu(yi[i]), yv[i]);
       }
       if (t < len) {
         __nv_bfloat16* yrow = p.y + ((b * L + t0 + t) * H + h) * P + hf * 32;
 #pragma unroll
         for (int k = 0; k < 4; ++k)
           *reinterpret_cast<uint4*>(yrow + k * 8) =
-              make_uint4(bf16x2(yd[k * 8 + 0], yd[k * 8 + 1]), bf16x2(yd[k * 8 + 2], yd[k * 8 + 3]),
-                         bf16x2(yd[k * 8 + 4], yd[k * 8 + 5]), bf16x2(yd[k * 8 + 6], yd[k * 8 + 7]));
+              make_uint4(bf16x2(yv[k * 8 + 0], yv[k * 8 + 1]), bf16x2(yv[k * 8 + 2], yv[k * 8 + 3]),
+                         bf16x2(yv[k * 8 + 4], yv[k * 8 + 5]), bf16x2(yv[k * 8 + 6], yv[k * 8 + 7]));
       }
     }
     fence_async_smem();
