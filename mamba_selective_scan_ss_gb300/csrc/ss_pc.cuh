@@ -11,7 +11,10 @@
 // row and step against four row streams).  A group of S lanes (S a power of
 // two, dstate <= 4*S <= 128) serves one row; lane j holds states [4j, 4j+4)
 // and streams their B and C rows 32 bytes (8 fp32 or 16 bf16 steps) at a
-// time, a whole DRAM sector per row, used at once.  dt, du and
+// time, a whole DRAM sector per row, with the next 32 bytes' loads in flight.
+// One CTA per SM: with 64 rows per SM the partly read L2 lines of all row
+// streams (about 44 MB over the GPU) stay in L2 until they are used up, so
+// DRAM delivers each byte once.  dt, du and
 // the gate are computed by every lane of the row from the row's own vector
 // loads (the same 32 bytes for all its lanes); the read-out is summed over the
 // group by a butterfly of shuffles and lane 0 stores y.
@@ -91,7 +94,7 @@ struct PcStep {
 // grid = ceil(rows * 2^seg_shift / 256), block = 256.  VEC: seqlen a multiple
 // of kPcSteps and every row 16-byte aligned.
 template <typename T, bool HAS_Z, bool VEC>
-__global__ void __launch_bounds__(256) ss_fwd_pc(const PcParams p) {
+__global__ void __launch_bounds__(256, 1) ss_fwd_pc(const PcParams p) {
   constexpr int V = kPcSteps<T>;
   const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const int64_t row = gid >> p.seg_shift;
@@ -131,9 +134,16 @@ __global__ void __launch_bounds__(256) ss_fwd_pc(const PcParams p) {
       v.c[e].load(Cq[e], t, L);
     }
   };
-  PcStep<T, VEC, HAS_Z> cur;
+  // vector path: the next iteration's loads are in flight while this one is
+  // used; the element-wise path (a correctness path) loads at each iteration
+  PcStep<T, VEC, HAS_Z> cur, nxt;
+  if (VEC) load(0, cur);
   for (int64_t t0 = 0; t0 < L; t0 += V) {
-    load(t0, cur);
+    if (VEC) {
+      if (t0 + V < L) load(t0 + V, nxt);
+    } else {
+      load(t0, cur);
+    }
     float yv[V];
 #pragma unroll
     for (int s = 0; s < V; ++s) {
@@ -173,6 +183,7 @@ __global__ void __launch_bounds__(256) ss_fwd_pc(const PcParams p) {
           if (t0 + s < L) yo[s] = Elem<T>::from_f32(yv[s]);
       }
     }
+    if (VEC) cur = nxt;
   }
   if (active && p.last_state) {
 #pragma unroll
