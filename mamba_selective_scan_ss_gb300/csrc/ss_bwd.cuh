@@ -17,17 +17,17 @@
 // states (d(dt), du, the pre-gate read-out) stay inside the thread.  A CTA
 // holds 64 rows; the B/C values of each block of kBwdBlock steps are staged
 // once in shared memory and read as broadcasts.  The one exchange between
-// threads is the sum of dB/dC over the CTA's rows, step by step: every thread
-// writes its 32 contributions to a padded table and 32 threads add its
-// columns in row order.
+// threads is the sum of dB/dC over the rows, step by step and within each
+// warp (no CTA barrier): every thread writes its 32 contributions to a padded
+// table and lane k of the warp adds column k over the warp's 32 rows in order.
 //
 // Time: a forward pass stores the state every kBwdBlock steps (checkpoints in
 // scratch); the reverse pass then, block by block from the end, recomputes the
 // block's states from its checkpoint into shared memory and runs the reverse
 // recurrence over them (decays recomputed with ex2).
 //
-// Reductions are deterministic: dB/dC per CTA in row order, then
-// ss_bwd_reduce_bc over the CTAs of a batch row in order; dA, dD and dbias
+// Reductions are deterministic: dB/dC per warp in row order, then
+// ss_bwd_reduce_bc over the CTAs of a batch row and their warps in order; dA, dD and dbias
 // per (batch, channel), then ss_bwd_reduce_rows over the batch in order.
 #pragma once
 
@@ -97,6 +97,7 @@ __global__ void __launch_bounds__(kBwdThreads, 6) ss_bwd_main(const BwdParams p)
   __shared__ float bc[2][S][NT];                 // B, C of the block's steps
   __shared__ float hp[S][NT][kBwdRows];          // state before each step of the block
   __shared__ float red[kBwdRows][2 * NT + 1];    // one step's dC (0..15), dB (16..31) per row
+  __shared__ float wpart[kBwdRows / 32][S][2 * NT];  // the block's per-warp dC/dB sums
 
   const int tid = threadIdx.x;
   const int64_t cta = blockIdx.x;
@@ -250,15 +251,29 @@ __global__ void __launch_bounds__(kBwdThreads, 6) ss_bwd_main(const BwdParams p)
           static_cast<T*>(p.dz)[xi] = Elem<T>::from_f32(dz);
         }
       }
-      __syncthreads();
-      // dB/dC of step t over the CTA's rows, in row order
-      if (tid < 2 * NT) {
+      // dB/dC of step t over the warp's 32 rows, in row order: lane k sums
+      // column k (no CTA barrier); the two warps' sums meet once per block
+      __syncwarp();
+      {
+        const int lane = tid & 31, w = tid >> 5;
         float acc = 0.f;
-        for (int r = 0; r < kBwdRows; ++r) acc += red[r][tid];
-        const int m = tid < NT ? 1 : 0, nn = tid & (NT - 1);
-        p.part_bc[((cta * 2 + m) * NT + nn) * L + t] = acc;
+#pragma unroll 8
+        for (int r = 0; r < 32; ++r) acc += red[w * 32 + r][lane];
+        wpart[w][st][lane] = acc;
       }
-      __syncthreads();
+      __syncwarp();
+    }
+    // the block's dB/dC: the two warps' sums added, step by step
+    __syncthreads();
+    for (int idx = tid; idx < S * 2 * NT; idx += kBwdThreads) {
+      const int st = idx / (2 * NT), k = idx - st * (2 * NT);
+      if (st < cnt) {
+        float v = 0.f;
+#pragma unroll
+        for (int w = 0; w < kBwdRows / 32; ++w) v += wpart[w][st][k];
+        const int m = k < NT ? 1 : 0, nn = k & (NT - 1);
+        p.part_bc[((cta * 2 + m) * NT + nn) * L + t0 + st] = v;
+      }
     }
   }
   if (valid) {
