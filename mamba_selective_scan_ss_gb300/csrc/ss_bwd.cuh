@@ -12,24 +12,35 @@
 //   du_t = dy'_t D + sum_n g_t[n] dt_t B[n,t]
 //   ddelta_t = d(dt_t) sigmoid(delta_t + bias)   (1 without softplus),  dbias += ddelta_t
 //
-// Layout: one thread per row with all (up to 16) states in registers, as in
-// the forward, so the row's scalars (dt, du, the gate) and its sums over the
+// Layout: one thread per row with all (up to 16) states in registers as eight
+// fp32 pairs (packed f32x2 arithmetic, even state in the low lane), as in the
+// forward, so the row's scalars (dt, du, the gate) and its sums over the
 // states (d(dt), du, the pre-gate read-out) stay inside the thread.  A CTA
 // holds 64 rows; the B/C values of each block of kBwdBlock steps are staged
-// once in shared memory and read as broadcasts.  The one exchange between
-// threads is the sum of dB/dC over the rows, step by step and within each
-// warp (no CTA barrier): every thread writes its 32 contributions to a padded
-// table and lane k of the warp adds column k over the warp's 32 rows in order.
+// once in shared memory and read as 16-byte broadcasts.  The one exchange
+// between threads is the sum of dB/dC over the rows, step by step and within
+// each warp (no CTA barrier): every thread stores its 32 contributions as
+// eight 16-byte groups of a swizzled table, each lane adds four columns over
+// eight rows, and two shuffles combine the warp's four row groups.
 //
 // Time: a forward pass stores the state every kBwdBlock steps (checkpoints in
 // scratch); the reverse pass then, block by block from the end, recomputes the
 // block's states from its checkpoint into shared memory and runs the reverse
-// recurrence over them (decays recomputed with ex2).
+// recurrence over them (decays recomputed with ex2).  Every block's global
+// loads (row streams, B/C, checkpoint) are issued one block ahead, and its
+// row outputs are collected in registers and stored as 16-byte vectors.
 //
-// Reductions are deterministic: dB/dC per warp in row order, then
+// The reverse step uses g a h_{t-1} for both dA (times dt) and d(dt) (times
+// A), g du for dB, and dt sum_n g B for du: the same sums as the formulas
+// above, factored so that each state pair costs twelve packed operations.
+//
+// Reductions are deterministic: dB/dC per warp in a fixed order (rows in
+// order within each group of eight, then the groups as (0+2)+(1+3)), then
 // ss_bwd_reduce_bc over the CTAs of a batch row and their warps in order; dA, dD and dbias
 // per (batch, channel), then ss_bwd_reduce_rows over the batch in order.
 #pragma once
+
+#include <type_traits>
 
 #include "ss_device.cuh"
 
@@ -39,6 +50,7 @@ constexpr int kBwdBlock = 8;       // steps per recomputed block (and checkpoint
 constexpr int kBwdRows = 64;       // rows per CTA (one thread each)
 constexpr int kBwdLanes = 16;      // states per group (dstate <= 16)
 constexpr int kBwdThreads = kBwdRows;
+constexpr int kBwdMinBlocks = 5;  // resident CTAs per SM the register budget is sized for
 
 struct BwdParams {
   const void* u;
@@ -70,36 +82,153 @@ struct BwdParams {
   int vec;              // rows 16-byte aligned: a block's row values load as 16-byte vectors
 };
 
-// Steps [t0, t0 + kBwdBlock) of one row as floats: 16-byte loads when the
-// block is whole and the row aligned (vec), else one element at a time.
+// The kBwdBlock values of one row stream over a block of steps, in the I/O
+// dtype's bits: one 32-bit word per step (fp32) or per two steps (bf16, the
+// earlier step in the low half).  Loaded one block ahead of its use.
 template <typename T>
-__device__ __forceinline__ void load_block(const T* row, int64_t t0, int cnt, bool vec,
-                                           float (&out)[kBwdBlock]) {
-  constexpr int V = Elem<T>::kVec;  // elements per 16 bytes (4 or 8)
-  if (vec && cnt == kBwdBlock) {
+struct RowBlk {
+  static constexpr bool kF32 = std::is_same<T, float>::value;
+  static constexpr int kWords = kF32 ? kBwdBlock : kBwdBlock / 2;
+  uint32_t w[kWords];
+
+  // steps [t0, t0 + cnt): 16-byte loads when the block is whole and the row
+  // aligned (vec), else one element at a time; steps past cnt read as 0
+  __device__ __forceinline__ void load(const T* row, int64_t t0, int cnt, bool vec) {
+    if (vec && cnt == kBwdBlock) {
 #pragma unroll
-    for (int q = 0; q < kBwdBlock / V; ++q) {
-      const Vec16<T> v = *reinterpret_cast<const Vec16<T>*>(row + t0 + q * V);
+      for (int q = 0; q < kWords / 4; ++q) {
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(row + t0) + q);
+        w[4 * q + 0] = v.x;
+        w[4 * q + 1] = v.y;
+        w[4 * q + 2] = v.z;
+        w[4 * q + 3] = v.w;
+      }
+    } else {
 #pragma unroll
-      for (int e = 0; e < V; ++e) out[q * V + e] = Elem<T>::to_f32(v.e[e]);
+      for (int st = 0; st < kBwdBlock; ++st) {
+        const uint32_t bits = st < cnt ? bits_of(row[t0 + st]) : 0u;
+        if constexpr (kF32) {
+          w[st] = bits;
+        } else {
+          if (st & 1) w[st / 2] |= bits << 16;
+          else w[st / 2] = bits;
+        }
+      }
     }
-  } else {
-#pragma unroll
-    for (int st = 0; st < kBwdBlock; ++st) out[st] = st < cnt ? Elem<T>::to_f32(row[t0 + st]) : 0.f;
   }
-}
+  __device__ __forceinline__ float get(int st) const {
+    if constexpr (kF32) return __uint_as_float(w[st]);
+    else return __uint_as_float((st & 1) ? (w[st / 2] & 0xffff0000u) : (w[st / 2] << 16));
+  }
+  __device__ __forceinline__ static uint32_t bits_of(float x) { return __float_as_uint(x); }
+  __device__ __forceinline__ static uint32_t bits_of(__nv_bfloat16 x) {
+    return (uint32_t)__bfloat16_as_ushort(x);
+  }
+};
+
+// One output row over a block of steps, filled from the last step down and
+// kept in the I/O dtype's bits (bf16: rounded to nearest even as each pair of
+// steps completes), then stored whole.
+template <typename T>
+struct OutBlk {
+  static constexpr bool kF32 = std::is_same<T, float>::value;
+  static constexpr int kWords = kF32 ? kBwdBlock : kBwdBlock / 2;
+  uint32_t w[kWords];
+  float pend = 0.f;  // bf16: an odd step's value until the even step before it arrives
+
+  __device__ __forceinline__ void put(int st, float v) {
+    if constexpr (kF32) {
+      w[st] = __float_as_uint(v);
+    } else if (st & 1) {
+      pend = v;
+    } else {
+      uint32_t x;
+      asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(x) : "f"(pend), "f"(v));
+      w[st / 2] = x;
+    }
+  }
+  // steps [t0, t0 + cnt): 16-byte stores when the block is whole and the row
+  // aligned (vec), else one element at a time
+  __device__ __forceinline__ void store(T* row, int64_t t0, int cnt, bool vec) const {
+    if (vec && cnt == kBwdBlock) {
+#pragma unroll
+      for (int q = 0; q < kWords / 4; ++q)
+        reinterpret_cast<uint4*>(row + t0)[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+    } else {
+#pragma unroll
+      for (int st = 0; st < kBwdBlock; ++st) {
+        if (st >= cnt) continue;
+        if constexpr (kF32)
+          row[t0 + st] = __uint_as_float(w[st]);
+        else
+          row[t0 + st] = __ushort_as_bfloat16((unsigned short)((st & 1) ? (w[st / 2] >> 16) : (w[st / 2] & 0xffffu)));
+      }
+    }
+  }
+};
 
 __device__ __forceinline__ float sigmoid_f(float x) { return rcp_approx(1.f + ex2(-x * kLog2e)); }
 
+// Row r of the per-warp dB/dC table: kBwdTable floats, stored as 16-byte
+// groups whose position is XOR-swizzled by the row (group j of row r sits at
+// j ^ (r & 7)), so that eight threads storing one group each of eight
+// consecutive rows, and eight lanes loading eight groups of one row, both hit
+// 32 distinct banks.
+constexpr int kBwdTable = 2 * kBwdLanes;  // dC of states 0..15, then dB
+__device__ __forceinline__ int red_at(int r, int group) { return r * kBwdTable + 4 * (group ^ (r & 7)); }
+
+// B (and C) values of one block, kBwdBlock steps of every state, loaded one
+// block ahead by the CTA's threads together (element i of the block: tensor
+// i / (NT S), state (i / S) % NT, step i % S), as I/O-dtype bits.
+template <typename T, int TENSORS>
+struct BcBlk {
+  static constexpr int kPer = TENSORS * kBwdLanes * kBwdBlock / kBwdThreads;
+  uint32_t w[kPer];
+  __device__ __forceinline__ void load(const T* Bg, const T* Cg, int64_t L, int64_t N, int64_t t0,
+                                       int cnt, int tid) {
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int i = tid + j * kBwdThreads;
+      const int m = i / (kBwdLanes * kBwdBlock), n = (i / kBwdBlock) % kBwdLanes,
+                st = i % kBwdBlock;
+      const T* src = m == 0 ? Bg : Cg;
+      w[j] = (st < cnt && n < N) ? RowBlk<T>::bits_of(src[(int64_t)n * L + t0 + st]) : 0u;
+    }
+  }
+  // into bc[m][st][n] as floats
+  __device__ __forceinline__ void put(float (*bc)[kBwdBlock][kBwdLanes], int tid) const {
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int i = tid + j * kBwdThreads;
+      const int m = i / (kBwdLanes * kBwdBlock), n = (i / kBwdBlock) % kBwdLanes,
+                st = i % kBwdBlock;
+      bc[m][st][n] = std::is_same<T, float>::value ? __uint_as_float(w[j]) : __uint_as_float(w[j] << 16);
+    }
+  }
+};
+
+// dt of the block's steps (softplus of delta + bias, two steps at a time)
+template <typename T>
+__device__ __forceinline__ void block_dt(const RowBlk<T>& x, float bias, bool softplus,
+                                         float (&dts)[kBwdBlock]) {
+#pragma unroll
+  for (int m = 0; m < kBwdBlock / 2; ++m) {
+    const f2 xb = pack(x.get(2 * m) + bias, x.get(2 * m + 1) + bias);
+    const f2 d = softplus ? softplus2(xb) : xb;
+    unpack(d, dts[2 * m], dts[2 * m + 1]);
+  }
+}
+
 template <typename T, bool HAS_Z>
-__global__ void __launch_bounds__(kBwdThreads, 6) ss_bwd_main(const BwdParams p) {
-  constexpr int S = kBwdBlock, NT = kBwdLanes;
-  __shared__ float bc[2][S][NT];                 // B, C of the block's steps
-  __shared__ float hp[S][NT][kBwdRows];          // state before each step of the block
-  __shared__ float red[kBwdRows][2 * NT + 1];    // one step's dC (0..15), dB (16..31) per row
-  __shared__ float wpart[kBwdRows / 32][S][2 * NT];  // the block's per-warp dC/dB sums
+__global__ void __launch_bounds__(kBwdThreads, sizeof(T) == 2 ? kBwdMinBlocks : kBwdMinBlocks - 1) ss_bwd_main(const BwdParams p) {
+  constexpr int S = kBwdBlock, NT = kBwdLanes, NP = NT / 2;
+  __shared__ __align__(16) float bc[2][2][S][NT];      // B, C of a block's steps (two buffers)
+  __shared__ f2 hp[S][NP][kBwdRows];                   // state before each step of the block
+  __shared__ __align__(16) float red[kBwdRows * kBwdTable];  // one step's dC, dB per row
+  __shared__ float wpart[kBwdRows / 32][S][kBwdTable];  // the block's per-warp dC/dB sums
 
   const int tid = threadIdx.x;
+  const int lane = tid & 31, warp = tid >> 5;
   const int64_t cta = blockIdx.x;
   const int64_t b = cta / p.dtiles;
   const int64_t d = (cta - b * p.dtiles) * kBwdRows + tid;
@@ -114,159 +243,224 @@ __global__ void __launch_bounds__(kBwdThreads, 6) ss_bwd_main(const BwdParams p)
   const T* __restrict__ yg = static_cast<const T*>(p.dy) + row * L;
   const T* __restrict__ Bg = static_cast<const T*>(p.B) + b * N * L;
   const T* __restrict__ Cg = static_cast<const T*>(p.C) + b * N * L;
-  float A2[NT];
+  f2 A2[NP];  // A log2(e) of state pairs (2k, 2k+1)
 #pragma unroll
-  for (int n = 0; n < NT; ++n) A2[n] = n < N ? p.A[dc * N + n] * kLog2e : 0.f;
+  for (int k = 0; k < NP; ++k)
+    A2[k] = pack(2 * k < N ? p.A[dc * N + 2 * k] * kLog2e : 0.f,
+                 2 * k + 1 < N ? p.A[dc * N + 2 * k + 1] * kLog2e : 0.f);
   const float bias = p.bias ? p.bias[dc] : 0.f;
   const float Dd = p.D ? p.D[dc] : 0.f;
   auto ck = [&](int64_t blk, int n) -> float& {
     return p.ckpt[((cta * p.nblk + blk) * NT + n) * kBwdRows + tid];
   };
-  // B (and C) of steps [t0, t0 + cnt) into shared memory, zero past dstate
-  auto stage = [&](int64_t t0, int cnt, int tensors) {
-    for (int i = tid; i < tensors * NT * S; i += kBwdThreads) {
-      const int m = i / (NT * S), n = (i / S) % NT, st = i % S;
-      const T* src = m == 0 ? Bg : Cg;
-      bc[m][st][n] = (st < cnt && n < N) ? Elem<T>::to_f32(src[(int64_t)n * L + t0 + st]) : 0.f;
-    }
-  };
+  auto count = [&](int64_t blk) { return (int)min((int64_t)S, L - blk * S); };
   const bool vec = p.vec != 0;
-  auto dt_of = [&](float x) { return p.softplus ? lo_of(softplus2(splat(x))) : x; };
+  const bool softplus = p.softplus != 0;
 
   // ---- forward: checkpoints at the end of every block but the last ----
   {
-    float h[NT];
+    f2 h[NP];
 #pragma unroll
-    for (int n = 0; n < NT; ++n) h[n] = 0.f;
+    for (int k = 0; k < NP; ++k) h[k] = splat(0.f);
+    RowBlk<T> xn, un;
+    BcBlk<T, 1> bn;
+    xn.load(dg, 0, count(0), vec);
+    un.load(ug, 0, count(0), vec);
+    bn.load(Bg, Cg, L, N, 0, count(0), tid);
     for (int64_t blk = 0; blk < p.nblk; ++blk) {
-      const int64_t t0 = blk * S;
-      const int cnt = (int)min((int64_t)S, L - t0);
-      stage(t0, cnt, 1);
-      float xs[S], us[S];
-      load_block<T>(dg, t0, cnt, vec, xs);
-      load_block<T>(ug, t0, cnt, vec, us);
-      __syncthreads();
+      const int cnt = count(blk);
+      const RowBlk<T> xs = xn, us = un;
+      bn.put(bc[blk & 1], tid);
+      if (blk + 1 < p.nblk) {  // the next block's loads, in flight during this one
+        const int64_t t1 = (blk + 1) * S;
+        xn.load(dg, t1, count(blk + 1), vec);
+        un.load(ug, t1, count(blk + 1), vec);
+        bn.load(Bg, Cg, L, N, t1, count(blk + 1), tid);
+      }
+      __syncthreads();  // bc of this block visible; its other buffer is free
+      float dts[S];
+      block_dt<T>(xs, bias, softplus, dts);
+      const float(*bcb)[S][NT] = bc[blk & 1];
 #pragma unroll
       for (int st = 0; st < S; ++st) {
         if (st < cnt) {
-          const float dtv = dt_of(xs[st] + bias);
-          const float du = dtv * us[st];
+          const f2 dt2 = splat(dts[st]), du2 = splat(dts[st] * us.get(st));
 #pragma unroll
-          for (int n = 0; n < NT; ++n) h[n] = fmaf(ex2(dtv * A2[n]), h[n], du * bc[0][st][n]);
+          for (int k4 = 0; k4 < NT / 4; ++k4) {
+            const ulonglong2 bq = *reinterpret_cast<const ulonglong2*>(&bcb[0][st][4 * k4]);
+            h[2 * k4] = fma2(ex2x2(mul2(dt2, A2[2 * k4])), h[2 * k4], mul2(du2, f2{bq.x}));
+            h[2 * k4 + 1] =
+                fma2(ex2x2(mul2(dt2, A2[2 * k4 + 1])), h[2 * k4 + 1], mul2(du2, f2{bq.y}));
+          }
         }
       }
       if (blk + 1 < p.nblk) {
 #pragma unroll
-        for (int n = 0; n < NT; ++n) ck(blk, n) = h[n];
+        for (int k = 0; k < NP; ++k) unpack(h[k], ck(blk, 2 * k), ck(blk, 2 * k + 1));
       }
-      __syncthreads();  // bc is restaged by the next block
     }
   }
+  __syncthreads();  // the forward's last reads of bc are done before the reverse restages it
 
-  // ---- reverse, block by block ----
-  float g[NT], dA_acc[NT];
+  // ---- reverse, block by block from the end ----
+  f2 g[NP], dA2[NP];
 #pragma unroll
-  for (int n = 0; n < NT; ++n) {
-    g[n] = (valid && n < N && p.dlast) ? p.dlast[row * N + n] : 0.f;
-    dA_acc[n] = 0.f;
+  for (int k = 0; k < NP; ++k) {
+    float gv[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int n = 2 * k + e;
+      gv[e] = (valid && n < N && p.dlast) ? p.dlast[row * N + n] : 0.f;
+    }
+    g[k] = pack(gv[0], gv[1]);
+    dA2[k] = splat(0.f);
   }
   float dD_acc = 0.f, dbias_acc = 0.f;
+  RowBlk<T> xn{}, un{}, yn{}, zn{};
+  BcBlk<T, 2> bn;
+  float hn[NT];  // checkpoint the next block's recompute starts from
+  auto load_ckpt = [&](int64_t blk) {  // the state entering block blk
+#pragma unroll
+    for (int n = 0; n < NT; ++n) hn[n] = blk > 0 ? ck(blk - 1, n) : 0.f;
+  };
+  auto prefetch = [&](int64_t blk) {
+    const int64_t t0 = blk * S;
+    const int cnt = count(blk);
+    xn.load(dg, t0, cnt, vec);
+    un.load(ug, t0, cnt, vec);
+    yn.load(yg, t0, cnt, vec);
+    if (HAS_Z) zn.load(zg, t0, cnt, vec);
+    bn.load(Bg, Cg, L, N, t0, cnt, tid);
+    load_ckpt(blk);
+  };
+  prefetch(p.nblk - 1);
   for (int64_t blk = p.nblk - 1; blk >= 0; --blk) {
     const int64_t t0 = blk * S;
-    const int cnt = (int)min((int64_t)S, L - t0);
-    stage(t0, cnt, 2);
-    // the row's scalars of the block's steps
-    float xs[S], dts[S], us[S], dys[S], zs[S];
-    load_block<T>(dg, t0, cnt, vec, xs);
-    load_block<T>(ug, t0, cnt, vec, us);
-    load_block<T>(yg, t0, cnt, vec, dys);
-    if (HAS_Z) load_block<T>(zg, t0, cnt, vec, zs);
+    const int cnt = count(blk);
+    const RowBlk<T> xs = xn, us = un, ys = yn, zs = zn;
+    f2 h[NP];
+#pragma unroll
+    for (int k = 0; k < NP; ++k) h[k] = pack(hn[2 * k], hn[2 * k + 1]);
+    bn.put(bc[blk & 1], tid);
+    if (blk > 0) prefetch(blk - 1);
+    __syncthreads();  // bc of this block visible
+    const float(*bcb)[S][NT] = bc[blk & 1];
+    float dts[S];
+    block_dt<T>(xs, bias, softplus, dts);
+
+    // recompute the block's states from its checkpoint (each thread its own column of hp)
 #pragma unroll
     for (int st = 0; st < S; ++st) {
-      xs[st] += bias;
-      dts[st] = dt_of(xs[st]);
-      if (!valid) dys[st] = 0.f;
-      if (!HAS_Z) zs[st] = 0.f;
-    }
-    __syncthreads();
-    // recompute the block's states from its checkpoint
-    {
-      float h[NT];
+      if (st < cnt) {
+        const f2 dt2 = splat(dts[st]), du2 = splat(dts[st] * us.get(st));
 #pragma unroll
-      for (int n = 0; n < NT; ++n) h[n] = blk > 0 ? ck(blk - 1, n) : 0.f;
+        for (int k4 = 0; k4 < NT / 4; ++k4) {
+          const ulonglong2 bq = *reinterpret_cast<const ulonglong2*>(&bcb[0][st][4 * k4]);
 #pragma unroll
-      for (int st = 0; st < S; ++st) {
-        if (st < cnt) {
-          const float du = dts[st] * us[st];
-#pragma unroll
-          for (int n = 0; n < NT; ++n) {
-            hp[st][n][tid] = h[n];
-            h[n] = fmaf(ex2(dts[st] * A2[n]), h[n], du * bc[0][st][n]);
+          for (int e = 0; e < 2; ++e) {
+            const int k = 2 * k4 + e;
+            hp[st][k][tid] = h[k];
+            h[k] = fma2(ex2x2(mul2(dt2, A2[k])), h[k], mul2(du2, f2{e ? bq.y : bq.x}));
           }
         }
       }
     }
+
     // reverse over the block's steps
+    OutBlk<T> o_dx, o_du, o_dz;
 #pragma unroll
     for (int st = S - 1; st >= 0; --st) {
-      if (st >= cnt) continue;
-      const int64_t t = t0 + st;
-      float dyp = dys[st], sig = 0.f;
+      if (st >= cnt) {
+        o_dx.put(st, 0.f);
+        o_du.put(st, 0.f);
+        o_dz.put(st, 0.f);
+        continue;
+      }
+      const float z = HAS_Z ? zs.get(st) : 0.f;
+      const float dyv = valid ? ys.get(st) : 0.f;
+      float dyp = dyv, sig = 0.f;
       if (HAS_Z) {
-        sig = sigmoid_f(zs[st]);
-        dyp = dys[st] * zs[st] * sig;
+        sig = sigmoid_f(z);
+        dyp = dyv * z * sig;
       }
-      const float dtv = dts[st], u = us[st], du = dtv * u;
-      float ddt_a[2] = {0.f, 0.f}, ddt_b[2] = {0.f, 0.f}, dsum[2] = {0.f, 0.f},
-            ysum[2] = {0.f, 0.f};
+      const float dtv = dts[st], u = us.get(st), du = dtv * u;
+      const f2 dt2 = splat(dtv), du2 = splat(du), dyp2 = splat(dyp);
+      // even states in the low lane, odd in the high lane of each sum;
+      // sum_n g B dt (for du) is dt times ddt_b = sum_n g B
+      f2 ddt_a = splat(0.f), ddt_b = splat(0.f), ysum = splat(0.f);
 #pragma unroll
-      for (int n = 0; n < NT; ++n) {
-        const float prev = hp[st][n][tid];
-        const float a = ex2(dtv * A2[n]);
-        const float bb = bc[0][st][n], cc = bc[1][st][n];
-        const float ap = a * prev;
-        const float ht = fmaf(du, bb, ap);
-        const float gn = fmaf(cc, dyp, g[n]);
-        const float gd = gn * dtv;
-        red[tid][n] = dyp * ht;           // dC
-        red[tid][NT + n] = gd * u;        // dB
-        dA_acc[n] = fmaf(gd, ap, dA_acc[n]);
-        ddt_a[n & 1] = fmaf(gn * A2[n], ap, ddt_a[n & 1]);
-        ddt_b[n & 1] = fmaf(gn, bb, ddt_b[n & 1]);
-        dsum[n & 1] = fmaf(gd, bb, dsum[n & 1]);
-        ysum[n & 1] = fmaf(cc, ht, ysum[n & 1]);
-        g[n] = a * gn;
+      for (int k4 = 0; k4 < NT / 4; ++k4) {
+        const ulonglong2 bq = *reinterpret_cast<const ulonglong2*>(&bcb[0][st][4 * k4]);
+        const ulonglong2 cq = *reinterpret_cast<const ulonglong2*>(&bcb[1][st][4 * k4]);
+        f2 dCv[2], dBv[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int k = 2 * k4 + e;
+          const f2 bb{e ? bq.y : bq.x}, cc{e ? cq.y : cq.x};
+          const f2 a = ex2x2(mul2(dt2, A2[k]));
+          const f2 ap = mul2(a, hp[st][k][tid]);
+          const f2 ht = fma2(du2, bb, ap);
+          const f2 gn = fma2(cc, dyp2, g[k]);
+          const f2 gap = mul2(gn, ap);  // g a h_{t-1}: shared by dA and d(dt)
+          dCv[e] = mul2(dyp2, ht);
+          dBv[e] = mul2(gn, du2);
+          dA2[k] = fma2(gap, dt2, dA2[k]);
+          ddt_a = fma2(gap, A2[k], ddt_a);
+          ddt_b = fma2(gn, bb, ddt_b);
+          ysum = fma2(cc, ht, ysum);
+          g[k] = mul2(a, gn);
+        }
+        *reinterpret_cast<ulonglong2*>(&red[red_at(tid, k4)]) = make_ulonglong2(dCv[0].v, dCv[1].v);
+        *reinterpret_cast<ulonglong2*>(&red[red_at(tid, NT / 4 + k4)]) =
+            make_ulonglong2(dBv[0].v, dBv[1].v);
       }
-      const float ddt = (ddt_a[0] + ddt_a[1]) * kLn2 + (ddt_b[0] + ddt_b[1]) * u;
-      const float dx = p.softplus ? ddt * sigmoid_f(xs[st]) : ddt;
+      const float gb = lo_of(ddt_b) + hi_of(ddt_b);
+      const float ddt = (lo_of(ddt_a) + hi_of(ddt_a)) * kLn2 + gb * u;
+      const float dx = softplus ? ddt * sigmoid_f(xs.get(st) + bias) : ddt;
       dbias_acc += dx;
       dD_acc = fmaf(dyp, u, dD_acc);
-      if (valid) {
-        const int64_t xi = row * L + t;
-        static_cast<T*>(p.ddelta)[xi] = Elem<T>::from_f32(dx);
-        static_cast<T*>(p.du)[xi] = Elem<T>::from_f32(fmaf(dyp, Dd, dsum[0] + dsum[1]));
-        if (HAS_Z) {
-          const float yp = fmaf(Dd, u, ysum[0] + ysum[1]);
-          const float dz = dys[st] * yp * sig * fmaf(zs[st], 1.f - sig, 1.f);
-          static_cast<T*>(p.dz)[xi] = Elem<T>::from_f32(dz);
-        }
+      o_dx.put(st, dx);
+      o_du.put(st, fmaf(dyp, Dd, gb * dtv));
+      if (HAS_Z) {
+        const float yp = fmaf(Dd, u, lo_of(ysum) + hi_of(ysum));
+        o_dz.put(st, dyv * yp * sig * fmaf(z, 1.f - sig, 1.f));
       }
-      // dB/dC of step t over the warp's 32 rows, in row order: lane k sums
-      // column k (no CTA barrier); the two warps' sums meet once per block
+      // dB/dC of step t over the warp's 32 rows (no CTA barrier): lane
+      // (rg = lane / 8, cq = lane % 8) adds columns 4cq..4cq+3 over the rows
+      // rg*8 .. rg*8+7 in order, then two exchanges add the four row groups
+      // ((rg, rg^2), then (rg^1, rg^3)), each lane ending with one column
       __syncwarp();
       {
-        const int lane = tid & 31, w = tid >> 5;
-        float acc = 0.f;
-#pragma unroll 8
-        for (int r = 0; r < 32; ++r) acc += red[w * 32 + r][lane];
-        wpart[w][st][lane] = acc;
+        const int r0 = warp * 32 + (lane >> 3) * 8, cqi = lane & 7;
+        ulonglong2 v = *reinterpret_cast<const ulonglong2*>(&red[red_at(r0, cqi)]);
+        f2 s0{v.x}, s1{v.y};
+#pragma unroll
+        for (int r = 1; r < 8; ++r) {
+          v = *reinterpret_cast<const ulonglong2*>(&red[red_at(r0 + r, cqi)]);
+          s0 = add2(s0, f2{v.x});
+          s1 = add2(s1, f2{v.y});
+        }
+        const bool b1 = (lane & 16) != 0, b0 = (lane & 8) != 0;
+        f2 keep = b1 ? s1 : s0;
+        const f2 send = b1 ? s0 : s1;
+        keep = add2(keep, f2{__shfl_xor_sync(0xffffffffu, send.v, 16)});
+        float klo, khi;
+        unpack(keep, klo, khi);
+        const float mine = b0 ? khi : klo;
+        const float tot = mine + __shfl_xor_sync(0xffffffffu, b0 ? klo : khi, 8);
+        wpart[warp][st][4 * cqi + 2 * (int)b1 + (int)b0] = tot;
       }
       __syncwarp();
     }
+    if (valid) {
+      o_dx.store(static_cast<T*>(p.ddelta) + row * L, t0, cnt, vec);
+      o_du.store(static_cast<T*>(p.du) + row * L, t0, cnt, vec);
+      if (HAS_Z) o_dz.store(static_cast<T*>(p.dz) + row * L, t0, cnt, vec);
+    }
     // the block's dB/dC: the two warps' sums added, step by step
     __syncthreads();
-    for (int idx = tid; idx < S * 2 * NT; idx += kBwdThreads) {
-      const int st = idx / (2 * NT), k = idx - st * (2 * NT);
+    for (int idx = tid; idx < S * kBwdTable; idx += kBwdThreads) {
+      const int st = idx / kBwdTable, k = idx - st * kBwdTable;
       if (st < cnt) {
         float v = 0.f;
 #pragma unroll
@@ -278,7 +472,8 @@ __global__ void __launch_bounds__(kBwdThreads, 6) ss_bwd_main(const BwdParams p)
   }
   if (valid) {
 #pragma unroll
-    for (int n = 0; n < NT; ++n) p.part_a[(b * p.dim + d) * NT + n] = dA_acc[n];
+    for (int k = 0; k < NP; ++k)
+      unpack(dA2[k], p.part_a[(b * p.dim + d) * NT + 2 * k], p.part_a[(b * p.dim + d) * NT + 2 * k + 1]);
     p.part_dd[(b * p.dim + d) * 2 + 0] = dD_acc;
     p.part_dd[(b * p.dim + d) * 2 + 1] = dbias_acc;
   }
