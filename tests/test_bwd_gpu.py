@@ -17,7 +17,7 @@ torch = pytest.importorskip("torch")
 import mamba_selective_scan_ss_gb300 as ss
 import oracle
 from mamba_selective_scan_ss_gb300 import _build
-from mamba_selective_scan_ss_gb300.inputs import ScanWorkload, make_inputs
+from mamba_selective_scan_ss_gb300.inputs import WORKLOADS, ScanWorkload, make_inputs
 
 pytestmark = pytest.mark.gpu
 
@@ -105,6 +105,29 @@ def test_backward_optional_inputs(orc, dtype, opts):
 def test_backward_without_softplus_and_with_state_gradient(orc, dtype):
     run_case(orc, W(2, 48, 16, 72, dtype=dtype, seed=74), with_dlast=True, softplus=False)
     run_case(orc, W(1, 64, 16, 300, dtype=dtype, seed=75), with_dlast=True)
+
+
+def test_backward_full_size_sampled_batch_row(orc):
+    """The Mamba-2.8B-shaped layer (batch 8, dim 5120, 16 states, seqlen 2048,
+    bf16 I/O, z gate) in the benchmark's launch: 640 CTAs of 64 rows, 256
+    checkpointed blocks per row.  One batch row is checked whole against the
+    oracle run on that row alone: du, ddelta and dz of its 5120 channels, and
+    dB, dC, which sum over exactly those channels.  dA, dD and dbias also sum
+    over the batch rows; the small cases cover them."""
+    w = WORKLOADS["2"]
+    inp = make_inputs(w)
+    dy, _ = grad_inputs(w, 91, False)
+    d = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    got = ss.selective_scan_bwd(d["u"], d["delta"], d["A"], d["B"], d["C"], d["D"], d["z"],
+                                d["delta_bias"], True, dy=dy.cuda())
+    torch.cuda.synchronize()
+    b = 5
+    row = {k: (inp[k][b:b + 1].contiguous() if k in ("u", "delta", "B", "C", "z") else inp[k])
+           for k in inp}
+    ref = orc.bwd(row["u"], row["delta"], row["A"], row["B"], row["C"], row["D"], row["z"],
+                  row["delta_bias"], True, dy=dy[b:b + 1].contiguous(), dtype=w.dtype)
+    for name in ("du", "ddelta", "dz", "dB", "dC"):
+        compare(got[name][b:b + 1], ref[name], name, w.dtype)
 
 
 def test_backward_is_deterministic():
