@@ -662,8 +662,8 @@ def run_bwd(args, world, rank, local):
     nbytes += 2 * 4 * w.dim * w.dstate + 4 * 4 * w.dim               # A, dA; D, bias, dD, dbias
 
     def step():
-        ss.selective_scan_bwd(d["u"], d["delta"], d["A"], d["B"], d["C"], d["D"], d["z"],
-                              d["delta_bias"], d["delta_softplus"], dy=dy, stream=stream)
+        return ss.selective_scan_bwd(d["u"], d["delta"], d["A"], d["B"], d["C"], d["D"], d["z"],
+                                     d["delta_bias"], d["delta_softplus"], dy=dy, stream=stream)
 
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
@@ -688,6 +688,52 @@ def run_bwd(args, world, rank, local):
     ms_max = max_over_ranks(ev0.elapsed_time(ev1), world)
     ms_step = ms_max / args.steps
     value = w.updates * args.steps * world / (ms_max * 1e-3)
+
+    # e2e: the forward's inputs and dy from pinned host memory, every gradient
+    # back to pinned host memory, every step
+    e2e = None
+    if args.e2e_steps > 0:
+        host = {k: (v.pin_memory() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+        dy_host = dy.cpu().pin_memory()
+        dy_dev = torch.empty_like(dy)
+        with torch.cuda.stream(stream):
+            probe = step()
+        torch.cuda.synchronize(dev)
+        g_host = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory()
+                  for k, v in probe.items() if v is not None}
+        del probe
+        h2d = sum(v.numel() * v.element_size() for v in host.values()
+                  if isinstance(v, torch.Tensor)) + dy_host.numel() * dy_host.element_size()
+        d2h = sum(v.numel() * v.element_size() for v in g_host.values())
+
+        def e2e_step():
+            with torch.cuda.stream(stream):
+                for k, v in host.items():
+                    if isinstance(v, torch.Tensor):
+                        d[k].copy_(v, non_blocking=True)
+                dy_dev.copy_(dy_host, non_blocking=True)
+                got = ss.selective_scan_bwd(d["u"], d["delta"], d["A"], d["B"], d["C"], d["D"],
+                                            d["z"], d["delta_bias"], d["delta_softplus"],
+                                            dy=dy_dev, stream=stream)
+                for k, v in g_host.items():
+                    v.copy_(got[k], non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        e_ms = max_over_ranks(e0.elapsed_time(e1), world)
+        e2e = {"value": w.updates * args.e2e_steps * world / (e_ms * 1e-3),
+               "unit": "state-updates/s", "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(d2h), "ms_per_step": e_ms / args.e2e_steps}
+
     if rank != 0:
         return
     pk = measured_peaks()
@@ -711,7 +757,12 @@ def run_bwd(args, world, rank, local):
                                 f"lane-ops per update at the probes' {rates['ex2_per_clk_sm']:.1f} "
                                 f"and {rates['fp32_per_clk_sm']:.1f} /clk/SM x {rates['sms']} SMs "
                                 f"x {mhz:.0f} MHz sampled")}
-    roof.update({"traffic": None, "algorithmic_bytes_per_step": nbytes,
+    kernel_src = [REPO / "mamba_selective_scan_ss_gb300" / "csrc" / f
+                  for f in ("ss_bwd.cuh", "ss_device.cuh", "ss_api.cu")]
+    traffic, traffic_src = traffic_record(kernel_src, w.name)
+    roof.update({"traffic": traffic, "traffic_source": traffic_src,
+                 "traffic_scope": "ss_bwd_main, the call's dominant kernel",
+                 "algorithmic_bytes_per_step": nbytes,
                  "updates_per_step": w.updates, "t_hbm_us": t_hbm * 1e6,
                  "t_sfu_us": t_sfu * 1e6, "t_fp32_us": t_fp32 * 1e6,
                  "measured_step_us": t_step * 1e6,
@@ -729,7 +780,7 @@ def run_bwd(args, world, rank, local):
                    "l2": "inputs larger than L2" if 4 * x_bytes > 2 * L2_BYTES else
                          "inputs partly L2-resident between calls",
                    "parallelism": f"replicas x{world}"},
-        "roofline": roof, "cpu_baseline": cpu, "e2e": None,
+        "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": 3 * args.steps, "clocks": clocks, "wall_s_timed_region": t_wall,
     }), flush=True)
 
