@@ -14,7 +14,7 @@ torch = pytest.importorskip("torch")
 import mamba_selective_scan_ss_gb300 as ss
 import oracle
 from mamba_selective_scan_ss_gb300 import _build
-from mamba_selective_scan_ss_gb300.inputs import ScanWorkload, make_inputs
+from mamba_selective_scan_ss_gb300.inputs import WORKLOADS, ScanWorkload, make_inputs
 
 pytestmark = pytest.mark.gpu
 
@@ -98,6 +98,29 @@ def test_per_channel_with_shared_rows_equals_shared_layout():
     atol, rtol = TOL["f32"]
     assert torch.allclose(y_p, y_s, atol=atol, rtol=rtol)
     assert torch.allclose(s_p, s_s, atol=atol, rtol=rtol)
+
+
+def test_per_channel_full_size_sampled_rows(orc):
+    """The benchmark's per-channel workload (batch 8, dim 5120, 16 states,
+    seqlen 512, bf16 I/O, z gate) in its launch: rows are independent, so
+    blocks of 64 channels at the start, middle and end of the grid are checked
+    against the oracle run on those rows alone."""
+    w = WORKLOADS["pc_2"]
+    inp = make_inputs(w)
+    d = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    y, last = ss.selective_scan_fwd(d["u"], d["delta"], d["A"], d["B"], d["C"], d["D"], d["z"],
+                                    d["delta_bias"], d["delta_softplus"])
+    torch.cuda.synchronize()
+    y, last = y.cpu(), last.cpu()
+    for b, c0 in [(0, 0), (3, 2560), (7, w.dim - 64)]:
+        rows = slice(c0, c0 + 64)
+        sub = {k: inp[k][b:b + 1, rows].contiguous() for k in ("u", "delta", "z", "B", "C")}
+        sub.update({k: inp[k][rows].contiguous() for k in ("A", "D", "delta_bias")})
+        y_ref, last_ref = orc.fwd(sub["u"], sub["delta"], sub["A"], sub["B"], sub["C"], sub["D"],
+                                  sub["z"], sub["delta_bias"], inp["delta_softplus"],
+                                  dtype=w.dtype, bc_per_channel=True)
+        close(y[b:b + 1, rows], y_ref, w.dtype, f"y rows {b},{c0}")
+        close(last[b:b + 1, rows], last_ref, w.dtype, f"last_state rows {b},{c0}")
 
 
 def test_per_channel_rejects_more_than_128_states():
