@@ -84,7 +84,8 @@ def run_case(orc, w, seed=5, with_dlast=False, softplus=True):
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("shape", [(2, 64, 16, 64), (1, 70, 16, 37), (3, 5, 16, 200),
-                                   (2, 130, 16, 1024)])
+                                   (2, 130, 16, 1024), (2, 40, 16, 1), (1, 40, 16, 7),
+                                   (1, 40, 16, 8), (1, 40, 16, 9), (1, 1, 16, 100)])
 def test_backward_matches_oracle(orc, dtype, shape):
     run_case(orc, W(*shape, dtype=dtype, seed=71))
 
