@@ -373,6 +373,51 @@ def pin_backward_finite_differences(orc, seed=22):
 
 
 # --------------------------------------------------------------------------
+# Euler's identity for the backward: with the step sizes fixed, the loss
+#   L = sum dy * y + sum dlast * last_state = sum dy' * y' + sum dlast * h_L
+# (dy' = dy silu(z), y' the output before the gate) is linear in u, in B, in
+# C and in D, so the gradient dotted with its own input gives back that part
+# of the loss exactly:
+#   sum u du = L,  sum B dB = sum dy' (C.h) + sum dlast h_L,
+#   sum C dC = sum dy' (C.h),  sum D dD = sum dy' D u.
+# The right-hand sides come from the forward (pinned above) run without the
+# gate and without D; a wrong sign, index or missing term in du, dB, dC or dD
+# breaks the equality.
+def pin_backward_euler_identities(orc, seed=27):
+    rng = np.random.default_rng(seed)
+    for softplus, z, D, with_dlast in ((True, True, True, True), (False, False, True, False),
+                                       (True, True, False, True)):
+        b, d, n, L = 2, 3, 4, 6
+        p = _rand_problem(rng, b, d, n, L, z=z, D=D)
+        if not softplus:
+            p["delta"] = np.abs(p["delta"]).astype(np.float32) + np.float32(0.05)
+            p["delta_bias"] = None
+        dy = rng.standard_normal((b, d, L)).astype(np.float32)
+        dlast = rng.standard_normal((b, d, n)) if with_dlast else None
+        g = orc.bwd(**p, delta_softplus=softplus, dy=dy, dlast=dlast)
+        bare = dict(p, z=None, D=None)
+        ch, h_L = orc.fwd(**bare, delta_softplus=softplus)   # C.h and the last state
+        dyp = dy.astype(np.float64)
+        if p["z"] is not None:
+            dyp = dyp * _silu(p["z"].astype(np.float64))
+        u = p["u"].astype(np.float64)
+        du_part = (np.sum(dyp * u * p["D"].astype(np.float64)[None, :, None])
+                   if p["D"] is not None else 0.0)
+        last = float(np.sum(dlast * h_L)) if dlast is not None else 0.0
+        lin = float(np.sum(dyp * ch))
+        tag = f"(softplus={softplus}, z={z}, D={D}, dlast={with_dlast})"
+        _close(np.sum(u * g["du"]), lin + du_part + last, rtol=1e-10, atol=1e-12,
+               what=f"sum u du {tag}")
+        _close(np.sum(p["B"].astype(np.float64) * g["dB"]), lin + last, rtol=1e-10,
+               atol=1e-12, what=f"sum B dB {tag}")
+        _close(np.sum(p["C"].astype(np.float64) * g["dC"]), lin, rtol=1e-10, atol=1e-12,
+               what=f"sum C dC {tag}")
+        if p["D"] is not None:
+            _close(np.sum(p["D"].astype(np.float64) * g["dD"]), du_part, rtol=1e-10,
+                   atol=1e-12, what=f"sum D dD {tag}")
+
+
+# --------------------------------------------------------------------------
 # Per-channel B/C (the task spec's kernel sketch keeps B and C per [b,d,t]):
 # with every channel given the same rows the result equals the shared layout
 # bit for bit, and every channel equals the shared-layout oracle run alone on
@@ -522,6 +567,7 @@ ALL_PINS = [
     pin_invariances,
     pin_bf16_widening,
     pin_backward_finite_differences,
+    pin_backward_euler_identities,
     pin_per_channel_bc,
     pin_ssd_quadratic_form,
     pin_ssd_is_mamba1_with_scalar_decay,

@@ -62,6 +62,9 @@ MUTANTS = {
     "bwd_dB_without_u": ("j->dB[(b * N + n) * L + t] += gn * dt * u;",
                          "j->dB[(b * N + n) * L + t] += gn * dt;"),
     "bwd_dlast_ignored": ("g[n] = j->dlast ? j->dlast[row * N + n] : 0.0;", "g[n] = 0.0;"),
+    "bwd_dD_before_gate": ("      dD += dyp * u;\n", "      dD += dy * u;\n"),
+    "bwd_dB_time_reversed": ("j->dB[(b * N + n) * L + t] += gn * dt * u;",
+                             "j->dB[(b * N + n) * L + (L - 1 - t)] += gn * dt * u;"),
     # the Mamba-2 forward
     "ssd_group_by_modulo": ("const int64_t g = hd / (H / G);", "const int64_t g = hd % G;"),
     "ssd_decay_missing_dt": ("const double decay = exp(A * dt);", "const double decay = exp(A);"),
