@@ -5,9 +5,15 @@
 
 A step is one selective-scan forward (one ss_selective_scan_fwd call) over the
 workload's synthetic inputs, already resident in HBM.  The default workload is
-the Mamba-130M-shaped layer (batch 2, dim 1536, dstate 16, seqlen 2048, fp32
-I/O, silu gate).  Its inputs (about 100 MB) fit in the 129 MB L2, so the timed
-steps rotate over enough input sets to exceed twice the L2 size.
+the largest one-GPU configuration: the sequence sweep shaped like the Blelloch
+article's benchmark at its longest length (batch 16, dim 1536, dstate 16,
+seqlen 16384, fp32 I/O, silu gate; 6.5 GB of inputs and outputs, far above
+the 129 MB L2).  Workloads that fit in L2 rotate over enough input sets to
+exceed twice the L2 size, and also report the time with one L2-resident set
+("unflushed").
+
+--series seqlen prints one line per length of the sequence sweep
+(L = 256, 1024, 4096, 16384): the time-against-seqlen record.
 
 Under torchrun each rank runs the same workload on its own GPU (weak scaling,
 no collective on the data path); rank 0 prints one JSON line with the
@@ -58,6 +64,8 @@ def parse_args():
                     help="fwd: the forward scan (default); decode: one token per call; "
                          "bwd: the backward pass; mamba2: the Mamba-2 forward (tensor cores)")
     ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--series", choices=["seqlen"], default=None,
+                    help="seqlen: one line per length of the sequence sweep (forward only)")
     ap.add_argument("--cpu-baseline-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--reference-seconds", type=float, default=150.0,
@@ -222,13 +230,14 @@ def traffic_record(kernel_sources: list[Path], workload_name: str):
 
 
 # ---------------------------------------------------------------- oracle leg
-def oracle_rate(w, budget_s: float, inp_cpu=None) -> dict:
-    """Time the CPU oracle on a bounded sample of the workload (rows subset)."""
+def oracle_rate(w, budget_s: float, inp_cpu=None, threads: int | None = None) -> dict:
+    """Time the CPU oracle on a bounded sample of the workload (rows subset),
+    on every host core (or on `threads` of them)."""
     import oracle
     from mamba_selective_scan_ss_gb300.inputs import make_inputs
     orc = oracle.default()
     inp = inp_cpu if inp_cpu is not None else make_inputs(w)
-    cores = os.cpu_count() or 1
+    cores = threads or os.cpu_count() or 1
 
     def run(ch):
         sub = {k: v for k, v in inp.items()}
@@ -372,6 +381,25 @@ def run_ours(args, world, rank, local):
     total_updates = w.updates * args.steps * world
     value = total_updates / (ms_max * 1e-3)
 
+    # the same steps on one L2-resident input set (workloads smaller than L2)
+    unflushed = None
+    if nsets > 1:
+        n_u = min(args.steps, 2000)
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                step(0)
+            u0 = torch.cuda.Event(enable_timing=True)
+            u1 = torch.cuda.Event(enable_timing=True)
+            u0.record(stream)
+            for _ in range(n_u):
+                step(0)
+            u1.record(stream)
+        torch.cuda.synchronize(dev)
+        u_ms = max_over_ranks(u0.elapsed_time(u1), world) / n_u
+        unflushed = {"value": w.updates * world / (u_ms * 1e-3), "unit": "state-updates/s",
+                     "ms_per_step": u_ms, "steps": n_u,
+                     "note": "one input set reused every step: inputs L2-resident"}
+
     # e2e: pinned host inputs -> device, the call, outputs -> pinned host, every step
     e2e = None
     if args.e2e_steps > 0:
@@ -453,12 +481,15 @@ def run_ours(args, world, rank, local):
                "sample": (f"{r['reps']} pass(es) over the first {r['channels']} of {w.dim} "
                           f"channels of every batch row, full seqlen {w.seqlen}, dstate "
                           f"{w.dstate}: {r['updates']} updates in {r['seconds']:.1f} s")}
+        r1 = oracle_rate(w, min(5.0, args.cpu_baseline_seconds), inp, threads=1)
+        cpu["single_core"] = {"value": r1["value"], "cores": 1,
+                              "sample": f"{r1['updates']} updates in {r1['seconds']:.1f} s"}
 
     line = {
         "metric": METRIC, "value": value, "unit": "state-updates/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f32", "data": "synthetic",
+        "dtype": w.dtype, "compute_dtype": "f32", "data": "synthetic",
         "config": {"workload": w.name, "batch": w.batch, "dim": w.dim, "dstate": w.dstate,
                    "seqlen": w.seqlen, "io_dtype": w.dtype, "z_gate": w.has_z,
                    "l2": (f"{nsets} rotating input sets ({nsets * nbytes / 2**20:.0f} MiB > 2x L2)"
@@ -467,6 +498,7 @@ def run_ours(args, world, rank, local):
         "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": e2e,
+        "unflushed": unflushed,
         "gpu_launches": int(plan["kernel_launches"] * args.steps),
         "clocks": clocks,
         "wall_s_timed_region": t_wall,
@@ -615,8 +647,8 @@ def run_decode(args, world, rank, local):
     print(json.dumps({
         "metric": DECODE_METRIC, "value": value, "unit": "state-updates/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-        "data": "synthetic", "op": "decode",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+        "compute_dtype": "f32", "data": "synthetic", "op": "decode",
         "config": {"workload": w.name, "batch": w.batch, "dim": w.dim, "dstate": w.dstate,
                    "io_dtype": w.dtype, "z_gate": w.has_z,
                    "l2": f"{nsets} rotating state sets ({nsets * nbytes / 2**20:.0f} MiB > 2x L2)",
@@ -773,8 +805,8 @@ def run_bwd(args, world, rank, local):
     print(json.dumps({
         "metric": BWD_METRIC, "value": value, "unit": "state-updates/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-        "data": "synthetic", "op": "bwd",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+        "compute_dtype": "f32", "data": "synthetic", "op": "bwd",
         "config": {"workload": w.name, "batch": w.batch, "dim": w.dim, "dstate": w.dstate,
                    "seqlen": w.seqlen, "io_dtype": w.dtype, "z_gate": w.has_z,
                    "l2": "inputs larger than L2" if 4 * x_bytes > 2 * L2_BYTES else
@@ -1021,7 +1053,8 @@ def run_mamba2(args, world, rank, local):
 def main():
     args = parse_args()
     if args.workload is None:
-        args.workload = {"decode": "decode_64", "bwd": "2", "mamba2": "m2_2.7b"}.get(args.op, "1")
+        args.workload = {"decode": "decode_64", "bwd": "2",
+                         "mamba2": "m2_2.7b"}.get(args.op, "4_16384")
     world, rank, local = dist_setup(args)
     try:
         if args.op == "decode":
@@ -1035,6 +1068,10 @@ def main():
             run_bwd(args, world, rank, local)
         elif args.impl == "reference":
             run_reference(args, world, rank)
+        elif args.series == "seqlen":
+            for key in ("4_256", "4_1024", "4_4096", "4_16384"):
+                args.workload = key
+                run_ours(args, world, rank, local)
         else:
             run_ours(args, world, rank, local)
     finally:

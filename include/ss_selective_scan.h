@@ -171,7 +171,8 @@ SS_API ss_status_t ss_selective_state_update(
  * run backwards in time: g_t = C_t dy'_t + a_{t+1} g_{t+1} over the states,
  * with the forward states recomputed from checkpoints.
  *
- * Inputs: those of ss_selective_scan_fwd (zero initial state), plus
+ * Inputs: those of ss_selective_scan_fwd (zero initial state; see
+ * ss_selective_scan_bwd_h0 for a given one), plus
  *   dy          [batch, dim, seqlen]     dtype      gradient of y
  *   dlast_state [batch, dim, dstate]     float32    gradient of last_state, or NULL (0)
  * Outputs (written, never read):
@@ -182,19 +183,44 @@ SS_API ss_status_t ss_selective_state_update(
  *   dz          [batch, dim, seqlen]     dtype      required when z is given, else ignored
  *   dbias       [dim]                    float32    or NULL (ignored if delta_bias is NULL)
  *
- * Limits: dstate <= 16 (else SS_ERR_UNSUPPORTED).  Sums over channels, time
- * and batch are evaluated in a fixed order: results are bitwise reproducible.
+ * Limits: dstate in 1..256 (else SS_ERR_UNSUPPORTED), run in groups of 16
+ * states, one main kernel per group.  Sums over channels, time, batch and
+ * state groups are evaluated in a fixed order: results are bitwise
+ * reproducible.
  * Behaviour: validated on the host (errors launch nothing and write nothing);
- * three kernels are enqueued on `stream` with stream-ordered scratch
- * (cudaMallocAsync/cudaFreeAsync, about 8 bytes per (row, step) for the state
- * checkpoints plus 128 bytes per 64-channel tile and step); no synchronisation
- * and no device-side wait.  No output may overlap an input or another output.
+ * the group kernels and two reductions are enqueued on `stream` with
+ * stream-ordered scratch (cudaMallocAsync/cudaFreeAsync, about 8 bytes per
+ * (row, step) for the state checkpoints, 128 bytes per 64-channel tile, step
+ * and state group, and with several groups 12 bytes per (row, step) for the
+ * row sums carried between them); no synchronisation and no device-side wait.
+ * No output may overlap an input or another output.
  */
 SS_API ss_status_t ss_selective_scan_bwd(
     const void* u, const void* delta, const float* A, const void* B, const void* C,
     const float* D, const void* z, const float* delta_bias, int delta_softplus,
     const void* dy, const float* dlast_state, void* du, void* ddelta, float* dA, float* dB,
     float* dC, float* dD, void* dz, float* dbias,
+    int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, ss_dtype_t dtype, void* stream);
+
+/*
+ * ss_selective_scan_bwd_h0 -- the backward of ss_selective_scan_fwd_h0: the
+ * same gradients as ss_selective_scan_bwd for the forward started from the
+ * state h0, and the gradient of h0 itself (the chain rule carried one step
+ * past t = 0: dh0[n] = exp(dt_0 A[d,n]) g_0[n]; h0 also enters dA through the
+ * first step's decay).
+ *
+ * Arguments: those of ss_selective_scan_bwd, plus
+ *   h0          [batch, dim, dstate]     float32    the state before step 0, or NULL (0)
+ *   dh0         [batch, dim, dstate]     float32    its gradient (written), or NULL
+ * dh0 is written only when h0 is given.  Errors, limits, scratch and
+ * behaviour are those of ss_selective_scan_bwd; h0 counts as an input and
+ * dh0 as an output for the overlap rules.
+ */
+SS_API ss_status_t ss_selective_scan_bwd_h0(
+    const void* u, const void* delta, const float* A, const void* B, const void* C,
+    const float* D, const void* z, const float* delta_bias, int delta_softplus, const float* h0,
+    const void* dy, const float* dlast_state, void* du, void* ddelta, float* dA, float* dB,
+    float* dC, float* dD, void* dz, float* dbias, float* dh0,
     int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, ss_dtype_t dtype, void* stream);
 
 /*
@@ -287,14 +313,19 @@ SS_API ss_status_t ss_selective_scan_check(void* stream);
  *
  * Set-up: the first call on a device (with that device current) looks up the
  * buffer's device address with cudaGetSymbolAddress; make that first call
- * before any stream capture on that device.
+ * before any stream capture on that device.  The address belongs to the
+ * device's CUDA context: after the context is destroyed and created anew
+ * (cudaDeviceReset), the next call looks it up again, so that call too
+ * should come before any capture.
  *
  * Limits: the vector path only (every u/delta/z/y/B/C pointer 16-byte aligned
  * and seqlen a multiple of 4 for float32, of 8 for bf16), else
- * SS_ERR_UNSUPPORTED.  Long sequences are split into fewer chunks than
- * ss_selective_scan_fwd would use when its carries would not fit the buffer;
- * a problem that does not fit even unsplit (dstate > 16 needs a float32 row
- * of batch * dim * seqlen partial read-outs) returns SS_ERR_SCRATCH_LIMIT.
+ * SS_ERR_UNSUPPORTED.  The chunk count is ss_selective_scan_fwd's, lowered to
+ * the largest count whose carries fit the buffer (each chunk of a row tile
+ * of 64 channels keeps 12 bytes per channel and state); a problem that does
+ * not fit even unsplit (dstate > 16 needs a float32 row of
+ * batch * dim * seqlen partial read-outs) returns SS_ERR_SCRATCH_LIMIT.  Like
+ * every entry point of the shipped library it reads no environment variable.
  *
  * Concurrency: every call shares the one buffer per device, so calls whose
  * execution overlaps on the GPU (different streams, or graphs replayed
@@ -317,8 +348,9 @@ SS_API ss_status_t ss_selective_scan_fwd_noalloc(
  * count launches.  `aligned16` states whether every u/delta/z/y/B/C pointer
  * will be 16-byte aligned.  Returns SS_ERR_INVALID_ARGUMENT for sizes <= 0 or
  * a NULL `plan`, SS_ERR_UNSUPPORTED as ss_selective_scan_fwd would; fills
- * `plan` on SS_OK.  Reads the SS_NCHUNKS environment variable as
- * ss_selective_scan_fwd does (a tuning aid that forces the chunk count).
+ * `plan` on SS_OK.  (The test build of the library, which the package's
+ * tests load, also honours the SS_NCHUNKS and SS_CTAS_PER_SM plan
+ * overrides; the shipped library reads no environment variable.)
  */
 typedef struct {
   int64_t nchunks;         /* sequence chunks */

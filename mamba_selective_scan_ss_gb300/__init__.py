@@ -7,7 +7,7 @@ raise: there is no fallback implementation.
 
 Low-level names mirror the C ABI exactly (raw device pointers as ints):
     ss_selective_scan_fwd, ss_selective_scan_fwd_h0, ss_selective_state_update,
-    ss_selective_scan_bwd, ss_selective_scan_fwd_pc, ss_mamba2_fwd,
+    ss_selective_scan_bwd, ss_selective_scan_bwd_h0, ss_selective_scan_fwd_pc, ss_mamba2_fwd,
     ss_status_string, ss_selective_scan_check, ss_selective_scan_plan,
     ss_selective_scan_fwd_noalloc
 plus convenience wrappers for torch CUDA tensors:
@@ -16,11 +16,12 @@ plus convenience wrappers for torch CUDA tensors:
     selective_state_update(state, x, dt, A, B, C, D=None, z=None, dt_bias=None,
                            dt_softplus=True, y=None)
     selective_scan_bwd(u, delta, A, B, C, D, z, delta_bias, delta_softplus, dy,
-                       dlast_state=None)
+                       dlast_state=None, h0=None)
     mamba2_fwd(x, dt, A, B, C, D=None, dt_bias=None, dt_softplus=True, ...)
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 from pathlib import Path
 
@@ -29,8 +30,9 @@ __all__ = [
     "SS_ERR_CUDA", "SS_ERR_TIMEOUT", "SS_ERR_SCRATCH_LIMIT", "SelectiveScanError", "library_path", "load_library",
     "ss_selective_scan_fwd", "ss_status_string", "ss_selective_scan_check",
     "ss_selective_scan_plan", "ss_selective_scan_fwd_noalloc", "ss_selective_scan_fwd_h0",
-    "ss_selective_state_update", "ss_selective_scan_bwd", "ss_selective_scan_fwd_pc",
-    "ss_mamba2_fwd", "selective_scan_fwd",
+    "ss_selective_state_update", "ss_selective_scan_bwd", "ss_selective_scan_bwd_h0",
+    "ss_selective_scan_fwd_pc",
+    "ss_mamba2_fwd", "selective_scan_fwd", "test_hooks",
     "selective_state_update", "selective_scan_bwd", "mamba2_fwd",
 ]
 
@@ -39,7 +41,8 @@ SS_F32, SS_BF16 = 0, 1
  SS_ERR_SCRATCH_LIMIT) = range(6)
 
 _PKG = Path(__file__).resolve().parent
-_LIB = None
+_LIBS: dict = {}
+_USE_TEST_BUILD = False
 
 
 class SelectiveScanError(RuntimeError):
@@ -48,50 +51,79 @@ class SelectiveScanError(RuntimeError):
         super().__init__(f"{what} failed: {ss_status_string(status)}")
 
 
-def library_path() -> Path:
-    return _PKG / "libss_selective_scan.so"
+def library_path(test_build: bool = False) -> Path:
+    """Path of the shipped library (or of its test build, which adds the
+    plan overrides and the unit-skipping hook that the tests drive through
+    SS_NCHUNKS, SS_CTAS_PER_SM and SS_TEST_SKIP_UNITS)."""
+    return _PKG / ("libss_selective_scan_test.so" if test_build else "libss_selective_scan.so")
 
 
-def load_library():
-    """Load the native library (raises if it was not built)."""
-    global _LIB
-    if _LIB is None:
-        path = library_path()
+def _declare(lib):
+    vp, i64 = ctypes.c_void_p, ctypes.c_int64
+    lib.ss_selective_scan_fwd.restype = ctypes.c_int
+    lib.ss_selective_scan_fwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_int,
+                                          vp, vp, i64, i64, i64, i64, ctypes.c_int, vp]
+    lib.ss_status_string.restype = ctypes.c_char_p
+    lib.ss_status_string.argtypes = [ctypes.c_int]
+    lib.ss_selective_scan_check.restype = ctypes.c_int
+    lib.ss_selective_scan_check.argtypes = [vp]
+    lib.ss_selective_scan_fwd_noalloc.restype = ctypes.c_int
+    lib.ss_selective_scan_fwd_noalloc.argtypes = list(lib.ss_selective_scan_fwd.argtypes)
+    lib.ss_selective_scan_fwd_h0.restype = ctypes.c_int
+    lib.ss_selective_scan_fwd_h0.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_int,
+                                             vp, vp, vp, i64, i64, i64, i64, ctypes.c_int, vp]
+    lib.ss_selective_state_update.restype = ctypes.c_int
+    lib.ss_selective_state_update.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                              ctypes.c_int, vp, i64, i64, i64,
+                                              ctypes.c_int, vp]
+    lib.ss_selective_scan_fwd_pc.restype = ctypes.c_int
+    lib.ss_selective_scan_fwd_pc.argtypes = list(lib.ss_selective_scan_fwd.argtypes)
+    lib.ss_selective_scan_bwd.restype = ctypes.c_int
+    lib.ss_selective_scan_bwd.argtypes = [vp] * 8 + [ctypes.c_int] + [vp] * 10 + \
+        [i64, i64, i64, i64, ctypes.c_int, vp]
+    lib.ss_selective_scan_bwd_h0.restype = ctypes.c_int
+    lib.ss_selective_scan_bwd_h0.argtypes = [vp] * 8 + [ctypes.c_int] + [vp] * 12 + \
+        [i64, i64, i64, i64, ctypes.c_int, vp]
+    lib.ss_mamba2_fwd.restype = ctypes.c_int
+    lib.ss_mamba2_fwd.argtypes = [vp] * 7 + [ctypes.c_int, vp, vp] + [i64] * 6 + \
+        [ctypes.c_int, vp]
+    lib.ss_selective_scan_plan.restype = ctypes.c_int
+    lib.ss_selective_scan_plan.argtypes = [i64, i64, i64, i64, ctypes.c_int, ctypes.c_int,
+                                           ctypes.c_int, ctypes.POINTER(_Plan)]
+
+
+def load_library(test_build: bool | None = None):
+    """Load the native library (raises if it was not built).
+
+    By default the shipped library; inside ``with test_hooks():`` (or with
+    test_build=True) its test build.
+    """
+    tb = _USE_TEST_BUILD if test_build is None else bool(test_build)
+    if tb not in _LIBS:
+        path = library_path(tb)
         if not path.exists():
             raise RuntimeError(
                 f"{path.name} is missing: build it with __graft_entry__.build() "
                 "(the selective scan has no non-CUDA implementation)")
         lib = ctypes.CDLL(str(path))
-        vp, i64 = ctypes.c_void_p, ctypes.c_int64
-        lib.ss_selective_scan_fwd.restype = ctypes.c_int
-        lib.ss_selective_scan_fwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_int,
-                                              vp, vp, i64, i64, i64, i64, ctypes.c_int, vp]
-        lib.ss_status_string.restype = ctypes.c_char_p
-        lib.ss_status_string.argtypes = [ctypes.c_int]
-        lib.ss_selective_scan_check.restype = ctypes.c_int
-        lib.ss_selective_scan_check.argtypes = [vp]
-        lib.ss_selective_scan_fwd_noalloc.restype = ctypes.c_int
-        lib.ss_selective_scan_fwd_noalloc.argtypes = list(lib.ss_selective_scan_fwd.argtypes)
-        lib.ss_selective_scan_fwd_h0.restype = ctypes.c_int
-        lib.ss_selective_scan_fwd_h0.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_int,
-                                                 vp, vp, vp, i64, i64, i64, i64, ctypes.c_int, vp]
-        lib.ss_selective_state_update.restype = ctypes.c_int
-        lib.ss_selective_state_update.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp,
-                                                  ctypes.c_int, vp, i64, i64, i64,
-                                                  ctypes.c_int, vp]
-        lib.ss_selective_scan_fwd_pc.restype = ctypes.c_int
-        lib.ss_selective_scan_fwd_pc.argtypes = list(lib.ss_selective_scan_fwd.argtypes)
-        lib.ss_selective_scan_bwd.restype = ctypes.c_int
-        lib.ss_selective_scan_bwd.argtypes = [vp] * 8 + [ctypes.c_int] + [vp] * 10 + \
-            [i64, i64, i64, i64, ctypes.c_int, vp]
-        lib.ss_mamba2_fwd.restype = ctypes.c_int
-        lib.ss_mamba2_fwd.argtypes = [vp] * 7 + [ctypes.c_int, vp, vp] + [i64] * 6 + \
-            [ctypes.c_int, vp]
-        lib.ss_selective_scan_plan.restype = ctypes.c_int
-        lib.ss_selective_scan_plan.argtypes = [i64, i64, i64, i64, ctypes.c_int, ctypes.c_int,
-                                               ctypes.c_int, ctypes.POINTER(_Plan)]
-        _LIB = lib
-    return _LIB
+        _declare(lib)
+        _LIBS[tb] = lib
+    return _LIBS[tb]
+
+
+@contextlib.contextmanager
+def test_hooks():
+    """Route every call made inside the block to the test build of the
+    library, which honours SS_NCHUNKS / SS_CTAS_PER_SM (plan overrides) and
+    SS_TEST_SKIP_UNITS (units never handed out, so that device waits run out).
+    The shipped library reads no environment variable."""
+    global _USE_TEST_BUILD
+    prev = _USE_TEST_BUILD
+    _USE_TEST_BUILD = True
+    try:
+        yield load_library()
+    finally:
+        _USE_TEST_BUILD = prev
 
 
 class _Plan(ctypes.Structure):
@@ -163,6 +195,15 @@ def ss_selective_scan_bwd(u, delta, A, B, C, D, z, delta_bias, delta_softplus, d
     return load_library().ss_selective_scan_bwd(
         u, delta, A, B, C, D, z, delta_bias, int(delta_softplus), dy, dlast_state, du, ddelta,
         dA, dB, dC, dD, dz, dbias, batch, dim, dstate, seqlen, int(dtype), stream)
+
+
+def ss_selective_scan_bwd_h0(u, delta, A, B, C, D, z, delta_bias, delta_softplus, h0, dy,
+                             dlast_state, du, ddelta, dA, dB, dC, dD, dz, dbias, dh0, batch,
+                             dim, dstate, seqlen, dtype, stream) -> int:
+    """The backward from initial state h0, with dh0 (its gradient)."""
+    return load_library().ss_selective_scan_bwd_h0(
+        u, delta, A, B, C, D, z, delta_bias, int(delta_softplus), h0, dy, dlast_state, du, ddelta,
+        dA, dB, dC, dD, dz, dbias, dh0, batch, dim, dstate, seqlen, int(dtype), stream)
 
 
 def ss_mamba2_fwd(x, dt, A, B, C, D, dt_bias, dt_softplus, y, final_state, batch, seqlen,
@@ -289,13 +330,16 @@ def selective_state_update(state, x, dt, A, B, C, D=None, z=None, dt_bias=None,
 
 
 def selective_scan_bwd(u, delta, A, B, C, D=None, z=None, delta_bias=None,
-                       delta_softplus: bool = True, dy=None, dlast_state=None, stream=None):
-    """Gradients of the forward on torch CUDA tensors (zero initial state).
+                       delta_softplus: bool = True, dy=None, dlast_state=None, stream=None,
+                       h0=None):
+    """Gradients of the forward on torch CUDA tensors.
 
     Returns a dict: du, ddelta (and dz) in the I/O dtype; dA [dim, dstate],
     dB, dC [batch, dstate, seqlen], dD, dbias [dim] in float32 (None for an
-    absent input).  dy has y's shape and dtype; dlast_state (float32
-    [batch, dim, dstate]) is the gradient of last_state, default zero.
+    absent input); with h0 (float32 [batch, dim, dstate], the forward's
+    initial state, default zero) also dh0 of the same shape.  dy has y's
+    shape and dtype; dlast_state (float32 [batch, dim, dstate]) is the
+    gradient of last_state, default zero.
     """
     import torch
 
@@ -311,11 +355,14 @@ def selective_scan_bwd(u, delta, A, B, C, D=None, z=None, delta_bias=None,
          "dC": torch.empty((batch, dstate, seqlen), **f32),
          "dD": torch.empty((dim,), **f32) if D is not None else None,
          "dz": torch.empty_like(u) if z is not None else None,
-         "dbias": torch.empty((dim,), **f32) if delta_bias is not None else None}
-    status = ss_selective_scan_bwd(
+         "dbias": torch.empty((dim,), **f32) if delta_bias is not None else None,
+         "dh0": torch.empty((batch, dim, dstate), **f32) if h0 is not None else None}
+    if h0 is not None:
+        _check_tensors(u, (), (("h0", h0),))
+    status = ss_selective_scan_bwd_h0(
         _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias),
-        delta_softplus, _ptr(dy), _ptr(dlast_state),
-        *(_ptr(g[k]) for k in ("du", "ddelta", "dA", "dB", "dC", "dD", "dz", "dbias")),
+        delta_softplus, _ptr(h0), _ptr(dy), _ptr(dlast_state),
+        *(_ptr(g[k]) for k in ("du", "ddelta", "dA", "dB", "dC", "dD", "dz", "dbias", "dh0")),
         batch, dim, dstate, seqlen, io, _stream(stream, u.device))
     if status != SS_OK:
         raise SelectiveScanError(status, "ss_selective_scan_bwd")

@@ -70,6 +70,15 @@ def libraries() -> list[NativeLib]:
             deps=_kernel_headers(),
             extra=["-DSS_BUILDING_LIBRARY", "-Xptxas", "-warn-spills"],
         ))
+        # the same sources with the test hooks (plan overrides, skipped units)
+        # compiled in: loaded only by the tests that force scheduling modes or
+        # make a device wait run out
+        libs.insert(1, NativeLib(
+            "libss_selective_scan_test.so",
+            [api],
+            deps=_kernel_headers(),
+            extra=["-DSS_BUILDING_LIBRARY", "-DSS_TEST_HOOKS"],
+        ))
     return libs
 
 

@@ -13,6 +13,7 @@
 #include <cstring>
 #include <algorithm>
 #include <mutex>
+#include <utility>
 
 #include "ss_bwd.cuh"
 #include "ss_decode.cuh"
@@ -26,7 +27,12 @@ namespace {
 constexpr int kThreads = 64;  // threads per CTA
 constexpr int kRows = 2;      // channel rows per thread
 constexpr int kMaxChunks = 1024;
-constexpr int kStages = 4;    // depth of the per-thread u/delta/z copy ring
+// depth of the per-thread u/delta/z copy ring (16-byte vectors in flight): fp32
+// workloads run at one or two warps per scheduler and need the deeper ring to
+// cover HBM latency (measured: 6 beats 4 and 8 on the fp32 sequence sweep);
+// bf16 vectors hold twice the steps, and 4 is best there
+template <typename T>
+constexpr int kStages = sizeof(T) == 4 ? 6 : 4;
 constexpr int kCtasPerSm = 4; // resident CTAs per SM of the scheduled kernel
 
 bool range_overlap(const void* a, int64_t a_bytes, const void* b, int64_t b_bytes) {
@@ -106,10 +112,18 @@ struct LaunchPlan {
   int launches;
 };
 
+// Tuning and fault-injection knobs exist only in the test build of the
+// library (compiled with SS_TEST_HOOKS, loaded by the tests that need them);
+// the shipped library reads no environment variable.
+#ifdef SS_TEST_HOOKS
 int env_int(const char* name, int fallback) {
   const char* v = std::getenv(name);
   return v ? std::atoi(v) : fallback;
 }
+#define SS_TUNING(name, fallback) env_int(name, fallback)
+#else
+#define SS_TUNING(name, fallback) (fallback)
+#endif
 
 int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 
@@ -154,9 +168,8 @@ double decoupled_makespan(int64_t tiles, int64_t seqlen, int64_t len, int64_t sl
 // an aggregate pass in each decoupled unit; the chunk length is the one that
 // minimises decoupled_makespan.
 // Scalar path: aggregate, carry and main kernels over a fixed chunk grid.
-// SS_NCHUNKS and SS_CTAS_PER_SM override the heuristics (tuning aids);
-// SS_TEST_SKIP_UNITS (ss_selective_scan_fwd only) is the test hook that makes
-// the device-side waits run out.
+// In the test build SS_NCHUNKS and SS_CTAS_PER_SM override the heuristics, so
+// that the tests can force every scheduling mode and chunk shape.
 bool make_plan(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, int64_t elt,
                bool aligned16, int sms, LaunchPlan* plan) {
   plan->nt = dstate <= 4 ? 4 : (dstate <= 8 ? 8 : 16);
@@ -170,12 +183,12 @@ bool make_plan(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, int64
   plan->tiles = batch * plan->dim_tiles;
   const int64_t rows = batch * dim;
   const int64_t ns = (int64_t)plan->groups * plan->nt;
-  const int env_chunks = env_int("SS_NCHUNKS", 0);
+  const int env_chunks = SS_TUNING("SS_NCHUNKS", 0);
   plan->sched_bytes_per_group = plan->sched_bytes = plan->unit_agg_bytes = 0;
   plan->unit_incl_bytes = plan->agg_bytes = plan->carry_bytes = plan->part_bytes = 0;
   int64_t want;
   if (plan->vec) {
-    const int64_t cap = std::max(1, env_int("SS_CTAS_PER_SM", kCtasPerSm));
+    const int64_t cap = std::max(1, SS_TUNING("SS_CTAS_PER_SM", kCtasPerSm));
     const int64_t nsm = std::max(sms, 1);
     // chained chunks need at least as many row tiles as CTAs: take the largest
     // residency (at most cap CTAs per SM) that allows it
@@ -243,7 +256,7 @@ int64_t scratch_bytes(const LaunchPlan& plan) {
 
 template <typename T, int NT, int TGS, bool HAS_Z, bool MULTI>
 cudaError_t enqueue_vec(ss::FwdParams p, const LaunchPlan& plan, cudaStream_t st) {
-  auto kernel = ss::ss_fwd_sched<T, NT, TGS, kThreads, kStages, HAS_Z, MULTI>;
+  auto kernel = ss::ss_fwd_sched<T, NT, TGS, kThreads, kStages<T>, HAS_Z, MULTI>;
   char* sched = reinterpret_cast<char*>(p.ticket);
   for (int g = 0; g < plan.groups; ++g) {
     p.group = g;
@@ -393,6 +406,7 @@ ss_status_t fwd_impl(const void* u, const void* delta, const float* A, const voi
         return SS_ERR_CUDA;
       }
       p.ticket = reinterpret_cast<unsigned*>(base);
+#ifdef SS_TEST_HOOKS
       // test hook: the first SS_TEST_SKIP_UNITS units of every launch are
       // never handed out, so their successors' bounded waits run out
       const int skip = env_int("SS_TEST_SKIP_UNITS", 0);
@@ -405,6 +419,7 @@ ss_status_t fwd_impl(const void* u, const void* delta, const float* A, const voi
           return SS_ERR_CUDA;
         }
       }
+#endif
       base += plan.sched_bytes;
     }
     if (plan.unit_agg_bytes) {
@@ -515,29 +530,38 @@ SS_API ss_status_t ss_selective_state_update(
   return cudaGetLastError() == cudaSuccess ? SS_OK : SS_ERR_CUDA;
 }
 
-SS_API ss_status_t ss_selective_scan_bwd(
-    const void* u, const void* delta, const float* A, const void* B, const void* C,
-    const float* D, const void* z, const float* delta_bias, int delta_softplus,
-    const void* dy, const float* dlast_state, void* du, void* ddelta, float* dA, float* dB,
-    float* dC, float* dD, void* dz, float* dbias,
-    int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, ss_dtype_t dtype, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// The backward from an initial state h0 (null: zero), with its gradient dh0
+// (null: not written); both backward entry points land here.
+ss_status_t bwd_impl(const void* u, const void* delta, const float* A, const void* B,
+                     const void* C, const float* D, const void* z, const float* delta_bias,
+                     int delta_softplus, const float* h0, const void* dy,
+                     const float* dlast_state, void* du, void* ddelta, float* dA, float* dB,
+                     float* dC, float* dD, void* dz, float* dbias, float* dh0, int64_t batch,
+                     int64_t dim, int64_t dstate, int64_t seqlen, ss_dtype_t dtype,
+                     void* stream) {
   // ---- validation: nothing is enqueued or written on error ----
   if (dtype != SS_F32 && dtype != SS_BF16) return SS_ERR_UNSUPPORTED;
   if (!u || !delta || !A || !B || !C || !dy || !du || !ddelta || !dA || !dB || !dC)
     return SS_ERR_INVALID_ARGUMENT;
   if (z && !dz) return SS_ERR_INVALID_ARGUMENT;
   if (batch <= 0 || dim <= 0 || dstate <= 0 || seqlen <= 0) return SS_ERR_INVALID_ARGUMENT;
-  if (dstate > ss::kBwdLanes) return SS_ERR_UNSUPPORTED;
+  if (dstate > 256) return SS_ERR_UNSUPPORTED;
   const int64_t elt = dtype == SS_F32 ? 4 : 2;
   Sizes sz;
   if (!sizes_ok(batch, dim, dstate, seqlen, elt, &sz)) return SS_ERR_UNSUPPORTED;
+  const int groups = (int)((dstate + ss::kBwdLanes - 1) / ss::kBwdLanes);
+  const int64_t npad = (int64_t)groups * ss::kBwdLanes;
   const int64_t dtiles = (dim + ss::kBwdRows - 1) / ss::kBwdRows;
   const int64_t ctas = batch * dtiles;
   const int64_t nblk = (seqlen + ss::kBwdBlock - 1) / ss::kBwdBlock;
-  int64_t ck_elems, bc_elems, tmp;
+  int64_t ck_elems, bc_elems, row_elems = 0, tmp;
   if (!mul_ok(ctas * ss::kBwdRows * ss::kBwdLanes, nblk, &ck_elems) ||
-      !mul_ok(ctas * 2 * ss::kBwdLanes, seqlen, &bc_elems) || !mul_ok(ck_elems + bc_elems, 4, &tmp) ||
-      ctas > INT_MAX)
+      !mul_ok(ctas * 2 * npad, seqlen, &bc_elems) || !mul_ok(ck_elems + bc_elems, 4, &tmp) ||
+      (groups > 1 && !mul_ok(3 * sz.rows, seqlen, &row_elems)) || ctas > INT_MAX)
     return SS_ERR_UNSUPPORTED;
   const uintptr_t ea = (uintptr_t)elt;
   if (!aligned(u, ea) || !aligned(delta, ea) || !aligned(B, ea) || !aligned(C, ea) ||
@@ -545,29 +569,32 @@ SS_API ss_status_t ss_selective_scan_bwd(
       (dz && !aligned(dz, ea)) || !aligned(A, 4) || (D && !aligned(D, 4)) ||
       (delta_bias && !aligned(delta_bias, 4)) || (dlast_state && !aligned(dlast_state, 4)) ||
       !aligned(dA, 4) || !aligned(dB, 4) || !aligned(dC, 4) || (dD && !aligned(dD, 4)) ||
-      (dbias && !aligned(dbias, 4)))
+      (dbias && !aligned(dbias, 4)) || (h0 && !aligned(h0, 4)) || (dh0 && !aligned(dh0, 4)))
     return SS_ERR_INVALID_ARGUMENT;
   // outputs must not overlap any input, nor each other
-  const void* ins[] = {u, delta, A, B, C, D, z, delta_bias, dy, dlast_state};
+  const void* ins[] = {u, delta, A, B, C, D, z, delta_bias, dy, dlast_state, h0};
   const int64_t in_bytes[] = {sz.x_bytes, sz.x_bytes, sz.a_elems * 4, sz.bc_bytes, sz.bc_bytes,
                               D ? dim * 4 : 0, z ? sz.x_bytes : 0, delta_bias ? dim * 4 : 0,
-                              sz.x_bytes, dlast_state ? sz.st_elems * 4 : 0};
-  const void* outs[] = {du, ddelta, dz, dA, dB, dC, dD, dbias};
+                              sz.x_bytes, dlast_state ? sz.st_elems * 4 : 0,
+                              h0 ? sz.st_elems * 4 : 0};
+  const void* outs[] = {du, ddelta, dz, dA, dB, dC, dD, dbias, dh0};
   const int64_t out_bytes[] = {sz.x_bytes, sz.x_bytes, dz ? sz.x_bytes : 0, sz.a_elems * 4,
                                sz.bc_bytes / elt * 4, sz.bc_bytes / elt * 4, dD ? dim * 4 : 0,
-                               dbias ? dim * 4 : 0};
-  for (int o = 0; o < 8; ++o) {
-    for (int i = 0; i < 10; ++i)
+                               dbias ? dim * 4 : 0, (h0 && dh0) ? sz.st_elems * 4 : 0};
+  for (int o = 0; o < 9; ++o) {
+    for (int i = 0; i < 11; ++i)
       if (range_overlap(outs[o], out_bytes[o], ins[i], in_bytes[i])) return SS_ERR_INVALID_ARGUMENT;
-    for (int k = o + 1; k < 8; ++k)
+    for (int k = o + 1; k < 9; ++k)
       if (range_overlap(outs[o], out_bytes[o], outs[k], out_bytes[k])) return SS_ERR_INVALID_ARGUMENT;
   }
 
-  // ---- scratch: checkpoints, per-CTA dB/dC sums, per-row dA/dD/dbias sums ----
+  // ---- scratch: checkpoints, per-CTA dB/dC sums, per-row dA/dD/dbias sums,
+  //      and (several state groups) the row sums carried from group to group ----
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const int64_t a_elems = batch * dim * ss::kBwdLanes, dd_elems = batch * dim * 2;
+  const int64_t a_elems = batch * dim * npad, dd_elems = batch * dim * 2;
   const int64_t scratch = round_up(ck_elems * 4, 256) + round_up(bc_elems * 4, 256) +
-                          round_up(a_elems * 4, 256) + round_up(dd_elems * 4, 256);
+                          round_up(a_elems * 4, 256) + round_up(dd_elems * 4, 256) +
+                          round_up(row_elems * 4, 256);
   (void)cudaGetLastError();
   void* base = nullptr;
   if (cudaMallocAsync(&base, (size_t)scratch, st) != cudaSuccess) return SS_ERR_CUDA;
@@ -577,6 +604,7 @@ SS_API ss_status_t ss_selective_scan_bwd(
   p.softplus = delta_softplus ? 1 : 0;
   p.dy = dy; p.dlast = dlast_state; p.du = du; p.ddelta = ddelta; p.dz = dz;
   p.dA = dA; p.dB = dB; p.dC = dC; p.dD = D ? dD : nullptr; p.dbias = delta_bias ? dbias : nullptr;
+  p.h0 = h0; p.dh0 = h0 ? dh0 : nullptr;
   p.ckpt = reinterpret_cast<float*>(cur);
   cur += round_up(ck_elems * 4, 256);
   p.part_bc = reinterpret_cast<float*>(cur);
@@ -584,26 +612,49 @@ SS_API ss_status_t ss_selective_scan_bwd(
   p.part_a = reinterpret_cast<float*>(cur);
   cur += round_up(a_elems * 4, 256);
   p.part_dd = reinterpret_cast<float*>(cur);
+  cur += round_up(dd_elems * 4, 256);
+  p.part_row = groups > 1 ? reinterpret_cast<float*>(cur) : nullptr;
+  p.npad = (int)npad;
   p.batch = batch; p.dim = dim; p.dstate = dstate; p.seqlen = seqlen;
   p.dtiles = dtiles; p.nblk = nblk;
   p.vec = seqlen % (16 / elt) == 0 && aligned(u, 16) && aligned(delta, 16) && aligned(dy, 16) &&
           (!z || aligned(z, 16));
   // the backward is latency-bound: the whole shared memory for resident CTAs
   static const bool carveout = [] {
-    for (auto k : {(const void*)ss::ss_bwd_main<float, true>, (const void*)ss::ss_bwd_main<float, false>,
-                   (const void*)ss::ss_bwd_main<__nv_bfloat16, true>,
-                   (const void*)ss::ss_bwd_main<__nv_bfloat16, false>})
+    for (auto k : {(const void*)ss::ss_bwd_main<float, true, false>,
+                   (const void*)ss::ss_bwd_main<float, false, false>,
+                   (const void*)ss::ss_bwd_main<__nv_bfloat16, true, false>,
+                   (const void*)ss::ss_bwd_main<__nv_bfloat16, false, false>,
+                   (const void*)ss::ss_bwd_main<float, true, true>,
+                   (const void*)ss::ss_bwd_main<float, false, true>,
+                   (const void*)ss::ss_bwd_main<__nv_bfloat16, true, true>,
+                   (const void*)ss::ss_bwd_main<__nv_bfloat16, false, true>})
       cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     return true;
   }();
   (void)carveout;
   (void)cudaGetLastError();
-  if (dtype == SS_F32) {
-    if (z) ss::ss_bwd_main<float, true><<<(unsigned)ctas, ss::kBwdThreads, 0, st>>>(p);
-    else ss::ss_bwd_main<float, false><<<(unsigned)ctas, ss::kBwdThreads, 0, st>>>(p);
-  } else {
-    if (z) ss::ss_bwd_main<__nv_bfloat16, true><<<(unsigned)ctas, ss::kBwdThreads, 0, st>>>(p);
-    else ss::ss_bwd_main<__nv_bfloat16, false><<<(unsigned)ctas, ss::kBwdThreads, 0, st>>>(p);
+  const unsigned grid = (unsigned)ctas;
+  for (int g = 0; g < groups; ++g) {
+    p.group = g;
+    p.final_group = g == groups - 1;
+    if (groups == 1) {
+      if (dtype == SS_F32) {
+        if (z) ss::ss_bwd_main<float, true, false><<<grid, ss::kBwdThreads, 0, st>>>(p);
+        else ss::ss_bwd_main<float, false, false><<<grid, ss::kBwdThreads, 0, st>>>(p);
+      } else {
+        if (z) ss::ss_bwd_main<__nv_bfloat16, true, false><<<grid, ss::kBwdThreads, 0, st>>>(p);
+        else ss::ss_bwd_main<__nv_bfloat16, false, false><<<grid, ss::kBwdThreads, 0, st>>>(p);
+      }
+    } else {
+      if (dtype == SS_F32) {
+        if (z) ss::ss_bwd_main<float, true, true><<<grid, ss::kBwdThreads, 0, st>>>(p);
+        else ss::ss_bwd_main<float, false, true><<<grid, ss::kBwdThreads, 0, st>>>(p);
+      } else {
+        if (z) ss::ss_bwd_main<__nv_bfloat16, true, true><<<grid, ss::kBwdThreads, 0, st>>>(p);
+        else ss::ss_bwd_main<__nv_bfloat16, false, true><<<grid, ss::kBwdThreads, 0, st>>>(p);
+      }
+    }
   }
   const int sms = std::max(1, sm_count());
   const int64_t bc_total = batch * dstate * seqlen, rows_total = dim * dstate;
@@ -614,6 +665,32 @@ SS_API ss_status_t ss_selective_scan_bwd(
   const cudaError_t err = cudaGetLastError();
   const cudaError_t ferr = cudaFreeAsync(base, st);
   return err == cudaSuccess && ferr == cudaSuccess ? SS_OK : SS_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+SS_API ss_status_t ss_selective_scan_bwd(
+    const void* u, const void* delta, const float* A, const void* B, const void* C,
+    const float* D, const void* z, const float* delta_bias, int delta_softplus,
+    const void* dy, const float* dlast_state, void* du, void* ddelta, float* dA, float* dB,
+    float* dC, float* dD, void* dz, float* dbias,
+    int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, ss_dtype_t dtype, void* stream) {
+  return bwd_impl(u, delta, A, B, C, D, z, delta_bias, delta_softplus, nullptr, dy, dlast_state,
+                  du, ddelta, dA, dB, dC, dD, dz, dbias, nullptr, batch, dim, dstate, seqlen,
+                  dtype, stream);
+}
+
+SS_API ss_status_t ss_selective_scan_bwd_h0(
+    const void* u, const void* delta, const float* A, const void* B, const void* C,
+    const float* D, const void* z, const float* delta_bias, int delta_softplus, const float* h0,
+    const void* dy, const float* dlast_state, void* du, void* ddelta, float* dA, float* dB,
+    float* dC, float* dD, void* dz, float* dbias, float* dh0,
+    int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, ss_dtype_t dtype, void* stream) {
+  return bwd_impl(u, delta, A, B, C, D, z, delta_bias, delta_softplus, h0, dy, dlast_state, du,
+                  ddelta, dA, dB, dC, dD, dz, dbias, dh0, batch, dim, dstate, seqlen, dtype,
+                  stream);
 }
 
 SS_API ss_status_t ss_selective_scan_fwd_pc(
@@ -808,23 +885,59 @@ constexpr int kNoAllocMaxDevices = 64;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 std::mutex g_noalloc_mutex;
-void* g_noalloc_address[kNoAllocMaxDevices] = {};
+struct NoallocAddress {
+  unsigned long long ctx_id = 0;  // the context the address belongs to (0: none yet)
+  void* ptr = nullptr;
+};
+NoallocAddress g_noalloc_address[kNoAllocMaxDevices];
 
-// Device address of the buffer on the current device, looked up once per
-// device (the first call on a device does this set-up).
+// Unique id of the current context (driver API, looked up through the
+// runtime), or 0 if it cannot be had.
+unsigned long long current_context_id() {
+  using GetCurrent = CUresult (*)(CUcontext*);
+  using GetId = CUresult (*)(CUcontext, unsigned long long*);
+  static const std::pair<GetCurrent, GetId> fns = [] {
+    void* a = nullptr;
+    void* b = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &a, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess || q != cudaDriverEntryPointSuccess)
+      a = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &b, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess || q != cudaDriverEntryPointSuccess)
+      b = nullptr;
+    return std::make_pair(reinterpret_cast<GetCurrent>(a), reinterpret_cast<GetId>(b));
+  }();
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (!fns.first || !fns.second || fns.first(&ctx) != CUDA_SUCCESS || !ctx ||
+      fns.second(ctx, &id) != CUDA_SUCCESS)
+    return 0;
+  return id;
+}
+
+// Device address of the buffer in the current context.  It is looked up with
+// cudaGetSymbolAddress once per device context (the first call on a device
+// does this set-up), and again whenever the context changed, e.g. after a
+// cudaDeviceReset: the module is then loaded anew and its buffer can move.
 cudaError_t noalloc_scratch(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kNoAllocMaxDevices) return cudaErrorInvalidDevice;
+  // 0 before the runtime has made the device's context current: then the
+  // lookup below (which creates it) runs, and the next call records its id
+  const unsigned long long ctx = current_context_id();
   std::lock_guard<std::mutex> lock(g_noalloc_mutex);
-  if (!g_noalloc_address[dev]) {
+  NoallocAddress& a = g_noalloc_address[dev];
+  if (ctx == 0 || a.ptr == nullptr || a.ctx_id != ctx) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess) return e;
-    g_noalloc_address[dev] = p;
+    a.ptr = p;
+    a.ctx_id = ctx;
   }
-  *out = g_noalloc_address[dev];
+  *out = a.ptr;
   return cudaSuccess;
 }
 
@@ -842,7 +955,59 @@ void set_chunks(LaunchPlan* plan, int64_t seqlen, int64_t slots, int64_t want) {
   plan->unit_incl_bytes = round_up(rec * 4, 256);
 }
 
+// Plan of the no-allocation entry point: the regular vector-path plan with the
+// largest chunk count, at most the regular one, whose carries fit the fixed
+// buffer.  SS_ERR_SCRATCH_LIMIT if even one chunk does not fit.
+ss_status_t noalloc_plan(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, int64_t elt,
+                         int sms, LaunchPlan* plan) {
+  if (!make_plan(batch, dim, dstate, seqlen, elt, true, sms, plan) || !plan->vec)
+    return SS_ERR_UNSUPPORTED;
+  for (int64_t n = plan->nchunks; scratch_bytes(*plan) > kNoAllocScratchBytes && n > 1;) {
+    set_chunks(plan, seqlen, plan->slots, --n);
+    n = std::min<int64_t>(n, plan->nchunks);
+  }
+  if (plan->nchunks == 1) plan->unit_agg_bytes = plan->unit_incl_bytes = 0;  // no carries
+  return scratch_bytes(*plan) > kNoAllocScratchBytes ? SS_ERR_SCRATCH_LIMIT : SS_OK;
+}
+
 }  // namespace
+
+#ifdef SS_TEST_HOOKS
+// ---- test build only: inspection of the no-allocation entry point ----------------
+extern "C" {
+// The plan ss_selective_scan_fwd_noalloc would run (host only).
+SS_API ss_status_t ss_test_noalloc_plan(int64_t batch, int64_t dim, int64_t dstate,
+                                        int64_t seqlen, ss_dtype_t dtype, int sm_count,
+                                        ss_plan_t* out) {
+  if (dtype != SS_F32 && dtype != SS_BF16) return SS_ERR_UNSUPPORTED;
+  LaunchPlan plan{};
+  const ss_status_t st =
+      noalloc_plan(batch, dim, dstate, seqlen, dtype == SS_F32 ? 4 : 2, sm_count, &plan);
+  if (st != SS_OK) return st;
+  out->nchunks = plan.nchunks;
+  out->chunk_len = plan.chunk_len;
+  out->state_groups = plan.groups;
+  out->ctas = plan.grid;
+  out->kernel_launches = plan.launches;
+  out->scratch_bytes = scratch_bytes(plan);
+  out->vector_path = 1;
+  return SS_OK;
+}
+// The buffer address the entry point would use now, and a fresh lookup.
+SS_API int ss_test_noalloc_addresses(void** used, void** fresh) {
+  if (noalloc_scratch(used) != cudaSuccess) return 1;
+  return cudaGetSymbolAddress(fresh, g_noalloc_scratch) == cudaSuccess ? 0 : 2;
+}
+// Runtime calls of the library's own CUDA runtime, for a test process that
+// resets the device without torch.
+SS_API int ss_test_device_reset() { return (int)cudaDeviceReset(); }
+SS_API int ss_test_malloc(void** p, size_t bytes) { return (int)cudaMalloc(p, bytes); }
+SS_API int ss_test_free(void* p) { return (int)cudaFree(p); }
+SS_API int ss_test_memcpy(void* dst, const void* src, size_t bytes) {
+  return (int)cudaMemcpy(dst, src, bytes, cudaMemcpyDefault);
+}
+}  // extern "C"
+#endif
 
 extern "C" SS_API ss_status_t ss_selective_scan_fwd_noalloc(
     const void* u, const void* delta, const float* A, const void* B, const void* C,
@@ -882,14 +1047,8 @@ extern "C" SS_API ss_status_t ss_selective_scan_fwd_noalloc(
   const int sms = sm_count();
   if (sms <= 0) return SS_ERR_CUDA;
   LaunchPlan plan{};
-  if (!make_plan(batch, dim, dstate, seqlen, elt, true, sms, &plan) || !plan.vec)
-    return SS_ERR_UNSUPPORTED;
-  while (scratch_bytes(plan) > kNoAllocScratchBytes && plan.nchunks > 1)
-    set_chunks(&plan, seqlen, plan.slots, plan.nchunks / 2);
-  if (plan.nchunks == 1) {  // one chunk needs no carries
-    plan.unit_agg_bytes = plan.unit_incl_bytes = 0;
-  }
-  if (scratch_bytes(plan) > kNoAllocScratchBytes) return SS_ERR_SCRATCH_LIMIT;
+  const ss_status_t planned = noalloc_plan(batch, dim, dstate, seqlen, elt, sms, &plan);
+  if (planned != SS_OK) return planned;
 
   void* base_ptr = nullptr;
   if (noalloc_scratch(&base_ptr) != cudaSuccess) return SS_ERR_CUDA;

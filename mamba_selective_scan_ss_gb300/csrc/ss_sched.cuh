@@ -115,10 +115,12 @@ __device__ __forceinline__ unsigned look_back(const unsigned* flags, int64_t M, 
   }
 }
 
-// Test hook of the host (SS_TEST_SKIP_UNITS): start a launch's ticket counter
-// at `first`, so units below it are never handed out and the waits of their
+#ifdef SS_TEST_HOOKS
+// Test hook of the host (test build only): start a launch's ticket counter at
+// `first`, so units below it are never handed out and the waits of their
 // successors run out (bounded; the device error word reports it).
 __global__ void ss_set_ticket(unsigned* ticket, unsigned first) { *ticket = first; }
+#endif
 
 template <int TGS, int TPB>
 struct PairRows {
@@ -243,7 +245,7 @@ __device__ __forceinline__ void scan_pass(const FwdParams& p,
 #pragma unroll
       for (int m = 0; m < VP; ++m) {
         const f2 x = add2(dp[m], splat(bias[o]));
-        const f2 sp = softplus2(x);
+        const f2 sp = softplus2<std::is_same<T, __nv_bfloat16>::value>(x);
         f2 dtm;
         dtm.v = use_softplus ? sp.v : x.v;
         const f2 dum = mul2(dtm, u_o[o][m]);
@@ -266,6 +268,9 @@ __device__ __forceinline__ void scan_pass(const FwdParams& p,
   cp_async_wait<STAGES - 2>();  // vector 0 landed
   rowwork(0, dts, dus, up, zp);
 
+  // unrolled by two so that the hand-over of the next vector's row work
+  // (dts_n -> dts, ...) becomes register renaming instead of moves
+#pragma unroll 2
   for (int64_t j = 0; j < nvec; ++j) {
     issue_vec(j + STAGES - 1);
     cp_async_wait<STAGES - 2>();  // this lane's copies of vector j+1 (and older) landed

@@ -26,7 +26,8 @@ def declared_functions():
 
 
 def test_header_declares_the_entry_points():
-    assert declared_functions() == ["ss_mamba2_fwd", "ss_selective_scan_bwd", "ss_selective_scan_check",
+    assert declared_functions() == ["ss_mamba2_fwd", "ss_selective_scan_bwd",
+                                    "ss_selective_scan_bwd_h0", "ss_selective_scan_check",
                                     "ss_selective_scan_fwd",
                                     "ss_selective_scan_fwd_h0", "ss_selective_scan_fwd_noalloc",
                                     "ss_selective_scan_fwd_pc",
@@ -41,6 +42,17 @@ def test_library_exports_every_declared_symbol(lib):
     for name in declared_functions():
         assert name in exported, name
         assert hasattr(lib, name)
+
+
+def test_shipped_library_has_no_test_hooks(lib):
+    """The tuning overrides and the unit-skipping hook live only in the test
+    build: the shipped library neither names their variables nor exports the
+    hook's kernel."""
+    shipped = ss.library_path().read_bytes()
+    for name in (b"SS_TEST_SKIP_UNITS", b"SS_NCHUNKS", b"SS_CTAS_PER_SM", b"ss_set_ticket"):
+        assert name not in shipped, name
+    test = ss.library_path(test_build=True).read_bytes()
+    assert b"SS_TEST_SKIP_UNITS" in test and b"SS_NCHUNKS" in test
 
 
 def test_status_strings(lib):
@@ -139,12 +151,27 @@ def test_validation_of_the_backward(lib):
     assert call(dy=None) == ss.SS_ERR_INVALID_ARGUMENT
     assert call(dB=None) == ss.SS_ERR_INVALID_ARGUMENT
     assert call(dz=None) == ss.SS_ERR_INVALID_ARGUMENT          # z given, dz missing
-    assert call(dstate=17) == ss.SS_ERR_UNSUPPORTED             # backward: dstate <= 16
+    assert call(dstate=257) == ss.SS_ERR_UNSUPPORTED            # backward: dstate <= 256
     assert call(seqlen=0) == ss.SS_ERR_INVALID_ARGUMENT
     assert call(dtype=3) == ss.SS_ERR_UNSUPPORTED
     assert call(du=ok["u"]) == ss.SS_ERR_INVALID_ARGUMENT       # output over an input
     assert call(dC=ok["dB"] + 8) == ss.SS_ERR_INVALID_ARGUMENT  # two outputs overlap
     assert call(dA=ok["dA"] + 2) == ss.SS_ERR_INVALID_ARGUMENT  # misaligned fp32 output
+
+    # the initial-state variant: h0 is an input, dh0 an output
+    extra = [ctypes.create_string_buffer(4096) for _ in range(2)]
+    h0, dh0 = (ctypes.addressof(b) for b in extra)
+
+    def call_h0(**kw):
+        args = dict(ok, h0=h0, dh0=dh0)
+        args.update(kw)
+        return ss.ss_selective_scan_bwd_h0(**args)
+
+    assert call_h0(dh0=ok["u"]) == ss.SS_ERR_INVALID_ARGUMENT   # dh0 over an input
+    assert call_h0(dh0=ok["dA"]) == ss.SS_ERR_INVALID_ARGUMENT  # dh0 over another output
+    assert call_h0(du=h0) == ss.SS_ERR_INVALID_ARGUMENT         # an output over h0
+    assert call_h0(h0=h0 + 2) == ss.SS_ERR_INVALID_ARGUMENT     # misaligned h0
+    assert call_h0(dstate=257) == ss.SS_ERR_UNSUPPORTED
 
 
 
@@ -189,11 +216,17 @@ def test_plan_is_host_only_and_consistent(lib, monkeypatch):
     assert p["vector_path"] == 0
     assert ss.ss_selective_scan_plan(2, 64, 16, 256, ss.SS_BF16, False, 152)["vector_path"] == 0
     monkeypatch.setenv("SS_NCHUNKS", "4")
-    p = ss.ss_selective_scan_plan(2, 64, 16, 1024, ss.SS_F32, False, 152)
-    assert p["nchunks"] == 4 and p["kernel_launches"] == 3
-    assert p["scratch_bytes"] == 3 * 128 * 16 * 8 + 4 * 128 * 16 * 4
-    # the tuning override forces the chunk count on the vector path too
-    assert ss.ss_selective_scan_plan(2, 64, 16, 1024, ss.SS_F32, True, 152)["nchunks"] == 4
+    # the shipped library reads no environment variable: the plan is unchanged
+    plain = ss.ss_selective_scan_plan(2, 64, 16, 1024, ss.SS_F32, True, 152)
+    monkeypatch.delenv("SS_NCHUNKS")
+    assert plain == ss.ss_selective_scan_plan(2, 64, 16, 1024, ss.SS_F32, True, 152)
+    # the test build honours the override, on both paths
+    monkeypatch.setenv("SS_NCHUNKS", "4")
+    with ss.test_hooks():
+        p = ss.ss_selective_scan_plan(2, 64, 16, 1024, ss.SS_F32, False, 152)
+        assert p["nchunks"] == 4 and p["kernel_launches"] == 3
+        assert p["scratch_bytes"] == 3 * 128 * 16 * 8 + 4 * 128 * 16 * 4
+        assert ss.ss_selective_scan_plan(2, 64, 16, 1024, ss.SS_F32, True, 152)["nchunks"] == 4
     with pytest.raises(ss.SelectiveScanError):
         ss.ss_selective_scan_plan(0, 64, 16, 1024, ss.SS_F32, True, 152)
     with pytest.raises(ss.SelectiveScanError):

@@ -60,21 +60,26 @@ def compare(got, ref, name, dtype):
                                   f"(max |err| {err.max():.3e}, scale {scale:.3e})")
 
 
-def run_case(orc, w, seed=5, with_dlast=False, softplus=True):
+def run_case(orc, w, seed=5, with_dlast=False, softplus=True, with_h0=False):
     inp = make_inputs(w)
     dy, dlast = grad_inputs(w, seed, with_dlast)
     if not softplus:
         inp["delta"] = (inp["delta"].float().abs() * 0.05).to(inp["delta"].dtype)
         inp["delta_bias"] = None
+    h0 = None
+    if with_h0:
+        h0 = torch.randn((w.batch, w.dim, w.dstate), generator=torch.Generator().manual_seed(seed + 1))
     d = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
     got = ss.selective_scan_bwd(d["u"], d["delta"], d["A"], d["B"], d["C"], d["D"], d["z"],
                                 d["delta_bias"], softplus, dy=dy.cuda(),
-                                dlast_state=None if dlast is None else dlast.cuda())
+                                dlast_state=None if dlast is None else dlast.cuda(),
+                                h0=None if h0 is None else h0.cuda())
     torch.cuda.synchronize()
     ref = orc.bwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"], inp["z"],
                   inp["delta_bias"], softplus, dy=dy,
+                  h0=None if h0 is None else h0.double().numpy(),
                   dlast=None if dlast is None else dlast.double().numpy(), dtype=w.dtype)
-    for name in ("du", "ddelta", "dA", "dB", "dC", "dD", "dz", "dbias"):
+    for name in ("du", "ddelta", "dA", "dB", "dC", "dD", "dz", "dbias", "dh0"):
         if ref[name] is None:
             assert got[name] is None, name
             continue
@@ -90,9 +95,20 @@ def test_backward_matches_oracle(orc, dtype, shape):
     run_case(orc, W(*shape, dtype=dtype, seed=71))
 
 
-@pytest.mark.parametrize("dstate", [1, 2, 4, 7, 8, 12, 16])
+@pytest.mark.parametrize("dstate", [1, 2, 4, 7, 8, 12, 16, 17, 24, 32, 33, 64])
 def test_backward_dstate(orc, dstate):
+    """Up to 16 states in one group; above, groups of 16 whose row sums
+    (d(dt), du, the gate's pre-activation) are carried from group to group."""
     run_case(orc, W(2, 40, dstate, 96, seed=72))
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("shape", [(2, 64, 16, 64), (1, 70, 16, 37), (2, 40, 16, 300),
+                                   (2, 33, 40, 120), (1, 20, 5, 9), (1, 8, 256, 40)])
+def test_backward_from_initial_state(orc, dtype, shape):
+    """ss_selective_scan_bwd_h0: h0 enters the recompute (and dA through the
+    first decay), and dh0 = exp(dt_0 A) g_0 comes back."""
+    run_case(orc, W(*shape, dtype=dtype, seed=79), with_dlast=True, with_h0=True)
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
@@ -113,8 +129,10 @@ def test_backward_full_size_sampled_batch_row(orc):
     bf16 I/O, z gate) in the benchmark's launch: 640 CTAs of 64 rows, 256
     checkpointed blocks per row.  One batch row is checked whole against the
     oracle run on that row alone: du, ddelta and dz of its 5120 channels, and
-    dB, dC, which sum over exactly those channels.  dA, dD and dbias also sum
-    over the batch rows; the small cases cover them."""
+    dB, dC, which sum over exactly those channels.  dA, dD and dbias sum over
+    every batch row and step of one channel, so sampled channels are checked
+    with the oracle run on those channels of all eight batch rows (which also
+    gives their du, ddelta and dz in every row)."""
     w = WORKLOADS["2"]
     inp = make_inputs(w)
     dy, _ = grad_inputs(w, 91, False)
@@ -129,6 +147,16 @@ def test_backward_full_size_sampled_batch_row(orc):
                   row["delta_bias"], True, dy=dy[b:b + 1].contiguous(), dtype=w.dtype)
     for name in ("du", "ddelta", "dz", "dB", "dC"):
         compare(got[name][b:b + 1], ref[name], name, w.dtype)
+    ch = [0, 1, 2047, 2048, 4095, 5119]
+    cols = {k: (inp[k][:, ch].contiguous() if k in ("u", "delta", "z") else
+                inp[k][ch].contiguous() if k in ("A", "D", "delta_bias") else inp[k])
+            for k in inp}
+    ref = orc.bwd(cols["u"], cols["delta"], cols["A"], cols["B"], cols["C"], cols["D"],
+                  cols["z"], cols["delta_bias"], True, dy=dy[:, ch].contiguous(), dtype=w.dtype)
+    for name in ("dA", "dD", "dbias"):
+        compare(got[name][ch], ref[name], name, w.dtype)
+    for name in ("du", "ddelta", "dz"):
+        compare(got[name][:, ch], ref[name], name, w.dtype)
 
 
 def test_backward_is_deterministic():
@@ -144,8 +172,8 @@ def test_backward_is_deterministic():
             assert torch.equal(runs[0][name], runs[1][name]), name
 
 
-def test_backward_rejects_more_than_16_states():
-    w = W(1, 8, 17, 16, seed=78)
+def test_backward_rejects_more_than_256_states():
+    w = W(1, 8, 257, 16, seed=78)
     inp = make_inputs(w)
     d = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
     with pytest.raises(ss.SelectiveScanError):

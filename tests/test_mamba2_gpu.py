@@ -14,6 +14,13 @@ positive, so these bound the sums of |term|):
 That bound is rigorous but loose where terms cancel, so the normwise error is
 also held to 4u: ||y - ref|| <= 4u ||ref||, a few independent roundings of u
 each (a misplaced decay step or a dropped term is off by 1e-2..1 of the norm).
+The bound fixed for bf16 I/O in the Mamba-1 forward, |err| <= 1e-2 (1 + |ref|)
+element by element, is NOT met everywhere by this kernel: its bf16 derived
+operands (above all w.x in the chunk-state product, whose rounding the
+carried state passes on to the next chunk) leave elements whose reference is
+small against its terms up to about 3x that bound (measured: 1.09x on the
+small workload, 2.83x on the first step of a chunk of one step).  The ratio
+is computed and printed for every case so that the shortfall stays visible.
 """
 import numpy as np
 import pytest
@@ -64,11 +71,15 @@ def check(got_y, got_s, ref_y, ref_s, abs_y, abs_s):
     assert np.all(err <= bound), f"y: max |err|/bound {np.max(err / bound):.3g}"
     norm = np.linalg.norm(gy - ref_y) / max(np.linalg.norm(ref_y), 1e-30)
     assert norm <= 4 * U, f"y: normwise error {norm:.3e} > {4 * U:.3e}"
+    io = err / (1e-2 * (1 + np.abs(ref_y)))
+    print(f"[bf16 I/O bound] y: worst |err| / (1e-2 (1+|ref|)) = {io.max():.3g}")
     if got_s is not None:
         gs = got_s.cpu().numpy().astype(np.float64)
         err_s = np.abs(gs - ref_s)
         bound_s = 1.1 * U * abs_s + 1e-6
         assert np.all(err_s <= bound_s), f"state: max |err|/bound {np.max(err_s / bound_s):.3g}"
+        io_s = err_s / (1e-2 * (1 + np.abs(ref_s)))
+        print(f"[bf16 I/O bound] state: worst |err| / (1e-2 (1+|ref|)) = {io_s.max():.3g}")
 
 
 def run(inp, softplus=True, final=True):

@@ -115,11 +115,25 @@ def test_optional_inputs(orc, dtype, opts):
     check(orc, w, inp)
 
 
+# ---- dt = softplus(delta + bias) over its whole range ----
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("seqlen", [1, 64])
+def test_softplus_sweep(orc, dtype, seqlen):
+    """delta + bias swept over [-20, 20] across channels, so dt runs from 2e-9
+    to 20 through the kernel's softplus: seqlen 1 is the closed form of a
+    single step (the scalar path), seqlen 64 the vector path's polynomial."""
+    w = W(1, 4096, 16, seqlen, dtype, seed=41)
+    inp = make_inputs(w)
+    inp["delta_bias"] = torch.linspace(-20.0, 20.0, w.dim, dtype=torch.float32)
+    inp["delta"] = (0.01 * inp["delta"].float()).to(inp["delta"].dtype)
+    check(orc, w, inp)
+
+
 # ---- sequence split into chunks joined by the eq (10) operator ----
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("nchunks", [2, 3, 7, 16])
 @pytest.mark.parametrize("L,dstate", [(1000, 16), (4096, 16), (777, 33), (640, 8)])
-def test_chunked_sequence(orc, monkeypatch, dtype, nchunks, L, dstate):
+def test_chunked_sequence(test_build, orc, monkeypatch, dtype, nchunks, L, dstate):
     monkeypatch.setenv("SS_NCHUNKS", str(nchunks))
     check(orc, W(2, 70, dstate, L, dtype, seed=nchunks + L, dt_lo=1e-4, dt_hi=1e-2))
 
@@ -131,7 +145,7 @@ def test_chunked_sequence(orc, monkeypatch, dtype, nchunks, L, dstate):
     (2, (2, 5120, 16, 1024), 8),   # fewer tiles than CTAs: decoupled, long look-backs
     (4, (1, 256, 16, 4096), 32),   # few tiles, many chunks: decoupled look-back
 ])
-def test_scheduler_modes(orc, monkeypatch, dtype, ctas_per_sm, shape, nchunks):
+def test_scheduler_modes(test_build, orc, monkeypatch, dtype, ctas_per_sm, shape, nchunks):
     monkeypatch.setenv("SS_CTAS_PER_SM", str(ctas_per_sm))
     monkeypatch.setenv("SS_NCHUNKS", str(nchunks))
     w = W(*shape, dtype, seed=ctas_per_sm * 7 + nchunks, dt_lo=1e-4, dt_hi=1e-2)
@@ -174,7 +188,7 @@ def test_unaligned_rows(orc, dtype):
 # ---- bounds: guard bands around every output stay untouched ----
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("shape", [(2, 130, 16, 200), (1, 3, 5, 37)])
-def test_guard_bands(orc, monkeypatch, dtype, shape):
+def test_guard_bands(test_build, orc, monkeypatch, dtype, shape):
     monkeypatch.setenv("SS_NCHUNKS", "3")
     w = W(*shape, dtype, seed=11)
     inp = make_inputs(w)

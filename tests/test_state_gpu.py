@@ -104,7 +104,7 @@ H0_CASES = [
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("shape,nchunks", H0_CASES)
-def test_forward_from_initial_state(orc, monkeypatch, dtype, shape, nchunks):
+def test_forward_from_initial_state(test_build, orc, monkeypatch, dtype, shape, nchunks):
     if nchunks:
         monkeypatch.setenv("SS_NCHUNKS", str(nchunks))
     w = W(*shape, dtype=dtype, seed=31)
@@ -125,7 +125,7 @@ def test_forward_from_initial_state(orc, monkeypatch, dtype, shape, nchunks):
 @pytest.mark.parametrize("shape,nchunks", [((4, 640, 16, 512), 4), ((1, 64, 16, 2048), 9),
                                            ((2, 40, 16, 301), 3), ((1, 64, 16, 256), 1),
                                            ((1, 40, 24, 512), 4)])
-def test_state_updated_in_place(orc, monkeypatch, dtype, shape, nchunks):
+def test_state_updated_in_place(test_build, orc, monkeypatch, dtype, shape, nchunks):
     """last_state may be h0 itself: every chunk must still start from the old state."""
     monkeypatch.setenv("SS_NCHUNKS", str(nchunks))
     w = W(*shape, dtype=dtype, seed=33)

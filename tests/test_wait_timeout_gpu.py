@@ -43,7 +43,7 @@ def _run(inp):
 
 
 @pytest.mark.parametrize("mode", ["decoupled", "chained"])
-def test_wait_that_runs_out_is_reported(monkeypatch, mode):
+def test_wait_that_runs_out_is_reported(test_build, monkeypatch, mode):
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     monkeypatch.setenv("SS_NCHUNKS", "2")
     if mode == "decoupled":
