@@ -502,30 +502,32 @@ SS_API ss_status_t ss_selective_state_update(
   ss::DecodeParams p{};
   p.state = state; p.x = x; p.dt = dt; p.A = A; p.B = B; p.C = C; p.D = D; p.z = z;
   p.bias = dt_bias; p.y = y;
-  p.dim = dim; p.dstate = dstate;
+  p.batch = batch; p.dim = dim; p.dstate = dstate;
   p.softplus = dt_softplus ? 1 : 0;
   p.quads = (int)((dstate + 3) / 4);
   // lanes per row: enough that no lane holds more than kDecodeQuads quads
   p.seg_shift = 0;
   while ((ss::kDecodeQuads << p.seg_shift) < p.quads) ++p.seg_shift;
-  const int64_t blocks_x = ((dim << p.seg_shift) + 255) / 256;
+  const int64_t blocks_x = ((dim << p.seg_shift) + ss::kDecodeThreads - 1) / ss::kDecodeThreads;
   if (blocks_x > INT_MAX) return SS_ERR_UNSUPPORTED;
+  // batch rows per CTA: as many as fit (up to kDecodeRows) while the CTAs
+  // still cover every SM a few times
+  const int64_t sms = std::max(1, sm_count());
+  p.rows_per_cta = std::max<int64_t>(
+      1, std::min<int64_t>(ss::kDecodeRows, (batch * blocks_x) / (4 * sms)));
+  const int64_t groups = (batch + p.rows_per_cta - 1) / p.rows_per_cta;
+  if (groups > 65535) return SS_ERR_UNSUPPORTED;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   (void)cudaGetLastError();
-  const int64_t bcv = dtype == SS_F32 ? 16 : 8;  // bytes of four B/C elements
-  const bool vec4 = dstate % 4 == 0 && aligned(state, 16) && aligned(A, 16) &&
-                    aligned(B, (uintptr_t)bcv) && aligned(C, (uintptr_t)bcv);
-  constexpr int64_t kMaxGridY = 65535;
-  for (int64_t b0 = 0; b0 < batch; b0 += kMaxGridY) {  // grid.y = batch rows
-    p.batch0 = b0;
-    const dim3 grid((unsigned)blocks_x, (unsigned)std::min(kMaxGridY, batch - b0));
-    if (dtype == SS_F32) {
-      if (vec4) ss::ss_state_update<float, true><<<grid, 256, 0, st>>>(p);
-      else ss::ss_state_update<float, false><<<grid, 256, 0, st>>>(p);
-    } else {
-      if (vec4) ss::ss_state_update<__nv_bfloat16, true><<<grid, 256, 0, st>>>(p);
-      else ss::ss_state_update<__nv_bfloat16, false><<<grid, 256, 0, st>>>(p);
-    }
+  const bool vec4 = dstate % 4 == 0 && aligned(state, 16) && aligned(A, 16);
+  const dim3 grid((unsigned)blocks_x, (unsigned)groups);
+  constexpr int kT = ss::kDecodeThreads;
+  if (dtype == SS_F32) {
+    if (vec4) ss::ss_state_update<float, true><<<grid, kT, 0, st>>>(p);
+    else ss::ss_state_update<float, false><<<grid, kT, 0, st>>>(p);
+  } else {
+    if (vec4) ss::ss_state_update<__nv_bfloat16, true><<<grid, kT, 0, st>>>(p);
+    else ss::ss_state_update<__nv_bfloat16, false><<<grid, kT, 0, st>>>(p);
   }
   return cudaGetLastError() == cudaSuccess ? SS_OK : SS_ERR_CUDA;
 }
