@@ -300,10 +300,47 @@ __global__ void k_update(float* out, int steps, ClockRec* rec) {
   out[blockIdx.x * blockDim.x + threadIdx.x] = ysum;
 }
 
+// Shared-memory loads as the scan kernel issues them for B and C: 16 bytes per
+// lane.  MODE 0: every lane of a warp reads the same 16 bytes (a broadcast, as
+// the B/C quads are); MODE 1: each lane its own 16 bytes, conflict-free; MODE
+// 2: 4-byte broadcast loads, for comparison.  Eight independent loads per
+// iteration, each folded into a running sum by one FADD.  Counts lane-loads.
+template <int MODE>
+__global__ void k_lds(float* out, int iters, ClockRec* rec) {
+  __shared__ __align__(16) float buf[4096];
+  for (int i = threadIdx.x; i < 4096; i += blockDim.x) buf[i] = 1e-3f * (i % 97);
+  const int lane = threadIdx.x & 31;
+  float acc[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) acc[j] = 0.f;
+  __syncthreads();
+  record_start(rec);
+  for (int i = 0; i < iters; ++i) {
+    const int base = (i * 256) & 4095;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (MODE == 2) {
+        acc[j] += buf[(base + 4 * j) & 4095];
+      } else {
+        const int idx = MODE == 0 ? ((base + 32 * j) & 4095) : ((base + 128 * j + 4 * lane) & 4095);
+        const float4 v = *reinterpret_cast<const float4*>(&buf[idx]);
+        acc[j] += v.x + v.w;
+      }
+    }
+  }
+  float s = 0.f;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) s += acc[j];
+  record_end(rec);
+  out[blockIdx.x * blockDim.x + threadIdx.x] = s;
+}
+
 }  // namespace
 
 // which: 0 = ex2, 1 = ffma, 2 = ffma2 (packed), 3 = update body scalar,
-//        4 = update body packed, 5 = pipe mix of one update (2 FFMA2 + 1 ex2).
+//        4 = update body packed, 5 = pipe mix of one update (2 FFMA2 + 1 ex2),
+//        6 / 7 / 8 = 16-byte broadcast / 16-byte distinct / 4-byte broadcast
+//        shared-memory loads (lane-loads).
 // result[0] = lane-ops (or state updates) per second over the whole GPU
 // result[1] = lane-ops (or updates) per clock per SM
 // result[2] = mean SM clock during the run, MHz
@@ -337,6 +374,9 @@ extern "C" __attribute__((visibility("default"))) int ss_peaks_measure(int which
       case 3: k_update<false><<<blocks, threads>>>(out, iters, rec); break;
       case 4: k_update<true><<<blocks, threads>>>(out, iters, rec); break;
       case 5: k_mix<<<blocks, threads>>>(out, iters, 0.999f, 1e-3f, rec); break;
+      case 6: k_lds<0><<<blocks, threads>>>(out, iters, rec); break;
+      case 7: k_lds<1><<<blocks, threads>>>(out, iters, rec); break;
+      case 8: k_lds<2><<<blocks, threads>>>(out, iters, rec); break;
       default: break;
     }
   };
@@ -365,6 +405,7 @@ extern "C" __attribute__((visibility("default"))) int ss_peaks_measure(int which
     case 2: per_thread = 2.0 * iters * kChains; break;
     case 3: per_thread = 16.0 * iters; break;
     case 4: per_thread = 128.0 * iters; break;  // iters vectors of 8 steps x 16 updates
+    case 6: case 7: case 8: per_thread = 8.0 * iters; break;
     default: break;
   }
   const double total = per_thread * blocks * threads;

@@ -2,7 +2,8 @@
 
 The roofline of the selective-scan forward kernel needs the per-SM rates of
 the MUFU ex2 unit and of the FP32 FMA pipe, which are measured here on the
-device at hand rather than taken from a data sheet.
+device at hand rather than taken from a data sheet, and the shared-memory load
+rates that bound how fast B and C reach the lanes.
 """
 from __future__ import annotations
 
@@ -18,10 +19,14 @@ PROBES = {
     "update_scalar": 3,   # selective-scan state updates, scalar FP32 body
     "update_packed": 4,   # selective-scan state updates, the scan kernel's f32x2 lane layout
     "update_mix": 5,      # pipe mix of one update (2 FFMA2 + 1 ex2), nothing else
+    "lds128_bcast": 6,    # 16-byte shared-memory loads, every lane the same address
+    "lds128_distinct": 7,  # 16-byte shared-memory loads, each lane its own address
+    "lds32_bcast": 8,     # 4-byte shared-memory loads, every lane the same address
 }
 
 DEFAULT_ITERS = {"ex2": 20000, "ffma": 40000, "ffma2": 20000,
-                 "update_scalar": 4000, "update_packed": 500, "update_mix": 20000}
+                 "update_scalar": 4000, "update_packed": 500, "update_mix": 20000,
+                 "lds128_bcast": 20000, "lds128_distinct": 20000, "lds32_bcast": 20000}
 
 
 def _lib():
@@ -56,7 +61,8 @@ def main() -> None:
     for the update probes (occupancy scaling of the update body)."""
     import json
 
-    runs = [("ex2", 4, 256), ("ffma", 4, 256), ("ffma2", 4, 256)]
+    runs = [("ex2", 4, 256), ("ffma", 4, 256), ("ffma2", 4, 256),
+            ("lds128_bcast", 4, 256), ("lds128_distinct", 4, 256), ("lds32_bcast", 4, 256)]
     for probe in ("update_mix", "update_packed", "update_scalar"):
         runs += [(probe, 2, 64), (probe, 4, 64), (probe, 4, 256)]
     for probe, bps, thr in runs:
