@@ -737,8 +737,8 @@ SS_API ss_status_t ss_selective_scan_fwd_pc(
   while ((1 << p.seg_shift) < quads) ++p.seg_shift;
   const int64_t blocks = ((p.rows << p.seg_shift) + 255) / 256;
   if (blocks > INT_MAX) return SS_ERR_UNSUPPORTED;
-  const bool vec = seqlen % (32 / elt) == 0 && aligned(u, 16) && aligned(delta, 16) &&
-                   aligned(B, 16) && aligned(C, 16) && aligned(y, 16) && (!z || aligned(z, 16));
+  const bool vec = seqlen % (32 / elt) == 0 && aligned(u, 32) && aligned(delta, 32) &&
+                   aligned(B, 32) && aligned(C, 32) && aligned(y, 16) && (!z || aligned(z, 32));
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   (void)cudaGetLastError();
   const unsigned g = (unsigned)blocks;
