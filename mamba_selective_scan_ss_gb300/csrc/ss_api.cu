@@ -438,6 +438,7 @@ ss_status_t fwd_impl(const void* u, const void* delta, const float* A, const voi
   }
   p.tiles = plan.tiles;
   p.chained = plan.chained ? 1 : 0;
+  p.y_pairs = (seqlen % (32 / elt) == 0 && aligned(y, 32)) ? 1 : 0;
 
   const cudaError_t err = dtype == SS_F32 ? dispatch<float>(p, plan, st)
                                           : dispatch<__nv_bfloat16>(p, plan, st);
@@ -1065,6 +1066,7 @@ extern "C" SS_API ss_status_t ss_selective_scan_fwd_noalloc(
   p.softplus = delta_softplus ? 1 : 0;
   p.tiles = plan.tiles;
   p.chained = plan.chained ? 1 : 0;
+  p.y_pairs = (seqlen % (32 / elt) == 0 && aligned(y, 32)) ? 1 : 0;
   char* base = static_cast<char*>(base_ptr);
   (void)cudaGetLastError();
   // the tickets and unit flags of the previous call must not be seen

@@ -67,6 +67,7 @@ struct FwdParams {
   float* unit_incl;   // [nchunks][tiles][rows_per_cta][NT] state at the unit's end
   int64_t tiles;      // row tiles: batch * dim_tiles
   int chained;        // 1: units wait for their predecessor; 0: decoupled look-back
+  int y_pairs;        // 1: y rows 32-byte aligned (seqlen a multiple of two vectors, y aligned)
 };
 
 // Row bookkeeping shared by the kernels: thread tid of the CTA owns channels
