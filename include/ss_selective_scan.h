@@ -269,7 +269,8 @@ SS_API ss_status_t ss_mamba2_fwd(
  * Arguments: those of ss_selective_scan_fwd, except
  *   B, C       [batch, dim, dstate, seqlen]   dtype   one row per channel
  *
- * Limits: dstate <= 128 (else SS_ERR_UNSUPPORTED); zero initial state.
+ * Limits: dstate <= 256 (else SS_ERR_UNSUPPORTED); zero initial state (see
+ * ss_selective_scan_fwd_pc_h0).
  * Behaviour: validated on the host (errors launch nothing and write
  * nothing); one kernel is enqueued on `stream`; no scratch, no device-side
  * wait, no synchronisation.  y and last_state must not overlap any input or
@@ -279,6 +280,26 @@ SS_API ss_status_t ss_selective_scan_fwd_pc(
     const void* u, const void* delta, const float* A, const void* B, const void* C,
     const float* D, const void* z, const float* delta_bias, int delta_softplus,
     void* y, float* last_state,
+    int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
+    ss_dtype_t dtype, void* stream);
+
+/*
+ * ss_selective_scan_fwd_pc_h0 -- ss_selective_scan_fwd_pc started from a given
+ * state: the per-channel layout run over a new segment of a sequence whose
+ * earlier part ended in state h0 (the sequential form of
+ * "从顺序到并行用PyTorch实现Blelloch算法加速Mamba状态空间模型" section 1).
+ *
+ * Arguments: those of ss_selective_scan_fwd_pc, plus
+ *   h0         [batch, dim, dstate]      float32    state before step 0, or NULL (zero)
+ *
+ * last_state may be h0 itself (the state updated in place); any other overlap
+ * of an output with an input is SS_ERR_INVALID_ARGUMENT.  Limits, validation
+ * and behaviour are those of ss_selective_scan_fwd_pc.
+ */
+SS_API ss_status_t ss_selective_scan_fwd_pc_h0(
+    const void* u, const void* delta, const float* A, const void* B, const void* C,
+    const float* D, const void* z, const float* delta_bias, int delta_softplus,
+    const float* h0, void* y, float* last_state,
     int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
     ss_dtype_t dtype, void* stream);
 

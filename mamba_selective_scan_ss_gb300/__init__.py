@@ -7,7 +7,8 @@ raise: there is no fallback implementation.
 
 Low-level names mirror the C ABI exactly (raw device pointers as ints):
     ss_selective_scan_fwd, ss_selective_scan_fwd_h0, ss_selective_state_update,
-    ss_selective_scan_bwd, ss_selective_scan_bwd_h0, ss_selective_scan_fwd_pc, ss_mamba2_fwd,
+    ss_selective_scan_bwd, ss_selective_scan_bwd_h0, ss_selective_scan_fwd_pc,
+    ss_selective_scan_fwd_pc_h0, ss_mamba2_fwd,
     ss_status_string, ss_selective_scan_check, ss_selective_scan_plan,
     ss_selective_scan_fwd_noalloc
 plus convenience wrappers for torch CUDA tensors:
@@ -31,7 +32,7 @@ __all__ = [
     "ss_selective_scan_fwd", "ss_status_string", "ss_selective_scan_check",
     "ss_selective_scan_plan", "ss_selective_scan_fwd_noalloc", "ss_selective_scan_fwd_h0",
     "ss_selective_state_update", "ss_selective_scan_bwd", "ss_selective_scan_bwd_h0",
-    "ss_selective_scan_fwd_pc",
+    "ss_selective_scan_fwd_pc", "ss_selective_scan_fwd_pc_h0",
     "ss_mamba2_fwd", "selective_scan_fwd", "test_hooks",
     "selective_state_update", "selective_scan_bwd", "mamba2_fwd",
 ]
@@ -78,6 +79,8 @@ def _declare(lib):
                                               ctypes.c_int, vp]
     lib.ss_selective_scan_fwd_pc.restype = ctypes.c_int
     lib.ss_selective_scan_fwd_pc.argtypes = list(lib.ss_selective_scan_fwd.argtypes)
+    lib.ss_selective_scan_fwd_pc_h0.restype = ctypes.c_int
+    lib.ss_selective_scan_fwd_pc_h0.argtypes = list(lib.ss_selective_scan_fwd_h0.argtypes)
     lib.ss_selective_scan_bwd.restype = ctypes.c_int
     lib.ss_selective_scan_bwd.argtypes = [vp] * 8 + [ctypes.c_int] + [vp] * 10 + \
         [i64, i64, i64, i64, ctypes.c_int, vp]
@@ -188,6 +191,14 @@ def ss_selective_scan_fwd_pc(u, delta, A, B, C, D, z, delta_bias, delta_softplus
         batch, dim, dstate, seqlen, int(dtype), stream)
 
 
+def ss_selective_scan_fwd_pc_h0(u, delta, A, B, C, D, z, delta_bias, delta_softplus, h0, y,
+                                last_state, batch, dim, dstate, seqlen, dtype, stream) -> int:
+    """The per-channel forward started from state h0 (fp32 [batch, dim, dstate])."""
+    return load_library().ss_selective_scan_fwd_pc_h0(
+        u, delta, A, B, C, D, z, delta_bias, int(delta_softplus), h0, y, last_state,
+        batch, dim, dstate, seqlen, int(dtype), stream)
+
+
 def ss_selective_scan_bwd(u, delta, A, B, C, D, z, delta_bias, delta_softplus, dy, dlast_state,
                           du, ddelta, dA, dB, dC, dD, dz, dbias, batch, dim, dstate, seqlen,
                           dtype, stream) -> int:
@@ -291,15 +302,16 @@ def selective_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None,
             batch, dim, dstate, seqlen, dt, s)
     per_channel = B.dim() == 4
     if per_channel:
-        if h0 is not None:
-            raise ValueError("per-channel B/C take no initial state")
-        status = ss_selective_scan_fwd_pc(*args, *outs)
+        if h0 is None:
+            status = ss_selective_scan_fwd_pc(*args, *outs)
+        else:
+            status = ss_selective_scan_fwd_pc_h0(*args, _ptr(h0), *outs)
     elif h0 is None:
         status = ss_selective_scan_fwd(*args, *outs)
     else:
         status = ss_selective_scan_fwd_h0(*args, _ptr(h0), *outs)
     if status != SS_OK:
-        what = "_pc" if per_channel else ("" if h0 is None else "_h0")
+        what = ("_pc" if per_channel else "") + ("" if h0 is None else "_h0")
         raise SelectiveScanError(status, "ss_selective_scan_fwd" + what)
     return (y, last_state) if return_last_state else y
 

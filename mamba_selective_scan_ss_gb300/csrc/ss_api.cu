@@ -315,6 +315,25 @@ cudaError_t dispatch(const ss::FwdParams& p, const LaunchPlan& plan, cudaStream_
   }
 }
 
+// The per-channel kernel for the given gate, vector-path and row-width choices.
+template <typename T>
+void pc_launch(const ss::PcParams& p, bool has_z, bool vec, unsigned grid, cudaStream_t st) {
+  const bool wide = p.seg_shift > 5;
+  auto go = [&](auto z, auto v, auto w) {
+    ss::ss_fwd_pc<T, decltype(z)::value, decltype(v)::value, decltype(w)::value>
+        <<<grid, 256, 0, st>>>(p);
+  };
+  using F = std::false_type;
+  using U = std::true_type;
+  if (wide) {
+    if (has_z) vec ? go(U{}, U{}, U{}) : go(U{}, F{}, U{});
+    else vec ? go(F{}, U{}, U{}) : go(F{}, F{}, U{});
+  } else {
+    if (has_z) vec ? go(U{}, U{}, F{}) : go(U{}, F{}, F{});
+    else vec ? go(F{}, U{}, F{}) : go(F{}, F{}, F{});
+  }
+}
+
 }  // namespace
 
 extern "C" {
@@ -702,11 +721,22 @@ SS_API ss_status_t ss_selective_scan_fwd_pc(
     void* y, float* last_state,
     int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
     ss_dtype_t dtype, void* stream) {
+  return ss_selective_scan_fwd_pc_h0(u, delta, A, B, C, D, z, delta_bias, delta_softplus,
+                                     nullptr, y, last_state, batch, dim, dstate, seqlen, dtype,
+                                     stream);
+}
+
+SS_API ss_status_t ss_selective_scan_fwd_pc_h0(
+    const void* u, const void* delta, const float* A, const void* B, const void* C,
+    const float* D, const void* z, const float* delta_bias, int delta_softplus,
+    const float* h0, void* y, float* last_state,
+    int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
+    ss_dtype_t dtype, void* stream) {
   // ---- validation: nothing is enqueued or written on error ----
   if (dtype != SS_F32 && dtype != SS_BF16) return SS_ERR_UNSUPPORTED;
   if (!u || !delta || !A || !B || !C || !y) return SS_ERR_INVALID_ARGUMENT;
   if (batch <= 0 || dim <= 0 || dstate <= 0 || seqlen <= 0) return SS_ERR_INVALID_ARGUMENT;
-  if (dstate > 128) return SS_ERR_UNSUPPORTED;
+  if (dstate > 256) return SS_ERR_UNSUPPORTED;
   const int64_t elt = dtype == SS_F32 ? 4 : 2;
   Sizes sz;
   int64_t bc_bytes;
@@ -715,14 +745,19 @@ SS_API ss_status_t ss_selective_scan_fwd_pc(
   const uintptr_t ea = (uintptr_t)elt;
   if (!aligned(u, ea) || !aligned(delta, ea) || !aligned(B, ea) || !aligned(C, ea) ||
       !aligned(y, ea) || (z && !aligned(z, ea)) || !aligned(A, 4) || (D && !aligned(D, 4)) ||
-      (delta_bias && !aligned(delta_bias, 4)) || (last_state && !aligned(last_state, 4)))
+      (delta_bias && !aligned(delta_bias, 4)) || (last_state && !aligned(last_state, 4)) ||
+      (h0 && !aligned(h0, 4)))
     return SS_ERR_INVALID_ARGUMENT;
-  const void* ins[] = {u, delta, B, C, z, A, D, delta_bias};
+  const void* ins[] = {u, delta, B, C, z, A, D, delta_bias, h0};
   const int64_t in_bytes[] = {sz.x_bytes, sz.x_bytes, bc_bytes, bc_bytes, z ? sz.x_bytes : 0,
-                              sz.a_elems * 4, D ? dim * 4 : 0, delta_bias ? dim * 4 : 0};
-  for (int i = 0; i < 8; ++i) {
+                              sz.a_elems * 4, D ? dim * 4 : 0, delta_bias ? dim * 4 : 0,
+                              h0 ? sz.st_elems * 4 : 0};
+  for (int i = 0; i < 9; ++i) {
     if (range_overlap(y, sz.x_bytes, ins[i], in_bytes[i])) return SS_ERR_INVALID_ARGUMENT;
-    if (last_state && range_overlap(last_state, sz.st_elems * 4, ins[i], in_bytes[i]))
+    // last_state may be h0 itself: each lane reads its states of h0 before it
+    // writes them back
+    if (last_state && !(i == 8 && last_state == h0) &&
+        range_overlap(last_state, sz.st_elems * 4, ins[i], in_bytes[i]))
       return SS_ERR_INVALID_ARGUMENT;
   }
   if (last_state && range_overlap(last_state, sz.st_elems * 4, y, sz.x_bytes))
@@ -731,7 +766,7 @@ SS_API ss_status_t ss_selective_scan_fwd_pc(
   ss::PcParams p{};
   p.u = u; p.delta = delta; p.A = A; p.B = B; p.C = C; p.D = D; p.z = z; p.bias = delta_bias;
   p.softplus = delta_softplus ? 1 : 0;
-  p.y = y; p.last_state = last_state;
+  p.y = y; p.last_state = last_state; p.h0 = h0;
   p.rows = batch * dim; p.dim = dim; p.dstate = dstate; p.seqlen = seqlen;
   const int quads = (int)((dstate + 3) / 4);
   p.seg_shift = 0;
@@ -743,23 +778,8 @@ SS_API ss_status_t ss_selective_scan_fwd_pc(
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   (void)cudaGetLastError();
   const unsigned g = (unsigned)blocks;
-  if (dtype == SS_F32) {
-    if (z) {
-      if (vec) ss::ss_fwd_pc<float, true, true><<<g, 256, 0, st>>>(p);
-      else ss::ss_fwd_pc<float, true, false><<<g, 256, 0, st>>>(p);
-    } else {
-      if (vec) ss::ss_fwd_pc<float, false, true><<<g, 256, 0, st>>>(p);
-      else ss::ss_fwd_pc<float, false, false><<<g, 256, 0, st>>>(p);
-    }
-  } else {
-    if (z) {
-      if (vec) ss::ss_fwd_pc<__nv_bfloat16, true, true><<<g, 256, 0, st>>>(p);
-      else ss::ss_fwd_pc<__nv_bfloat16, true, false><<<g, 256, 0, st>>>(p);
-    } else {
-      if (vec) ss::ss_fwd_pc<__nv_bfloat16, false, true><<<g, 256, 0, st>>>(p);
-      else ss::ss_fwd_pc<__nv_bfloat16, false, false><<<g, 256, 0, st>>>(p);
-    }
-  }
+  if (dtype == SS_F32) pc_launch<float>(p, z != nullptr, vec, g, st);
+  else pc_launch<__nv_bfloat16>(p, z != nullptr, vec, g, st);
   return cudaGetLastError() == cudaSuccess ? SS_OK : SS_ERR_CUDA;
 }
 

@@ -12,6 +12,10 @@
 // two, dstate <= 4*S <= 128) serves one row; lane j holds states [4j, 4j+4)
 // and streams their B and C rows 32 bytes (8 fp32 or 16 bf16 steps) at a
 // time, a whole DRAM sector per row, with the next 32 bytes' loads in flight.
+// Above 128 states a row takes 64 lanes (two warps of the CTA): each warp
+// sums its read-out by shuffles and the second warp hands its sums for the
+// iteration's steps to the first through shared memory (double-buffered, one
+// CTA barrier per iteration).
 // One CTA per SM: with 64 rows per SM the partly read L2 lines of all row
 // streams (about 44 MB over the GPU) stay in L2 until they are used up, so
 // DRAM delivers each byte once.  dt, du and
@@ -36,6 +40,7 @@ struct PcParams {
   int softplus;
   void* y;
   float* last_state;
+  const float* h0;       // [b,d,N] state before step 0, or null (zero)
   int64_t rows, dim, dstate, seqlen;
   int seg_shift;         // log2 of the lanes per row
 };
@@ -97,10 +102,12 @@ struct PcStep {
 };
 
 // grid = ceil(rows * 2^seg_shift / 256), block = 256.  VEC: seqlen a multiple
-// of kPcSteps and every input row 32-byte aligned (y 16-byte aligned).
-template <typename T, bool HAS_Z, bool VEC>
+// of kPcSteps and every input row 32-byte aligned (y 16-byte aligned).  WIDE:
+// 64 lanes per row (seg_shift 6, dstate up to 256).
+template <typename T, bool HAS_Z, bool VEC, bool WIDE>
 __global__ void __launch_bounds__(256, 1) ss_fwd_pc(const PcParams p) {
   constexpr int V = kPcSteps<T>;
+  __shared__ float s_half[WIDE ? 2 : 1][WIDE ? 4 : 1][V];  // [buffer][row of the CTA][step]
   const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const int64_t row = gid >> p.seg_shift;
   const int lane = (int)(gid & ((1 << p.seg_shift) - 1));
@@ -124,7 +131,7 @@ __global__ void __launch_bounds__(256, 1) ss_fwd_pc(const PcParams p) {
     Bq[e] = static_cast<const T*>(p.B) + (rc * N + n) * L;
     Cq[e] = static_cast<const T*>(p.C) + (rc * N + n) * L;
     A2[e] = has[e] ? p.A[d * N + n] * kLog2e : 0.f;
-    h[e] = 0.f;
+    h[e] = (has[e] && p.h0) ? p.h0[rc * N + n] : 0.f;
   }
   const float bias = p.bias ? p.bias[d] : 0.f;
   const float Dd = p.D ? p.D[d] : 0.f;
@@ -143,21 +150,21 @@ __global__ void __launch_bounds__(256, 1) ss_fwd_pc(const PcParams p) {
   // used; the element-wise path (a correctness path) loads at each iteration
   PcStep<T, VEC, HAS_Z> cur, nxt;
   if (VEC) load(0, cur);
+  const int warp_lanes = WIDE ? 32 : (1 << p.seg_shift);
   for (int64_t t0 = 0; t0 < L; t0 += V) {
     if (VEC) {
       if (t0 + V < L) load(t0 + V, nxt);
     } else {
       load(t0, cur);
     }
-    float yv[V];
+    float yv[V];  // the read-out of each step, summed over the warp's lanes of the row
 #pragma unroll
     for (int s = 0; s < V; ++s) {
       yv[s] = 0.f;
       if (!VEC && t0 + s >= L) continue;  // padding past the row's end (warp-uniform)
       const float x = cur.x.at(s) + bias;
       const float dtv = p.softplus ? lo_of(softplus2(splat(x))) : x;
-      const float uv = cur.u.at(s);
-      const float du = dtv * uv;
+      const float du = dtv * cur.u.at(s);
       float part = 0.f;
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
@@ -165,11 +172,30 @@ __global__ void __launch_bounds__(256, 1) ss_fwd_pc(const PcParams p) {
         h[e] = fmaf(a, h[e], du * (has[e] ? cur.b[e].at(s) : 0.f));
         part = fmaf(has[e] ? cur.c[e].at(s) : 0.f, h[e], part);
       }
-      for (int off = (1 << p.seg_shift) >> 1; off > 0; off >>= 1)
+      for (int off = warp_lanes >> 1; off > 0; off >>= 1)
         part += __shfl_xor_sync(0xffffffffu, part, off);
-      float y = fmaf(Dd, uv, part);
-      if (HAS_Z) y *= silu(cur.z.at(s));
-      yv[s] = y;
+      yv[s] = part;
+    }
+    if constexpr (WIDE) {
+      // the second warp of each row hands its sums to the first
+      const int buf = (int)((t0 / V) & 1), crow = (int)(threadIdx.x >> 6);
+      if (lane == 32) {
+#pragma unroll
+        for (int s = 0; s < V; ++s) s_half[buf][crow][s] = yv[s];
+      }
+      __syncthreads();
+      if (lane == 0) {
+#pragma unroll
+        for (int s = 0; s < V; ++s) yv[s] += s_half[buf][crow][s];
+      }
+    }
+    if (lane == 0) {
+#pragma unroll
+      for (int s = 0; s < V; ++s) {
+        float y = fmaf(Dd, cur.u.at(s), yv[s]);
+        if (HAS_Z) y *= silu(cur.z.at(s));
+        yv[s] = y;
+      }
     }
     if (active && lane == 0) {
       T* yo = static_cast<T*>(p.y) + rc * L + t0;

@@ -71,9 +71,72 @@ def test_per_channel_forward(orc, dtype, shape):
     check(orc, W(*shape, dtype=dtype))
 
 
-@pytest.mark.parametrize("dstate", [1, 3, 4, 5, 8, 12, 17, 32, 64, 100, 128])
+@pytest.mark.parametrize("dstate", [1, 3, 4, 5, 8, 12, 17, 32, 64, 100, 128,
+                                    129, 160, 200, 256])
 def test_per_channel_dstate(orc, dstate):
+    """Up to 128 states a row's lanes sit in one warp; above, a row takes two
+    warps whose read-outs meet in shared memory."""
     check(orc, W(2, 9, dstate, 40, seed=82))
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("dstate", [16, 200])
+def test_per_channel_vector_path_wide_rows(orc, dtype, dstate):
+    """Vector path (seqlen a multiple of 32 bytes of steps) with 64-lane rows
+    and a ragged last CTA (3 * 7 rows)."""
+    check(orc, W(3, 7, dstate, 96, dtype=dtype, seed=86))
+
+
+def check_h0(orc, w, in_place=False):
+    inp = make_inputs(w)
+    g = torch.Generator().manual_seed(w.seed + 1)
+    h0 = torch.randn((w.batch, w.dim, w.dstate), generator=g, dtype=torch.float32)
+    d = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    h0_d = h0.cuda()
+    last_buf = h0_d if in_place else None
+    y, last = ss.selective_scan_fwd(d["u"], d["delta"], d["A"], d["B"], d["C"], d["D"], d["z"],
+                                    d["delta_bias"], d["delta_softplus"], h0=h0_d,
+                                    last_state=last_buf)
+    torch.cuda.synchronize()
+    y_ref, last_ref = orc.fwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"],
+                              inp["z"], inp["delta_bias"], inp["delta_softplus"],
+                              h0=h0.numpy(), dtype=w.dtype, bc_per_channel=True)
+    close(y, y_ref, w.dtype, "y")
+    close(last, last_ref, w.dtype, "last_state")
+    if in_place:
+        assert last.data_ptr() == h0_d.data_ptr()
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("shape", [(2, 33, 16, 64), (1, 5, 7, 37), (2, 6, 200, 48)])
+def test_per_channel_from_initial_state(orc, dtype, shape):
+    check_h0(orc, W(*shape, dtype=dtype, seed=87))
+
+
+def test_per_channel_state_updated_in_place(orc):
+    check_h0(orc, W(2, 10, 16, 32, seed=88), in_place=True)
+
+
+def test_per_channel_chained_calls_equal_one_call():
+    """Two calls, the second from the first's last state, give the result of
+    one call over the whole sequence."""
+    w = W(2, 12, 16, 128, seed=89)
+    inp = make_inputs(w)
+    d = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    args = lambda sl, ks: [d[k][..., sl].contiguous() if d[k] is not None else None for k in ks]
+    y_all, s_all = ss.selective_scan_fwd(d["u"], d["delta"], d["A"], d["B"], d["C"], d["D"],
+                                         d["z"], d["delta_bias"], True)
+    half = slice(0, 64), slice(64, 128)
+    ys, state = [], None
+    for sl in half:
+        u, dl, B, C, z = args(sl, ("u", "delta", "B", "C", "z"))
+        y, state = ss.selective_scan_fwd(u, dl, d["A"], B, C, d["D"], z, d["delta_bias"], True,
+                                         h0=state)
+        ys.append(y)
+    torch.cuda.synchronize()
+    atol, rtol = TOL["f32"]
+    assert torch.allclose(torch.cat(ys, -1), y_all, atol=atol, rtol=rtol)
+    assert torch.allclose(state, s_all, atol=atol, rtol=rtol)
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
@@ -123,8 +186,8 @@ def test_per_channel_full_size_sampled_rows(orc):
         close(last[b:b + 1, rows], last_ref, w.dtype, f"last_state rows {b},{c0}")
 
 
-def test_per_channel_rejects_more_than_128_states():
-    w = W(1, 2, 129, 8, seed=85)
+def test_per_channel_rejects_more_than_256_states():
+    w = W(1, 2, 257, 8, seed=85)
     inp = make_inputs(w)
     d = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
     with pytest.raises(ss.SelectiveScanError):
