@@ -106,6 +106,9 @@ class Oracle:
         lib.ss_oracle_ssd.restype = ctypes.c_int
         lib.ss_oracle_ssd.argtypes = [ctypes.c_void_p] * 7 + [ctypes.c_int] + \
             [ctypes.c_void_p] * 2 + [ctypes.c_int64] * 6 + [ctypes.c_int, ctypes.c_int]
+        lib.ss_oracle_ssd_h0.restype = ctypes.c_int
+        lib.ss_oracle_ssd_h0.argtypes = [ctypes.c_void_p] * 7 + [ctypes.c_int] + \
+            [ctypes.c_void_p] * 3 + [ctypes.c_int64] * 6 + [ctypes.c_int, ctypes.c_int]
         lib.ss_oracle_combine.restype = None
         lib.ss_oracle_combine.argtypes = [ctypes.c_void_p] * 6 + [ctypes.c_int64]
         self.lib = lib
@@ -188,10 +191,11 @@ class Oracle:
         return out
 
     def ssd(self, x, dt, A, B, C, D=None, dt_bias=None, dt_softplus=True,
-            dtype: str = "f32", nthreads: int | None = None):
+            dtype: str = "f32", nthreads: int | None = None, initial_state=None):
         """Sequential fp64 Mamba-2 forward; returns (y [b,L,H,P], final_state [b,H,P,N]).
 
-        x [b,L,H,P], dt [b,L,H], A [H], B and C [b,L,G,N], D and dt_bias [H]."""
+        x [b,L,H,P], dt [b,L,H], A [H], B and C [b,L,G,N], D and dt_bias [H];
+        initial_state [b,H,P,N] is the state before step 0 (default zero)."""
         x_, dt_, B_, C_ = (_as_input(t, dtype) for t in (x, dt, B, C))
         A_, D_, bias_ = (_as_input(t, "f32") for t in (A, D, dt_bias))
         batch, seqlen, nheads, headdim = x_.shape
@@ -202,12 +206,17 @@ class Oracle:
                                  ("D", D_, (nheads,)), ("dt_bias", bias_, (nheads,))):
             if arr is not None and tuple(arr.shape) != shape:
                 raise ValueError(f"{name} has shape {arr.shape}, expected {shape}")
+        h0 = None
+        if initial_state is not None:
+            h0 = np.ascontiguousarray(initial_state, dtype=np.float64)
+            if h0.shape != (batch, nheads, headdim, dstate):
+                raise ValueError("initial_state has the wrong shape")
         y = np.empty((batch, seqlen, nheads, headdim), dtype=np.float64)
         final = np.empty((batch, nheads, headdim, dstate), dtype=np.float64)
         nt = nthreads if nthreads is not None else (os.cpu_count() or 1)
-        rc = self.lib.ss_oracle_ssd(
+        rc = self.lib.ss_oracle_ssd_h0(
             _ptr(x_), _ptr(dt_), _ptr(A_), _ptr(B_), _ptr(C_), _ptr(D_), _ptr(bias_),
-            int(bool(dt_softplus)), _ptr(y), _ptr(final),
+            int(bool(dt_softplus)), _ptr(h0), _ptr(y), _ptr(final),
             batch, seqlen, nheads, headdim, ngroups, dstate, DTYPES[dtype], nt)
         if rc != 0:
             raise RuntimeError(f"ss_oracle_ssd failed with status {rc}")

@@ -437,7 +437,7 @@ done:
  *   y_t[p] = sum_n C_t[n] * h_t[p,n] + D * x_t[p]
  *
  * dt_t = softplus(dt[b,t,h] + dt_bias[h]) when dt_softplus is set, else
- * dt + bias.  The state starts at zero.  Layouts: x, y [b,L,H,P]; dt [b,L,H];
+ * dt + bias.  The state starts at zero (or at h0, ss_oracle_ssd_h0).  Layouts: x, y [b,L,H,P]; dt [b,L,H];
  * B, C [b,L,G,N] (head h reads group h / (H/G)); A, D, dt_bias [H];
  * final_state [b,H,P,N].  Units (b, h) are independent and are split over
  * the threads.
@@ -451,6 +451,7 @@ typedef struct {
   const float* D;
   const float* bias;
   int softplus;
+  const double* h0;
   double* y;
   double* final_state;
   int64_t batch, seqlen, nheads, headdim, ngroups, dstate;
@@ -469,7 +470,7 @@ static void ssd_units(oracle_ssd_job* j) {
   for (int64_t unit = j->unit_begin; unit < j->unit_end; ++unit) {
     const int64_t b = unit / H, hd = unit % H;
     const int64_t g = hd / (H / G);  /* the head's group */
-    for (int64_t i = 0; i < P * N; ++i) h[i] = 0.0;
+    for (int64_t i = 0; i < P * N; ++i) h[i] = j->h0 ? j->h0[unit * P * N + i] : 0.0;
     const double A = (double)j->A[hd];
     const double bias = j->bias ? (double)j->bias[hd] : 0.0;
     const double Dh = j->D ? (double)j->D[hd] : 0.0;
@@ -504,10 +505,27 @@ static void* ssd_thread_main(void* arg) {
  * <= 0, nheads not a multiple of ngroups, an unknown dtype), 2 on an
  * allocation failure.  y is [b,L,H,P] doubles; final_state [b,H,P,N] doubles
  * or NULL; D and dt_bias may be NULL (no skip, zero bias). */
+int ss_oracle_ssd_h0(const void* x, const void* dt, const float* A, const void* B,
+                     const void* C, const float* D, const float* dt_bias, int dt_softplus,
+                     const double* h0, double* y, double* final_state, int64_t batch,
+                     int64_t seqlen, int64_t nheads, int64_t headdim, int64_t ngroups,
+                     int64_t dstate, int dtype, int nthreads);
+
 int ss_oracle_ssd(const void* x, const void* dt, const float* A, const void* B, const void* C,
                   const float* D, const float* dt_bias, int dt_softplus, double* y,
                   double* final_state, int64_t batch, int64_t seqlen, int64_t nheads,
                   int64_t headdim, int64_t ngroups, int64_t dstate, int dtype, int nthreads) {
+  return ss_oracle_ssd_h0(x, dt, A, B, C, D, dt_bias, dt_softplus, NULL, y, final_state, batch,
+                          seqlen, nheads, headdim, ngroups, dstate, dtype, nthreads);
+}
+
+/* The same from a given state h0 [b,H,P,N] (doubles; NULL: zero): the state
+ * before the first step, as for a sequence that continues an earlier one. */
+int ss_oracle_ssd_h0(const void* x, const void* dt, const float* A, const void* B,
+                     const void* C, const float* D, const float* dt_bias, int dt_softplus,
+                     const double* h0, double* y, double* final_state, int64_t batch,
+                     int64_t seqlen, int64_t nheads, int64_t headdim, int64_t ngroups,
+                     int64_t dstate, int dtype, int nthreads) {
   if (!x || !dt || !A || !B || !C || !y) return 1;
   if (batch <= 0 || seqlen <= 0 || nheads <= 0 || headdim <= 0 || ngroups <= 0 || dstate <= 0)
     return 1;
@@ -528,7 +546,7 @@ int ss_oracle_ssd(const void* x, const void* dt, const float* A, const void* B, 
   for (int i = 0; i < nthreads; ++i) {
     oracle_ssd_job* j = &jobs[i];
     j->x = x; j->dt = dt; j->A = A; j->B = B; j->C = C; j->D = D; j->bias = dt_bias;
-    j->softplus = dt_softplus; j->y = y; j->final_state = final_state;
+    j->softplus = dt_softplus; j->h0 = h0; j->y = y; j->final_state = final_state;
     j->batch = batch; j->seqlen = seqlen; j->nheads = nheads; j->headdim = headdim;
     j->ngroups = ngroups; j->dstate = dstate; j->dtype = dtype;
     j->unit_begin = units * i / nthreads;

@@ -554,6 +554,34 @@ def pin_ssd_jump_formula(orc, seed=26):
            what="ssd state after both chunks")
 
 
+# A given state h0 before step 0 is the state a preceding segment of the
+# sequence left: the second part run from the first part's final state equals
+# the tail of one run over the whole sequence.  With x = 0 nothing enters the
+# state, which only decays: h_t = exp(cum_t) h0 and y_t = C_t . h_t (closed form).
+def pin_ssd_initial_state(orc, seed=28):
+    rng = np.random.default_rng(seed)
+    b, L, H, P, G, N, L1 = 2, 11, 4, 2, 2, 3, 4
+    p = _ssd_problem(rng, b, L, H, P, G, N)
+    y_all, f_all = orc.ssd(**p)
+    part = lambda sl: {k: (np.ascontiguousarray(v[:, sl]) if k in ("x", "dt", "B", "C") else v)
+                       for k, v in p.items()}
+    _, f1 = orc.ssd(**part(slice(0, L1)))
+    y2, f2 = orc.ssd(**part(slice(L1, L)), initial_state=f1)
+    _close(y2, y_all[:, L1:], rtol=1e-12, atol=1e-13, what="ssd continued from a state: y")
+    _close(f2, f_all, rtol=1e-12, atol=1e-13, what="ssd continued from a state: final state")
+
+    q = dict(p, x=np.zeros_like(p["x"]))
+    h0 = rng.standard_normal((b, H, P, N))
+    y0, f0 = orc.ssd(**q, initial_state=h0)
+    cum = np.cumsum(_ssd_dt(q, True) * q["A"].astype(np.float64)[None, None, :], axis=1)
+    grp = np.arange(H) // (H // G)
+    Ch = q["C"].astype(np.float64)[:, :, grp, :]                     # [b,L,H,N]
+    y_cf = np.einsum("bthn,bth,bhpn->bthp", Ch, np.exp(cum), h0)
+    _close(y0, y_cf, rtol=1e-12, atol=1e-13, what="ssd decay of h0 alone: y")
+    _close(f0, np.exp(cum[:, -1])[:, :, None, None] * h0, rtol=1e-12, atol=1e-13,
+           what="ssd decay of h0 alone: final state")
+
+
 ALL_PINS = [
     pin_unrolled_sum,
     pin_zero_A_is_cumsum,
@@ -572,4 +600,5 @@ ALL_PINS = [
     pin_ssd_quadratic_form,
     pin_ssd_is_mamba1_with_scalar_decay,
     pin_ssd_jump_formula,
+    pin_ssd_initial_state,
 ]

@@ -79,6 +79,9 @@ MUTANTS = {
                          "const int64_t xrow = ((b * H + hd) * L + t) * P;"),
     "ssd_state_transposed": ("j->final_state[unit * P * N + i] = h[i];",
                              "j->final_state[unit * P * N + (i % N) * P + i / N] = h[i];"),
+    "ssd_h0_ignored": ("h[i] = j->h0 ? j->h0[unit * P * N + i] : 0.0;", "h[i] = 0.0;"),
+    "ssd_h0_transposed": ("h[i] = j->h0 ? j->h0[unit * P * N + i] : 0.0;",
+                          "h[i] = j->h0 ? j->h0[unit * P * N + (i % N) * P + i / N] : 0.0;"),
 }
 
 
