@@ -252,13 +252,36 @@ SS_API ss_status_t ss_selective_scan_bwd_h0(
  * nothing); one kernel is enqueued on `stream`, one CTA per (batch, head);
  * no scratch, no synchronisation; its waits on the tensor cores are bounded
  * (SS_ERR_TIMEOUT from ss_selective_scan_check).  y and final_state must not
- * overlap any input or each other.
+ * overlap any input or each other.  The state starts at zero (see
+ * ss_mamba2_fwd_h0).
  */
 SS_API ss_status_t ss_mamba2_fwd(
     const void* x, const void* dt, const float* A, const void* B, const void* C,
     const float* D, const float* dt_bias, int dt_softplus, void* y, float* final_state,
     int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim, int64_t ngroups,
     int64_t dstate, ss_dtype_t dtype, void* stream);
+
+/*
+ * ss_mamba2_fwd_h0 -- ss_mamba2_fwd started from a given state: the same
+ * recurrence run over a segment of a sequence whose earlier part left the
+ * state initial_state (h_{-1}), as for the sequential form of
+ * "从顺序到并行用PyTorch实现Blelloch算法加速Mamba状态空间模型" section 1.  The
+ * given state enters chunk 0 the way a chunk's incoming state enters every
+ * later chunk (the page's jump formula): y_t gains C_t exp(cum_t) h_{-1}, the
+ * state carries exp(cum_end) h_{-1} forward; its bf16 copy feeds the tensor
+ * cores like every carried state.
+ *
+ * Arguments: those of ss_mamba2_fwd, plus
+ *   initial_state [batch, nheads, headdim, dstate]  float32  or NULL (zero)
+ * final_state may be initial_state itself (the state updated in place); any
+ * other overlap of an output with an input is SS_ERR_INVALID_ARGUMENT.
+ * Limits, validation and behaviour are those of ss_mamba2_fwd.
+ */
+SS_API ss_status_t ss_mamba2_fwd_h0(
+    const void* x, const void* dt, const float* A, const void* B, const void* C,
+    const float* D, const float* dt_bias, int dt_softplus, const float* initial_state, void* y,
+    float* final_state, int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim,
+    int64_t ngroups, int64_t dstate, ss_dtype_t dtype, void* stream);
 
 /*
  * ss_selective_scan_fwd_pc -- the forward with B and C given per channel:

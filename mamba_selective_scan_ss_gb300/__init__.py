@@ -8,7 +8,7 @@ raise: there is no fallback implementation.
 Low-level names mirror the C ABI exactly (raw device pointers as ints):
     ss_selective_scan_fwd, ss_selective_scan_fwd_h0, ss_selective_state_update,
     ss_selective_scan_bwd, ss_selective_scan_bwd_h0, ss_selective_scan_fwd_pc,
-    ss_selective_scan_fwd_pc_h0, ss_mamba2_fwd,
+    ss_selective_scan_fwd_pc_h0, ss_mamba2_fwd, ss_mamba2_fwd_h0,
     ss_status_string, ss_selective_scan_check, ss_selective_scan_plan,
     ss_selective_scan_fwd_noalloc
 plus convenience wrappers for torch CUDA tensors:
@@ -33,7 +33,7 @@ __all__ = [
     "ss_selective_scan_plan", "ss_selective_scan_fwd_noalloc", "ss_selective_scan_fwd_h0",
     "ss_selective_state_update", "ss_selective_scan_bwd", "ss_selective_scan_bwd_h0",
     "ss_selective_scan_fwd_pc", "ss_selective_scan_fwd_pc_h0",
-    "ss_mamba2_fwd", "selective_scan_fwd", "test_hooks",
+    "ss_mamba2_fwd", "ss_mamba2_fwd_h0", "selective_scan_fwd", "test_hooks",
     "selective_state_update", "selective_scan_bwd", "mamba2_fwd",
 ]
 
@@ -89,6 +89,9 @@ def _declare(lib):
         [i64, i64, i64, i64, ctypes.c_int, vp]
     lib.ss_mamba2_fwd.restype = ctypes.c_int
     lib.ss_mamba2_fwd.argtypes = [vp] * 7 + [ctypes.c_int, vp, vp] + [i64] * 6 + \
+        [ctypes.c_int, vp]
+    lib.ss_mamba2_fwd_h0.restype = ctypes.c_int
+    lib.ss_mamba2_fwd_h0.argtypes = [vp] * 7 + [ctypes.c_int, vp, vp, vp] + [i64] * 6 + \
         [ctypes.c_int, vp]
     lib.ss_selective_scan_plan.restype = ctypes.c_int
     lib.ss_selective_scan_plan.argtypes = [i64, i64, i64, i64, ctypes.c_int, ctypes.c_int,
@@ -223,6 +226,13 @@ def ss_mamba2_fwd(x, dt, A, B, C, D, dt_bias, dt_softplus, y, final_state, batch
     return load_library().ss_mamba2_fwd(
         x, dt, A, B, C, D, dt_bias, int(dt_softplus), y, final_state, batch, seqlen, nheads,
         headdim, ngroups, dstate, int(dtype), stream)
+
+def ss_mamba2_fwd_h0(x, dt, A, B, C, D, dt_bias, dt_softplus, initial_state, y, final_state,
+                     batch, seqlen, nheads, headdim, ngroups, dstate, dtype, stream) -> int:
+    """The Mamba-2 forward from a given state (fp32 [batch, nheads, headdim, dstate])."""
+    return load_library().ss_mamba2_fwd_h0(
+        x, dt, A, B, C, D, dt_bias, int(dt_softplus), initial_state, y, final_state, batch,
+        seqlen, nheads, headdim, ngroups, dstate, int(dtype), stream)
 
 
 def ss_status_string(status: int) -> str:
@@ -382,19 +392,21 @@ def selective_scan_bwd(u, delta, A, B, C, D=None, z=None, delta_bias=None,
 
 
 def mamba2_fwd(x, dt, A, B, C, D=None, dt_bias=None, dt_softplus: bool = True,
-               return_final_state: bool = True, y=None, final_state=None, stream=None):
+               return_final_state: bool = True, y=None, final_state=None, stream=None,
+               initial_state=None):
     """The Mamba-2 forward on torch CUDA tensors (ss_mamba2_fwd).
 
     x: [batch, seqlen, nheads, headdim] bf16; dt: [batch, seqlen, nheads] bf16;
     A, D, dt_bias: [nheads] fp32; B, C: [batch, seqlen, ngroups, dstate] bf16.
     Returns y (like x), or (y, final_state) with final_state [batch, nheads,
-    headdim, dstate] fp32.
+    headdim, dstate] fp32.  initial_state (fp32, like final_state) is the state
+    before step 0 (default zero, ss_mamba2_fwd_h0); final_state may be it.
     """
     import torch
 
     io = _io_dtype(x)
     _check_tensors(x, (("x", x), ("dt", dt), ("B", B), ("C", C)),
-                   (("A", A), ("D", D), ("dt_bias", dt_bias)))
+                   (("A", A), ("D", D), ("dt_bias", dt_bias), ("initial_state", initial_state)))
     batch, seqlen, nheads, headdim = x.shape
     ngroups, dstate = B.shape[2], B.shape[3]
     if y is None:
@@ -402,11 +414,11 @@ def mamba2_fwd(x, dt, A, B, C, D=None, dt_bias=None, dt_softplus: bool = True,
     if final_state is None and return_final_state:
         final_state = torch.empty((batch, nheads, headdim, dstate), device=x.device,
                                   dtype=torch.float32)
-    status = ss_mamba2_fwd(_ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(dt_bias),
-                           dt_softplus, _ptr(y),
-                           _ptr(final_state) if return_final_state else None,
-                           batch, seqlen, nheads, headdim, ngroups, dstate, io,
-                           _stream(stream, x.device))
+    status = ss_mamba2_fwd_h0(_ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
+                              _ptr(dt_bias), dt_softplus, _ptr(initial_state), _ptr(y),
+                              _ptr(final_state) if return_final_state else None,
+                              batch, seqlen, nheads, headdim, ngroups, dstate, io,
+                              _stream(stream, x.device))
     if status != SS_OK:
-        raise SelectiveScanError(status, "ss_mamba2_fwd")
+        raise SelectiveScanError(status, "ss_mamba2_fwd_h0")
     return (y, final_state) if return_final_state else y

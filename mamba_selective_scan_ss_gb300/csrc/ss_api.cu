@@ -788,6 +788,15 @@ SS_API ss_status_t ss_mamba2_fwd(
     const float* D, const float* dt_bias, int dt_softplus, void* y, float* final_state,
     int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim, int64_t ngroups,
     int64_t dstate, ss_dtype_t dtype, void* stream) {
+  return ss_mamba2_fwd_h0(x, dt, A, B, C, D, dt_bias, dt_softplus, nullptr, y, final_state,
+                          batch, seqlen, nheads, headdim, ngroups, dstate, dtype, stream);
+}
+
+SS_API ss_status_t ss_mamba2_fwd_h0(
+    const void* x, const void* dt, const float* A, const void* B, const void* C,
+    const float* D, const float* dt_bias, int dt_softplus, const float* initial_state, void* y,
+    float* final_state, int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim,
+    int64_t ngroups, int64_t dstate, ss_dtype_t dtype, void* stream) {
   // ---- validation: nothing is enqueued or written on error ----
   if (dtype != SS_F32 && dtype != SS_BF16) return SS_ERR_UNSUPPORTED;
   if (!x || !dt || !A || !B || !C || !y) return SS_ERR_INVALID_ARGUMENT;
@@ -805,14 +814,19 @@ SS_API ss_status_t ss_mamba2_fwd(
   if (units > INT_MAX) return SS_ERR_UNSUPPORTED;
   if (!aligned(x, 16) || !aligned(B, 16) || !aligned(C, 16) || !aligned(y, 16) ||
       !aligned(dt, 2) || !aligned(A, 4) || (D && !aligned(D, 4)) ||
-      (dt_bias && !aligned(dt_bias, 4)) || (final_state && !aligned(final_state, 4)))
+      (dt_bias && !aligned(dt_bias, 4)) || (final_state && !aligned(final_state, 4)) ||
+      (initial_state && !aligned(initial_state, 4)))
     return SS_ERR_INVALID_ARGUMENT;
-  const void* ins[] = {x, dt, B, C, A, D, dt_bias};
+  const void* ins[] = {x, dt, B, C, A, D, dt_bias, initial_state};
   const int64_t in_bytes[] = {x_elems * 2, dt_elems * 2, bc_elems * 2, bc_elems * 2,
-                              nheads * 4, D ? nheads * 4 : 0, dt_bias ? nheads * 4 : 0};
-  for (int i = 0; i < 7; ++i) {
+                              nheads * 4, D ? nheads * 4 : 0, dt_bias ? nheads * 4 : 0,
+                              initial_state ? st_elems * 4 : 0};
+  for (int i = 0; i < 8; ++i) {
     if (range_overlap(y, x_elems * 2, ins[i], in_bytes[i])) return SS_ERR_INVALID_ARGUMENT;
-    if (final_state && range_overlap(final_state, st_elems * 4, ins[i], in_bytes[i]))
+    // final_state may be initial_state itself: each thread reads its part of
+    // the given state before it writes the same elements back
+    if (final_state && !(i == 7 && final_state == initial_state) &&
+        range_overlap(final_state, st_elems * 4, ins[i], in_bytes[i]))
       return SS_ERR_INVALID_ARGUMENT;
   }
   if (final_state && range_overlap(final_state, st_elems * 4, y, x_elems * 2))
@@ -846,6 +860,7 @@ SS_API ss_status_t ss_mamba2_fwd(
   p.bias = dt_bias;
   p.softplus = dt_softplus ? 1 : 0;
   p.y = static_cast<__nv_bfloat16*>(y);
+  p.h0 = initial_state;
   p.final_state = final_state;
   p.batch = batch; p.seqlen = seqlen; p.nheads = nheads; p.ngroups = ngroups;
   (void)cudaGetLastError();

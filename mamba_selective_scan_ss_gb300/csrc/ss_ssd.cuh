@@ -82,6 +82,7 @@ struct SsdParams {
   const float* bias;        // [H] or null
   int softplus;
   __nv_bfloat16* y;         // [b,L,H,P]
+  const float* h0;          // [b,H,P,N] state before step 0, or null (zero)
   float* final_state;       // [b,H,P,N] or null
   int64_t batch, seqlen, nheads, ngroups;
 };
@@ -366,7 +367,10 @@ __global__ void __launch_bounds__(kSsdThreads, 1) ss_ssd_fwd(const __grid_consta
       //                           which has also read the accumulators reused here)
       //   Y_dg, S(c) = M X, B^T w.x  needs M, w.x and x of chunk c, and Y_in(c)
       //                           issued (so that the slot release covers it)
-      int64_t ncb = 0, nyin = 1, nmm = 0;  // next chunk of each stream
+      // Y_in(0) exists only when the sequence starts from a given state; the
+      // k-th Y_in issued waits for the k-th phase of bHready
+      const int64_t yin0 = p.h0 ? 0 : 1;
+      int64_t ncb = 0, nyin = yin0, nmm = 0;  // next chunk of each stream
       long long idle = 0;
       while (nmm < nchunks) {
         bool progress = false;
@@ -383,7 +387,7 @@ __global__ void __launch_bounds__(kSsdThreads, 1) ss_ssd_fwd(const __grid_consta
           progress = true;
         }
         if (nyin < nchunks && nyin <= nmm && nyin < ncb &&
-            mbar_test(bHready, (uint32_t)((nyin - 1) & 1))) {
+            mbar_test(bHready, (uint32_t)((nyin - yin0) & 1))) {
           const uint32_t uC = uS0 + (int)(nyin & 1) * kSsdSlot;
           tc_fence_after();
           for (int ks = 0; ks < N / 16; ++ks)
@@ -393,7 +397,7 @@ __global__ void __launch_bounds__(kSsdThreads, 1) ss_ssd_fwd(const __grid_consta
           ++nyin;
           progress = true;
         }
-        if ((nmm == 0 || nyin > nmm) && nmm < ncb && mbar_test(bMready, (uint32_t)(nmm & 1)) &&
+        if ((nmm < yin0 || nyin > nmm) && nmm < ncb && mbar_test(bMready, (uint32_t)(nmm & 1)) &&
             mbar_test(bFullX, (uint32_t)(nmm & 1))) {
           const int sl = (int)(nmm & 1);
           const uint32_t uB = uS0 + sl * kSsdSlot + 2 * kSsdHalf;
@@ -424,8 +428,27 @@ __global__ void __launch_bounds__(kSsdThreads, 1) ss_ssd_fwd(const __grid_consta
     // ---------------- epilogue warps 8-11 (row r, all columns)
     const uint32_t tlane = tm + ((uint32_t)(q4 * 32) << 16);  // this warp's lanes
     float hs[P];  // state row n = r: hs[p] = H[p][n]
+    const bool has_h0 = p.h0 != nullptr;
+    auto store_h_copy = [&]() {  // bf16 copy of row n = r of H, the Y_in operand
 #pragma unroll
-    for (int i = 0; i < P; ++i) hs[i] = 0.f;
+      for (int j = 0; j < P / 8; ++j)
+        *reinterpret_cast<uint4*>(sH + sw128(r, j)) =
+            make_uint4(bf16x2(hs[j * 8 + 0], hs[j * 8 + 1]), bf16x2(hs[j * 8 + 2], hs[j * 8 + 3]),
+                       bf16x2(hs[j * 8 + 4], hs[j * 8 + 5]), bf16x2(hs[j * 8 + 6], hs[j * 8 + 7]));
+    };
+    if (has_h0) {  // the given state enters as H of chunk 0 (phase 0 of bHready)
+      const float* h0 = p.h0 + (b * H + h) * P * N;
+#pragma unroll
+      for (int i = 0; i < P; ++i) hs[i] = h0[i * N + r];
+      store_h_copy();
+      fence_async_smem();
+      tc_fence_before();
+      mbar_arrive(bHready);
+    } else {
+#pragma unroll
+      for (int i = 0; i < P; ++i) hs[i] = 0.f;
+    }
+    const bool yin_c0 = has_h0;  // chunk 0 has a Y_in product
     bool ok = true;
     for (int64_t c = 0; c < nchunks; ++c) {
       const int64_t t0 = c * Q;
@@ -438,12 +461,12 @@ __global__ void __launch_bounds__(kSsdThreads, 1) ss_ssd_fwd(const __grid_consta
       const float et = ok ? ex2(cum[r]) : 0.f;
       mbar_arrive(bTEmpty + 8 * tb);  // the table buffer is read
       ok = ok && mbar_wait(bMma2, (uint32_t)(c & 1), abort);
-      if (ok && c > 0) ok = mbar_wait(bYin, (uint32_t)((c - 1) & 1), abort);
+      const bool has_yin = c > 0 || yin_c0;
+      if (ok && has_yin) ok = mbar_wait(bYin, (uint32_t)((c - (yin_c0 ? 0 : 1)) & 1), abort);
       ok = __all_sync(0xffffffffu, ok);
       tc_fence_after();
       if (ok) {
         {  // state (row n = r): H <- exp(cum_end) H + S^T, then its bf16 copy
-          const int n = r;
           uint32_t sa[16], sb[16];  // the next 16 columns are read while these are used
           tmem_ld16_async(tlane + kTmS, sa);
 #pragma unroll
@@ -455,11 +478,7 @@ __global__ void __launch_bounds__(kSsdThreads, 1) ss_ssd_fwd(const __grid_consta
 #pragma unroll
             for (int i = 0; i < 16; ++i) hs[q * 16 + i] = fmaf(decay, hs[q * 16 + i], fu(sv[i]));
           }
-#pragma unroll
-          for (int j = 0; j < P / 8; ++j)
-            *reinterpret_cast<uint4*>(sH + sw128(n, j)) =
-                make_uint4(bf16x2(hs[j * 8 + 0], hs[j * 8 + 1]), bf16x2(hs[j * 8 + 2], hs[j * 8 + 3]),
-                           bf16x2(hs[j * 8 + 4], hs[j * 8 + 5]), bf16x2(hs[j * 8 + 6], hs[j * 8 + 7]));
+          store_h_copy();
         }
         // output (row t = r), 16 columns at a time: y = exp(cum_t) Y_in + Y_dg
         const int t = r;
@@ -468,9 +487,9 @@ __global__ void __launch_bounds__(kSsdThreads, 1) ss_ssd_fwd(const __grid_consta
         for (int q = 0; q < P / 16; ++q) {
           uint32_t yd[16], yi[16];
           tmem_ld16_async(tlane + kTmYdg + q * 16, yd);
-          if (c > 0) tmem_ld16_async(tlane + kTmYin + q * 16, yi);
+          if (has_yin) tmem_ld16_async(tlane + kTmYin + q * 16, yi);
           tmem_wait(yd);
-          if (c > 0) {
+          if (has_yin) {
             tmem_wait(yi);
 #pragma unroll
             for (int i = 0; i < 16; ++i) yd[i] = __float_as_uint(fmaf(et, fu(yi[i]), fu(yd[i])));

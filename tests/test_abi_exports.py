@@ -26,7 +26,7 @@ def declared_functions():
 
 
 def test_header_declares_the_entry_points():
-    assert declared_functions() == ["ss_mamba2_fwd", "ss_selective_scan_bwd",
+    assert declared_functions() == ["ss_mamba2_fwd", "ss_mamba2_fwd_h0", "ss_selective_scan_bwd",
                                     "ss_selective_scan_bwd_h0", "ss_selective_scan_check",
                                     "ss_selective_scan_fwd",
                                     "ss_selective_scan_fwd_h0", "ss_selective_scan_fwd_noalloc",

@@ -55,12 +55,13 @@ def W(b, L, H, G, seed=0, **kw):
     return Mamba2Workload(f"m2-b{b}-L{L}-h{H}-g{G}", b, L, H, 64, G, 128, "bf16", seed=seed, **kw)
 
 
-def oracle_with_bounds(orc, inp, softplus=True):
+def oracle_with_bounds(orc, inp, softplus=True, h0=None):
     ref_y, ref_s = orc.ssd(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], inp["D"],
-                           inp["dt_bias"], softplus, dtype="bf16")
+                           inp["dt_bias"], softplus, dtype="bf16", initial_state=h0)
     D_abs = None if inp["D"] is None else inp["D"].abs()
     abs_y, abs_s = orc.ssd(inp["x"].abs(), inp["dt"], inp["A"], inp["B"].abs(), inp["C"].abs(),
-                           D_abs, inp["dt_bias"], softplus, dtype="bf16")
+                           D_abs, inp["dt_bias"], softplus, dtype="bf16",
+                           initial_state=None if h0 is None else np.abs(h0))
     return ref_y, ref_s, abs_y, abs_s
 
 
@@ -82,10 +83,10 @@ def check(got_y, got_s, ref_y, ref_s, abs_y, abs_s):
         print(f"[bf16 I/O bound] state: worst |err| / (1e-2 (1+|ref|)) = {io_s.max():.3g}")
 
 
-def run(inp, softplus=True, final=True):
+def run(inp, softplus=True, final=True, h0=None, final_buf=None):
     d = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
     out = ss.mamba2_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["dt_bias"], softplus,
-                        return_final_state=final)
+                        return_final_state=final, initial_state=h0, final_state=final_buf)
     torch.cuda.synchronize()
     assert ss.ss_selective_scan_check(None) == ss.SS_OK
     return out if final else (out, None)
@@ -153,6 +154,47 @@ def test_full_size_sampled_heads(orc):
                "D": inp["D"][h:h + 1].contiguous(),
                "dt_bias": inp["dt_bias"][h:h + 1].contiguous()}
         check(y[b:b + 1, :, h:h + 1], s[b:b + 1, h:h + 1], *oracle_with_bounds(orc, sub))
+
+
+def initial_state(w, seed):
+    g = torch.Generator().manual_seed(seed)
+    return torch.randn((w.batch, w.nheads, w.headdim, w.dstate), generator=g) * 0.5
+
+
+@pytest.mark.parametrize("L", [1, 127, 128, 129, 300])
+def test_from_initial_state(orc, L):
+    """The state before step 0 given: it enters chunk 0 the way a carried
+    state enters every later chunk (its bf16 copy in the C.H^T product)."""
+    w = W(2, L, 4, 2, seed=60 + L)
+    inp = make_mamba2_inputs(w)
+    h0 = initial_state(w, 61 + L)
+    y, s = run(inp, h0=h0.cuda())
+    check(y, s, *oracle_with_bounds(orc, inp, h0=h0.numpy().astype(np.float64)))
+
+
+def test_initial_state_updated_in_place(orc):
+    w = W(1, 200, 2, 1, seed=62)
+    inp = make_mamba2_inputs(w)
+    h0 = initial_state(w, 63)
+    buf = h0.clone().cuda()
+    y, s = run(inp, h0=buf, final_buf=buf)
+    assert s.data_ptr() == buf.data_ptr()
+    check(y, s, *oracle_with_bounds(orc, inp, h0=h0.numpy().astype(np.float64)))
+
+
+def test_chained_calls_at_a_chunk_boundary_equal_one_call():
+    """Split at a multiple of the 128-step chunk, the second call starts from
+    the first call's fp32 final state, which is exactly the state the single
+    call carries across that boundary: the results agree bit for bit."""
+    w = W(2, 384, 4, 2, seed=64)
+    inp = make_mamba2_inputs(w)
+    y_all, s_all = run(inp)
+    part = lambda sl: {k: (v[:, sl].contiguous() if k in ("x", "dt", "B", "C") else v)
+                       for k, v in inp.items()}
+    y1, s1 = run(part(slice(0, 256)))
+    y2, s2 = run(part(slice(256, 384)), h0=s1)
+    assert torch.equal(torch.cat([y1, y2], 1), y_all)
+    assert torch.equal(s2, s_all)
 
 
 def test_is_deterministic():
