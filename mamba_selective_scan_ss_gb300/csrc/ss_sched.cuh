@@ -159,6 +159,15 @@ struct PipeSmem {
   float m[2][kTileSteps][NT];         // widened, transposed B, C tile
 };
 
+// The kernel's pipeline buffers, declared in a function of their own rather
+// than at kernel scope (measured: 1-2.5% faster on every workload, the fp32
+// ones most; the placement of the CTA's shared variables is the only change).
+template <class S>
+__device__ __forceinline__ S& pipe_smem() {
+  __shared__ __align__(16) S sm;
+  return sm;
+}
+
 // One pass over steps [t_begin, t_end) of a unit: AGG = false runs the
 // recurrence from h and writes y; AGG = true runs it from h (zero) without C,
 // z or y and accumulates sum dt of the lane's own steps (for the aggregate's
@@ -434,7 +443,7 @@ __global__ void __launch_bounds__(TPB) ss_fwd_sched(const FwdParams p) {
   constexpr int RPC = PairRows<TGS, TPB>::kRowsPerCta;
   static_assert(TGS == 1 || TGS == 2, "one or two lanes per row pair");
   static_assert(G % 4 == 0, "a lane holds a multiple of four states");
-  __shared__ __align__(16) PipeSmem<T, NT, TGS, TPB, STAGES> sm;
+  PipeSmem<T, NT, TGS, TPB, STAGES>& sm = pipe_smem<PipeSmem<T, NT, TGS, TPB, STAGES>>();
   __shared__ unsigned s_ticket, s_flag;
 
   const int tid = threadIdx.x;
