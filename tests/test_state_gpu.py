@@ -73,6 +73,40 @@ def h0_slack(inp, h0):
     return y, slack_state[..., -1]
 
 
+@pytest.mark.parametrize("seqlen", [4, 1])
+def test_decay_factor_error(seqlen):
+    """The per-step error STEP_EPS assumes for the decay a = exp(dt A): read
+    a back through the C ABI (state 1 before step 0, no input, dt = 0 after
+    the first step) on the vector path (seqlen 4) and the scalar path
+    (seqlen 1), and bound its relative error against exp(dt A) in fp64 of
+    the same fp32 dt and A.  The exponent dt A log2(e) is itself rounded in
+    fp32 (relative 2^-23 of |x|, x = dt A log2 e), so the bound is
+    2^-22 (1 + |x|), and within STEP_EPS where |x| <= 1 (a >= 1/2; a
+    stronger decay shrinks the state it carries, and its error with it)."""
+    b, d, n = 1, 256, 16
+    g = torch.Generator().manual_seed(71)
+    dt0 = torch.exp(torch.rand((d,), generator=g) * 8.0 - 7.0)          # e^-7 .. e^1
+    A = -(torch.rand((d, n), generator=g) * 3.0 + 0.01)                  # -3.01 .. -0.01
+    delta = torch.zeros((b, d, seqlen))
+    delta[:, :, 0] = dt0
+    u = torch.zeros((b, d, seqlen))
+    B = torch.zeros((b, n, seqlen))
+    C = torch.zeros((b, n, seqlen))
+    h0 = torch.ones((b, d, n))
+    _, last = ss.selective_scan_fwd(u.cuda(), delta.cuda(), A.cuda(), B.cuda(), C.cuda(),
+                                    None, None, None, False, h0=h0.cuda())
+    torch.cuda.synchronize()
+    got = last.cpu().double().numpy()[0]                                 # [d, n]
+    x = dt0.double().numpy()[:, None] * A.double().numpy()               # natural-log exponent
+    exact = np.exp(x)
+    rel = np.abs(got - exact) / exact
+    x2 = np.abs(x) / np.log(2.0)
+    print(f"[decay] seqlen {seqlen}: max rel error {rel.max():.3g} "
+          f"({np.log2(rel.max()):.1f} in log2); |x| <= 1: {rel[x2 <= 1].max():.3g}")
+    assert np.all(rel <= 2.0 ** -22 * (1.0 + x2)), f"max ratio {np.max(rel / (2.0 ** -22 * (1 + x2))):.3g}"
+    assert rel[x2 <= 1].max() <= STEP_EPS
+
+
 def dev(inp):
     return {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
 
