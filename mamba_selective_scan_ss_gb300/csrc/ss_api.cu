@@ -840,8 +840,12 @@ SS_API ss_status_t ss_mamba2_fwd_h0(
   static std::once_flag smem_once[64];
   cudaError_t attr = cudaSuccess;
   std::call_once(smem_once[dev], [&] {
-    attr = cudaFuncSetAttribute(ss::ss_ssd_fwd, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    attr = cudaFuncSetAttribute(ss::ss_ssd_fwd<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 (int)ss::kSsdSmemBytes);
+    if (attr == cudaSuccess)
+      attr = cudaFuncSetAttribute(ss::ss_ssd_fwd<true>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  (int)ss::kSsdSmemBytes);
   });
   if (attr != cudaSuccess) return SS_ERR_CUDA;
 
@@ -864,8 +868,9 @@ SS_API ss_status_t ss_mamba2_fwd_h0(
   p.final_state = final_state;
   p.batch = batch; p.seqlen = seqlen; p.nheads = nheads; p.ngroups = ngroups;
   (void)cudaGetLastError();
-  ss::ss_ssd_fwd<<<(unsigned)units, ss::kSsdThreads, ss::kSsdSmemBytes,
-                   static_cast<cudaStream_t>(stream)>>>(p);
+  const auto kernel = initial_state ? ss::ss_ssd_fwd<true> : ss::ss_ssd_fwd<false>;
+  kernel<<<(unsigned)units, ss::kSsdThreads, ss::kSsdSmemBytes,
+           static_cast<cudaStream_t>(stream)>>>(p);
   return cudaGetLastError() == cudaSuccess ? SS_OK : SS_ERR_CUDA;
 }
 
