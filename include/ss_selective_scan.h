@@ -227,7 +227,8 @@ SS_API ss_status_t ss_selective_scan_bwd_h0(
  * ss_mamba2_fwd -- the Mamba-2 forward (one scalar decay per head), the
  * recurrence of the Mamba-2 cuTile news page ("Прорыв в оптимизации
  * SSM-моделей", section "Технические детали оптимизации"), evaluated in
- * chunks with the page's jump formula on the tensor cores (tcgen05):
+ * chunks with the page's jump formula on the tensor cores (tcgen05) for its
+ * common shape, and as a selective scan per head group otherwise:
  *   dt_t = softplus(dt[b,t,h] + dt_bias[h])   (or dt + dt_bias when dt_softplus == 0)
  *   h_t  = exp(A[h] dt_t) h_{t-1} + dt_t x_t B_t^T       state [headdim, dstate], zero at t = 0
  *   y_t  = h_t C_t + D[h] x_t
@@ -235,25 +236,31 @@ SS_API ss_status_t ss_selective_scan_bwd_h0(
  * g = h / (nheads / ngroups).
  *
  * Arguments (device pointers, dense row-major):
- *   x           [batch, seqlen, nheads, headdim]   bf16
- *   dt          [batch, seqlen, nheads]            bf16
+ *   x           [batch, seqlen, nheads, headdim]   dtype
+ *   dt          [batch, seqlen, nheads]            dtype
  *   A           [nheads]                           float32
- *   B, C        [batch, seqlen, ngroups, dstate]   bf16
+ *   B, C        [batch, seqlen, ngroups, dstate]   dtype
  *   D, dt_bias  [nheads]                           float32, or NULL (0)
- *   y           [batch, seqlen, nheads, headdim]   bf16 (written)
+ *   y           [batch, seqlen, nheads, headdim]   dtype (written)
  *   final_state [batch, nheads, headdim, dstate]   float32 (written), or NULL
- * Limits: dtype SS_BF16, headdim 64 and dstate 128 (else SS_ERR_UNSUPPORTED);
- * nheads a multiple of ngroups, x, B, C and y 16-byte aligned (else
- * SS_ERR_INVALID_ARGUMENT).  Precision: the products run on bf16 operands
- * with fp32 accumulation; the decayed C.B weights, the decayed inputs and the
- * state carried into a chunk are rounded to bf16 where they enter a product
- * (the state itself stays fp32).
+ * Limits: dstate <= 256 (else SS_ERR_UNSUPPORTED); nheads a multiple of
+ * ngroups and every pointer aligned to its element (else
+ * SS_ERR_INVALID_ARGUMENT).
+ * Two paths.  bf16 with headdim 64, 128 states and 16-byte aligned x, B, C
+ * and y runs on the tensor cores: one kernel, one CTA per (batch, head), no
+ * scratch; the products run on bf16 operands with fp32 accumulation, and the
+ * decayed C.B weights, the decayed inputs and the state carried into a chunk
+ * are rounded to bf16 where they enter a product (the state itself stays
+ * fp32); its waits on the tensor cores are bounded (SS_ERR_TIMEOUT from
+ * ss_selective_scan_check).  Every other call (fp32 or bf16, any head dim, up
+ * to 256 states) runs each head group as one selective scan over the group's
+ * heads' channels: channel-major copies of x, dt, B and C in scratch
+ * allocated and freed on `stream` (stream-ordered allocation), the scan of
+ * ss_selective_scan_fwd with the arithmetic of that call (fp32, bf16 only
+ * where y is stored), and y copied back; several kernels.
  * Behaviour: validated on the host (errors launch nothing and write
- * nothing); one kernel is enqueued on `stream`, one CTA per (batch, head);
- * no scratch, no synchronisation; its waits on the tensor cores are bounded
- * (SS_ERR_TIMEOUT from ss_selective_scan_check).  y and final_state must not
- * overlap any input or each other.  The state starts at zero (see
- * ss_mamba2_fwd_h0).
+ * nothing); no synchronisation.  y and final_state must not overlap any input
+ * or each other.  The state starts at zero (see ss_mamba2_fwd_h0).
  */
 SS_API ss_status_t ss_mamba2_fwd(
     const void* x, const void* dt, const float* A, const void* B, const void* C,

@@ -55,7 +55,7 @@ class SelectiveScanError(RuntimeError):
 def library_path(test_build: bool = False) -> Path:
     """Path of the shipped library (or of its test build, which adds the
     plan overrides and the unit-skipping hook that the tests drive through
-    SS_NCHUNKS, SS_CTAS_PER_SM and SS_TEST_SKIP_UNITS)."""
+    SS_NCHUNKS, SS_CTAS_PER_SM, SS_MAMBA2_ROWS and SS_TEST_SKIP_UNITS)."""
     return _PKG / ("libss_selective_scan_test.so" if test_build else "libss_selective_scan.so")
 
 
@@ -120,7 +120,8 @@ def load_library(test_build: bool | None = None):
 @contextlib.contextmanager
 def test_hooks():
     """Route every call made inside the block to the test build of the
-    library, which honours SS_NCHUNKS / SS_CTAS_PER_SM (plan overrides) and
+    library, which honours SS_NCHUNKS / SS_CTAS_PER_SM (plan overrides),
+    SS_MAMBA2_ROWS (the Mamba-2 tensor-core shape on the general path) and
     SS_TEST_SKIP_UNITS (units never handed out, so that device waits run out).
     The shipped library reads no environment variable."""
     global _USE_TEST_BUILD

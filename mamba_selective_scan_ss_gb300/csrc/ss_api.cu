@@ -17,6 +17,7 @@
 
 #include "ss_bwd.cuh"
 #include "ss_decode.cuh"
+#include "ss_layout.cuh"
 #include "ss_pc.cuh"
 #include "ss_sched.cuh"
 #include "ss_selective_scan.h"
@@ -689,6 +690,90 @@ ss_status_t bwd_impl(const void* u, const void* delta, const float* A, const voi
   return err == cudaSuccess && ferr == cudaSuccess ? SS_OK : SS_ERR_CUDA;
 }
 
+// The general Mamba-2 path (any head dim, up to 256 states, fp32 or bf16):
+// each head group runs as one selective scan over its heads' channels, on
+// channel-major copies of its inputs (ss_layout.cuh), with A, D and the dt
+// bias repeated per channel.  The scan's arithmetic is the Mamba-1 forward's
+// (fp32 throughout; bf16 only where y is stored).  Scratch is allocated on the
+// stream and freed after the last kernel that uses it.
+ss_status_t mamba2_rows(const void* x, const void* dt, const float* A, const void* B,
+                        const void* C, const float* D, const float* dt_bias, int dt_softplus,
+                        const float* h0, void* y, float* final_state, int64_t batch,
+                        int64_t seqlen, int64_t nheads, int64_t headdim, int64_t ngroups,
+                        int64_t dstate, ss_dtype_t dtype, cudaStream_t st) {
+  const int64_t elt = dtype == SS_F32 ? 4 : 2;
+  const int64_t L = seqlen, N = dstate, G = ngroups;
+  const int64_t CH = nheads * headdim, Cg = CH / G;  // scan channels, per group
+  if (batch > 65535 || L > (int64_t)INT_MAX * ss::kTile) return SS_ERR_UNSUPPORTED;  // grid z, y
+  const int64_t rows_bytes = round_up(batch * CH * L * elt, 256);
+  const int64_t bc_bytes = round_up(G * batch * N * L * elt, 256);
+  const int64_t a_bytes = round_up(CH * N * 4, 256), v_bytes = round_up(CH * 4, 256);
+  const int64_t st_bytes = G > 1 ? round_up(batch * CH * N * 4, 256) : 0;
+  const int64_t total = 3 * rows_bytes + 2 * bc_bytes + a_bytes + 2 * v_bytes + 2 * st_bytes;
+  (void)cudaGetLastError();
+  void* scratch = nullptr;
+  if (cudaMallocAsync(&scratch, (size_t)total, st) != cudaSuccess) return SS_ERR_CUDA;
+  char* p = static_cast<char*>(scratch);
+  char* u = p;                   p += rows_bytes;
+  char* delta = p;               p += rows_bytes;
+  char* yr = p;                  p += rows_bytes;
+  char* Bt = p;                  p += bc_bytes;
+  char* Ct = p;                  p += bc_bytes;
+  float* Ae = reinterpret_cast<float*>(p);  p += a_bytes;
+  float* De = reinterpret_cast<float*>(p);  p += v_bytes;
+  float* be = reinterpret_cast<float*>(p);  p += v_bytes;
+  float* h0g = reinterpret_cast<float*>(p); p += st_bytes;
+  float* lastg = reinterpret_cast<float*>(p);
+
+  auto to_rows = [&](const void* in, void* out, int64_t Cin, int rep, int64_t groups) {
+    const dim3 grid((unsigned)((Cin * rep + ss::kTile - 1) / ss::kTile),
+                    (unsigned)((L + ss::kTile - 1) / ss::kTile), (unsigned)batch);
+    if (elt == 4)
+      ss::ss_to_rows<float><<<grid, 256, 0, st>>>(static_cast<const float*>(in),
+                                                  static_cast<float*>(out), batch, L, Cin, rep,
+                                                  groups);
+    else
+      ss::ss_to_rows<__nv_bfloat16><<<grid, 256, 0, st>>>(
+          static_cast<const __nv_bfloat16*>(in), static_cast<__nv_bfloat16*>(out), batch, L, Cin,
+          rep, groups);
+  };
+  to_rows(x, u, CH, 1, G);                  // x [b,L,H*P] -> [G][b][Cg][L]
+  to_rows(dt, delta, nheads, (int)headdim, G);  // dt [b,L,H] -> every channel of its head
+  to_rows(B, Bt, G * N, 1, G);              // B [b,L,G,N] -> [G][b][N][L]
+  to_rows(C, Ct, G * N, 1, G);
+  const int64_t pe = CH * N;
+  ss::ss_expand_heads<<<(unsigned)std::min<int64_t>((pe + 255) / 256, 4096), 256, 0, st>>>(
+      A, D, dt_bias, Ae, De, be, nheads, headdim, N);
+  const int64_t se = batch * CH * N;
+  const unsigned sgrid = (unsigned)std::min<int64_t>((se + 255) / 256, 8192);
+  if (G > 1 && h0) ss::ss_group_rows<<<sgrid, 256, 0, st>>>(h0, h0g, batch, G, Cg, N, 1);
+  ss_status_t status = cudaGetLastError() == cudaSuccess ? SS_OK : SS_ERR_CUDA;
+  for (int64_t g = 0; g < G && status == SS_OK; ++g) {
+    const int64_t ro = g * batch * Cg * L * elt, bo = g * batch * N * L * elt;
+    const float* h0_g = G > 1 ? (h0 ? h0g + g * batch * Cg * N : nullptr) : h0;
+    float* last_g = G > 1 ? (final_state ? lastg + g * batch * Cg * N : nullptr) : final_state;
+    status = fwd_impl(u + ro, delta + ro, Ae + g * Cg * N, Bt + bo, Ct + bo,
+                      D ? De + g * Cg : nullptr, nullptr, dt_bias ? be + g * Cg : nullptr,
+                      dt_softplus, h0_g, yr + ro, last_g, batch, Cg, N, L, dtype, st);
+  }
+  if (status == SS_OK) {
+    const dim3 grid((unsigned)((CH + ss::kTile - 1) / ss::kTile),
+                    (unsigned)((L + ss::kTile - 1) / ss::kTile), (unsigned)batch);
+    if (elt == 4)
+      ss::ss_from_rows<float><<<grid, 256, 0, st>>>(reinterpret_cast<const float*>(yr),
+                                                    static_cast<float*>(y), batch, L, CH, G);
+    else
+      ss::ss_from_rows<__nv_bfloat16><<<grid, 256, 0, st>>>(
+          reinterpret_cast<const __nv_bfloat16*>(yr), static_cast<__nv_bfloat16*>(y), batch, L,
+          CH, G);
+    if (G > 1 && final_state)
+      ss::ss_group_rows<<<sgrid, 256, 0, st>>>(lastg, final_state, batch, G, Cg, N, 0);
+    if (cudaGetLastError() != cudaSuccess) status = SS_ERR_CUDA;
+  }
+  if (cudaFreeAsync(scratch, st) != cudaSuccess && status == SS_OK) status = SS_ERR_CUDA;
+  return status;
+}
+
 }  // namespace
 
 extern "C" {
@@ -803,7 +888,8 @@ SS_API ss_status_t ss_mamba2_fwd_h0(
   if (batch <= 0 || seqlen <= 0 || nheads <= 0 || headdim <= 0 || ngroups <= 0 || dstate <= 0)
     return SS_ERR_INVALID_ARGUMENT;
   if (nheads % ngroups != 0) return SS_ERR_INVALID_ARGUMENT;
-  if (dtype != SS_BF16 || headdim != ss::kSsdP || dstate != ss::kSsdN) return SS_ERR_UNSUPPORTED;
+  if (dstate > 256) return SS_ERR_UNSUPPORTED;
+  const int64_t elt = dtype == SS_F32 ? 4 : 2;
   int64_t tokens, x_elems, bc_elems, dt_elems, units, st_elems;
   if (!mul_ok(batch, seqlen, &tokens) || !mul_ok(tokens, nheads, &dt_elems) ||
       !mul_ok(dt_elems, headdim, &x_elems) || !mul_ok(tokens, ngroups, &bc_elems) ||
@@ -812,25 +898,36 @@ SS_API ss_status_t ss_mamba2_fwd_h0(
       bc_elems > INT64_MAX / 4 || st_elems > INT64_MAX / 4)
     return SS_ERR_UNSUPPORTED;
   if (units > INT_MAX) return SS_ERR_UNSUPPORTED;
-  if (!aligned(x, 16) || !aligned(B, 16) || !aligned(C, 16) || !aligned(y, 16) ||
-      !aligned(dt, 2) || !aligned(A, 4) || (D && !aligned(D, 4)) ||
+  const uintptr_t ea = (uintptr_t)elt;
+  if (!aligned(x, ea) || !aligned(B, ea) || !aligned(C, ea) || !aligned(y, ea) ||
+      !aligned(dt, ea) || !aligned(A, 4) || (D && !aligned(D, 4)) ||
       (dt_bias && !aligned(dt_bias, 4)) || (final_state && !aligned(final_state, 4)) ||
       (initial_state && !aligned(initial_state, 4)))
     return SS_ERR_INVALID_ARGUMENT;
   const void* ins[] = {x, dt, B, C, A, D, dt_bias, initial_state};
-  const int64_t in_bytes[] = {x_elems * 2, dt_elems * 2, bc_elems * 2, bc_elems * 2,
+  const int64_t in_bytes[] = {x_elems * elt, dt_elems * elt, bc_elems * elt, bc_elems * elt,
                               nheads * 4, D ? nheads * 4 : 0, dt_bias ? nheads * 4 : 0,
                               initial_state ? st_elems * 4 : 0};
   for (int i = 0; i < 8; ++i) {
-    if (range_overlap(y, x_elems * 2, ins[i], in_bytes[i])) return SS_ERR_INVALID_ARGUMENT;
+    if (range_overlap(y, x_elems * elt, ins[i], in_bytes[i])) return SS_ERR_INVALID_ARGUMENT;
     // final_state may be initial_state itself: each thread reads its part of
     // the given state before it writes the same elements back
     if (final_state && !(i == 7 && final_state == initial_state) &&
         range_overlap(final_state, st_elems * 4, ins[i], in_bytes[i]))
       return SS_ERR_INVALID_ARGUMENT;
   }
-  if (final_state && range_overlap(final_state, st_elems * 4, y, x_elems * 2))
+  if (final_state && range_overlap(final_state, st_elems * 4, y, x_elems * elt))
     return SS_ERR_INVALID_ARGUMENT;
+
+  // the tensor-core kernel takes bf16, head dim 64 and 128 states with 16-byte
+  // aligned x, B, C and y (TMA); every other call runs on the scan kernels
+  const bool tc = dtype == SS_BF16 && headdim == ss::kSsdP && dstate == ss::kSsdN &&
+                  aligned(x, 16) && aligned(B, 16) && aligned(C, 16) && aligned(y, 16) &&
+                  SS_TUNING("SS_MAMBA2_ROWS", 0) == 0;
+  if (!tc)
+    return mamba2_rows(x, dt, A, B, C, D, dt_bias, dt_softplus, initial_state, y, final_state,
+                       batch, seqlen, nheads, headdim, ngroups, dstate, dtype,
+                       static_cast<cudaStream_t>(stream));
 
   if (seqlen > INT_MAX || batch > INT_MAX || nheads * headdim > INT_MAX ||
       ngroups * dstate > INT_MAX)

@@ -14,7 +14,7 @@ import pytest
 @pytest.fixture
 def test_build():
     """Route the test's library calls to the test build, which honours the
-    SS_NCHUNKS / SS_CTAS_PER_SM plan overrides and SS_TEST_SKIP_UNITS."""
+    SS_NCHUNKS / SS_CTAS_PER_SM plan overrides, SS_MAMBA2_ROWS and SS_TEST_SKIP_UNITS."""
     import mamba_selective_scan_ss_gb300 as ss
     with ss.test_hooks():
         yield

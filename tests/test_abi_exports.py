@@ -49,7 +49,8 @@ def test_shipped_library_has_no_test_hooks(lib):
     build: the shipped library neither names their variables nor exports the
     hook's kernel."""
     shipped = ss.library_path().read_bytes()
-    for name in (b"SS_TEST_SKIP_UNITS", b"SS_NCHUNKS", b"SS_CTAS_PER_SM", b"ss_set_ticket"):
+    for name in (b"SS_TEST_SKIP_UNITS", b"SS_NCHUNKS", b"SS_CTAS_PER_SM", b"SS_MAMBA2_ROWS",
+                 b"ss_set_ticket"):
         assert name not in shipped, name
     test = ss.library_path(test_build=True).read_bytes()
     assert b"SS_TEST_SKIP_UNITS" in test and b"SS_NCHUNKS" in test
@@ -189,12 +190,14 @@ def test_validation_of_the_mamba2_forward(lib):
     assert call(y=None) == ss.SS_ERR_INVALID_ARGUMENT
     assert call(seqlen=0) == ss.SS_ERR_INVALID_ARGUMENT
     assert call(nheads=3, ngroups=2) == ss.SS_ERR_INVALID_ARGUMENT  # heads not a multiple of groups
-    assert call(dtype=ss.SS_F32) == ss.SS_ERR_UNSUPPORTED           # bf16 only
     assert call(dtype=7) == ss.SS_ERR_UNSUPPORTED
-    assert call(headdim=32) == ss.SS_ERR_UNSUPPORTED                # head dim 64 only
-    assert call(dstate=64) == ss.SS_ERR_UNSUPPORTED                 # 128 states only
-    assert call(x=ok["x"] + 2) == ss.SS_ERR_INVALID_ARGUMENT        # rows not 16-byte aligned
+    assert call(dstate=257) == ss.SS_ERR_UNSUPPORTED                # at most 256 states
+    assert call(headdim=32, dstate=257) == ss.SS_ERR_UNSUPPORTED    # on the general path too
+    assert call(dtype=ss.SS_F32, dstate=300) == ss.SS_ERR_UNSUPPORTED
+    assert call(x=ok["x"] + 1) == ss.SS_ERR_INVALID_ARGUMENT        # not aligned to its element
+    assert call(dtype=ss.SS_F32, B=ok["B"] + 2) == ss.SS_ERR_INVALID_ARGUMENT
     assert call(y=ok["x"]) == ss.SS_ERR_INVALID_ARGUMENT            # output over an input
+    assert call(final_state=ok["y"]) == ss.SS_ERR_INVALID_ARGUMENT  # outputs overlap
 
 def test_plan_is_host_only_and_consistent(lib, monkeypatch):
     monkeypatch.delenv("SS_NCHUNKS", raising=False)
