@@ -578,9 +578,7 @@ __global__ void __launch_bounds__(kSsdThreads, 1) ss_ssd_fwd(const __grid_consta
       // ---- M (row t = r) from CB: D on the diagonal, zero above it.  The two
       // warps of a lane quarter split every 32-column block in 16-column halves
       // (this warp: half hf of blocks 0..3), so the causal work is shared
-      // evenly; the tensor-memory read of the next half is in flight while
-      // the current one is processed.  M's buffer is free once chunk c-1's
-      // products are done.
+      // evenly.  M's buffer is free once chunk c-1's products are done.
       ok = __all_sync(0xffffffffu, ok && mbar_wait(bCB + 8 * buf, (uint32_t)((c >> 1) & 1), abort));
       if (c > 0)
         ok = __all_sync(0xffffffffu, ok && mbar_wait(bMma2, (uint32_t)((c - 1) & 1), abort));
@@ -594,54 +592,54 @@ __global__ void __launch_bounds__(kSsdThreads, 1) ss_ssd_fwd(const __grid_consta
               make_uint4(bf16x2(m[0], m[1]), bf16x2(m[2], m[3]), bf16x2(m[4], m[5]),
                          bf16x2(m[6], m[7]));
         };
-        // two register buffers, chosen by the (unrolled) block index: a buffer
-        // is only read after the wait that names it
-        uint32_t ba[16], bb[16];
-        tmem_ld16_async(tcb, ba);  // block 0 (q4 >= 0 always)
-#pragma unroll
-        for (int i = 0; i < Q / 32; ++i) {
-          uint32_t(&cur)[16] = (i & 1) ? bb : ba;
-          uint32_t(&nxt)[16] = (i & 1) ? ba : bb;
+        // one 32-column block at a time; the loop is not unrolled, which keeps
+        // this role's code small (measured: the unrolled form, a tensor-memory
+        // read of the next block in flight, was 6% slower, the roles' code
+        // contending for the instruction cache)
+#pragma unroll 1
+        for (int i = 0; i <= q4; ++i) {  // at and below the diagonal
+          uint32_t cur[16];
+          tmem_ld16_async(tcb + 32 * i, cur);
+          tmem_wait(cur);
           const int s0 = 32 * i + 16 * hf;  // first column of this half
-          if (i <= q4) {
-            tmem_wait(cur);
-            if (i + 1 <= q4) tmem_ld16_async(tcb + 32 * (i + 1), nxt);
-            if (i < q4) {  // below the diagonal: exp2(cum_t - cum_e) exp2(cum_e - cum_s) dt_s
-              const float et = ex2(ct - cum[32 * i + 31]);
+          if (i < q4) {  // below the diagonal: exp2(cum_t - cum_e) exp2(cum_e - cum_s) dt_s
+            const float et = ex2(ct - cum[32 * i + 31]);
 #pragma unroll
-              for (int kk = 0; kk < 2; ++kk) {
-                float m[8], gv[8];
-                *reinterpret_cast<float4*>(gv) = *reinterpret_cast<const float4*>(gs + s0 + 8 * kk);
-                *reinterpret_cast<float4*>(gv + 4) =
-                    *reinterpret_cast<const float4*>(gs + s0 + 8 * kk + 4);
+            for (int kk = 0; kk < 2; ++kk) {
+              float m[8], gv[8];
+              *reinterpret_cast<float4*>(gv) = *reinterpret_cast<const float4*>(gs + s0 + 8 * kk);
+              *reinterpret_cast<float4*>(gv + 4) =
+                  *reinterpret_cast<const float4*>(gs + s0 + 8 * kk + 4);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) m[e] = fu(cur[8 * kk + e]) * et * gv[e];
-                store8(s0 / 8 + kk, m);
-              }
-            } else {  // the diagonal block: exp2(cum_t - cum_s) dt_s per element, masked
-#pragma unroll
-              for (int kk = 0; kk < 2; ++kk) {
-                float m[8], cv[8], dv[8];
-                const int sb = s0 + 8 * kk;
-                *reinterpret_cast<float4*>(cv) = *reinterpret_cast<const float4*>(cum + sb);
-                *reinterpret_cast<float4*>(cv + 4) = *reinterpret_cast<const float4*>(cum + sb + 4);
-                *reinterpret_cast<float4*>(dv) = *reinterpret_cast<const float4*>(dts + sb);
-                *reinterpret_cast<float4*>(dv + 4) = *reinterpret_cast<const float4*>(dts + sb + 4);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                  const int sc = sb + e;
-                  const float v = fu(cur[8 * kk + e]) * ex2(ct - cv[e]) * dv[e];
-                  m[e] = sc < t ? v : (sc == t ? v + Dh : 0.f);
-                }
-                store8(sb / 8, m);
-              }
+              for (int e = 0; e < 8; ++e) m[e] = fu(cur[8 * kk + e]) * et * gv[e];
+              store8(s0 / 8 + kk, m);
             }
-          } else {  // above the diagonal
+          } else {  // the diagonal block: exp2(cum_t - cum_s) dt_s per element, masked
 #pragma unroll
-            for (int kk = 0; kk < 2; ++kk)
-              *reinterpret_cast<uint4*>(sM + ((s0 / 8 + kk) >> 3) * kSsdHalf +
-                                        sw128(t, (s0 / 8 + kk) & 7)) = make_uint4(0, 0, 0, 0);
+            for (int kk = 0; kk < 2; ++kk) {
+              float m[8], cv[8], dv[8];
+              const int sb = s0 + 8 * kk;
+              *reinterpret_cast<float4*>(cv) = *reinterpret_cast<const float4*>(cum + sb);
+              *reinterpret_cast<float4*>(cv + 4) = *reinterpret_cast<const float4*>(cum + sb + 4);
+              *reinterpret_cast<float4*>(dv) = *reinterpret_cast<const float4*>(dts + sb);
+              *reinterpret_cast<float4*>(dv + 4) = *reinterpret_cast<const float4*>(dts + sb + 4);
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                const int sc = sb + e;
+                const float v = fu(cur[8 * kk + e]) * ex2(ct - cv[e]) * dv[e];
+                m[e] = sc < t ? v : (sc == t ? v + Dh : 0.f);
+              }
+              store8(sb / 8, m);
+            }
           }
+        }
+#pragma unroll 1
+        for (int i = q4 + 1; i < Q / 32; ++i) {  // above the diagonal
+          const int s0 = 32 * i + 16 * hf;
+#pragma unroll
+          for (int kk = 0; kk < 2; ++kk)
+            *reinterpret_cast<uint4*>(sM + ((s0 / 8 + kk) >> 3) * kSsdHalf +
+                                      sw128(t, (s0 / 8 + kk) & 7)) = make_uint4(0, 0, 0, 0);
         }
       }
       // ---- w.x (row s = r, columns [32 hf, 32 hf + 32)) once x has arrived
