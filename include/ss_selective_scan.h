@@ -83,7 +83,13 @@ typedef enum {
  *
  * Alignment: every pointer must be aligned to its element size (4 bytes for
  * float32 arrays, 2 bytes for bf16 arrays).  Rows whose start is also
- * 16-byte aligned take the vectorised path; others take a scalar path.
+ * 16-byte aligned (seqlen a multiple of 4 for float32, of 8 for bf16, and
+ * aligned buffers) take the vectorised path.  Other calls of at least 2^16
+ * rows x steps are run on the vectorised path through padded copies of the
+ * rows in stream-ordered scratch, whose extra steps leave the state unchanged
+ * (dt = 0 there), when that padding is exact: with the softplus, or with
+ * float32 I/O, or without a delta bias; the remaining calls take a scalar
+ * path.
  *
  * Behaviour: arguments are validated on the host first; on any error the
  * function returns that status, launches nothing and writes nothing.  On

@@ -361,6 +361,79 @@ ss_status_t fwd_impl(const void* u, const void* delta, const float* A, const voi
                      const void* C, const float* D, const void* z, const float* delta_bias,
                      int delta_softplus, const float* h0, void* y, float* last_state,
                      int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
+                     ss_dtype_t dtype, void* stream);
+
+constexpr int64_t kPadMinElems = 1 << 16;  // rows x steps below which ragged calls stay scalar
+
+// The forward of ragged rows through padded copies (see fwd_impl): u, delta,
+// z, B and C copied into rows of seqlen rounded up to the vector, in
+// stream-ordered scratch, the vector path run on them, and y copied back;
+// last_state is the padded run's own (the padding leaves the state as it is).
+ss_status_t fwd_padded(const void* u, const void* delta, const float* A, const void* B,
+                       const void* C, const float* D, const void* z, const float* delta_bias,
+                       int delta_softplus, const float* h0, void* y, float* last_state,
+                       int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
+                       ss_dtype_t dtype, cudaStream_t st) {
+  const int64_t elt = dtype == SS_F32 ? 4 : 2;
+  const int64_t Lp = round_up(seqlen, 16 / elt);
+  const int64_t rows = batch * dim, bc_rows = batch * dstate;
+  const int64_t x_bytes = round_up(rows * Lp * elt, 256), bc_bytes = round_up(bc_rows * Lp * elt, 256);
+  const int64_t total = (z ? 4 : 3) * x_bytes + 2 * bc_bytes;
+  (void)cudaGetLastError();
+  void* scratch = nullptr;
+  if (cudaMallocAsync(&scratch, (size_t)total, st) != cudaSuccess) return SS_ERR_CUDA;
+  char* q = static_cast<char*>(scratch);
+  char* up = q;               q += x_bytes;
+  char* dp = q;               q += x_bytes;
+  char* yp = q;               q += x_bytes;
+  char* Bp = q;               q += bc_bytes;
+  char* Cp = q;               q += bc_bytes;
+  char* zp = z ? q : nullptr;
+  const float neg_inf = -__builtin_huge_valf();
+  const int64_t vecs = Lp / (16 / elt);
+  auto grid_of = [&](int64_t nrows, int64_t nv) {
+    return dim3((unsigned)std::min<int64_t>((nv + 255) / 256, 64),
+                (unsigned)std::min<int64_t>(nrows, 65535));
+  };
+  auto pad = [&](const void* in, void* out, int64_t nrows, float fill, const float* neg_of) {
+    const dim3 grid = grid_of(nrows, vecs);
+    if (elt == 4)
+      ss::ss_pad_rows<float><<<grid, 256, 0, st>>>(static_cast<const float*>(in),
+                                                   static_cast<float*>(out), nrows, seqlen, Lp,
+                                                   fill, neg_of, dim);
+    else
+      ss::ss_pad_rows<__nv_bfloat16><<<grid, 256, 0, st>>>(
+          static_cast<const __nv_bfloat16*>(in), static_cast<__nv_bfloat16*>(out), nrows, seqlen,
+          Lp, fill, neg_of, dim);
+  };
+  pad(u, up, rows, 0.f, nullptr);
+  pad(delta, dp, rows, delta_softplus ? neg_inf : 0.f, delta_softplus ? nullptr : delta_bias);
+  if (z) pad(z, zp, rows, 0.f, nullptr);
+  pad(B, Bp, bc_rows, 0.f, nullptr);
+  pad(C, Cp, bc_rows, 0.f, nullptr);
+  ss_status_t status = cudaGetLastError() == cudaSuccess ? SS_OK : SS_ERR_CUDA;
+  if (status == SS_OK)
+    status = fwd_impl(up, dp, A, Bp, Cp, D, zp, delta_bias, delta_softplus, h0, yp, last_state,
+                      batch, dim, dstate, Lp, dtype, st);
+  if (status == SS_OK) {
+    const dim3 grid = grid_of(rows, (seqlen + 16 / elt - 1) / (16 / elt));
+    if (elt == 4)
+      ss::ss_unpad_rows<float><<<grid, 256, 0, st>>>(reinterpret_cast<const float*>(yp),
+                                                     static_cast<float*>(y), rows, seqlen, Lp);
+    else
+      ss::ss_unpad_rows<__nv_bfloat16><<<grid, 256, 0, st>>>(
+          reinterpret_cast<const __nv_bfloat16*>(yp), static_cast<__nv_bfloat16*>(y), rows,
+          seqlen, Lp);
+    if (cudaGetLastError() != cudaSuccess) status = SS_ERR_CUDA;
+  }
+  if (cudaFreeAsync(scratch, st) != cudaSuccess && status == SS_OK) status = SS_ERR_CUDA;
+  return status;
+}
+
+ss_status_t fwd_impl(const void* u, const void* delta, const float* A, const void* B,
+                     const void* C, const float* D, const void* z, const float* delta_bias,
+                     int delta_softplus, const float* h0, void* y, float* last_state,
+                     int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
                      ss_dtype_t dtype, void* stream) {
   // ---- validation: nothing is enqueued or written on error ----
   if (dtype != SS_F32 && dtype != SS_BF16) return SS_ERR_UNSUPPORTED;
@@ -403,6 +476,16 @@ ss_status_t fwd_impl(const void* u, const void* delta, const float* A, const voi
     return SS_ERR_UNSUPPORTED;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // Ragged rows (seqlen not a multiple of the 16-byte vector, or unaligned
+  // buffers): the vector path on padded copies is several times faster than
+  // the scalar path, and exact when the padding leaves the state unchanged:
+  // dt = 0 there (delta -inf under the softplus, else -bias, which is exact in
+  // fp32), u = B = C = 0.  Small calls stay on the scalar path.
+  if (!plan.vec && batch * dim * seqlen >= kPadMinElems &&
+      (delta_softplus || dtype == SS_F32 || !delta_bias) && SS_TUNING("SS_NO_PAD", 0) == 0)
+    return fwd_padded(u, delta, A, B, C, D, z, delta_bias, delta_softplus, h0, y, last_state,
+                      batch, dim, dstate, seqlen, dtype, st);
+
   ss::FwdParams p{};
   p.u = u; p.delta = delta; p.A = A; p.B = B; p.C = C; p.D = D; p.z = z; p.bias = delta_bias;
   p.h0 = h0;

@@ -1,5 +1,7 @@
-// Layout changes between the Mamba-2 token-major tensors and the channel-
-// major rows of the selective-scan kernels, for the general Mamba-2 path
+// Layout changes around the selective-scan kernels.  pad_rows / unpad_rows
+// give rows of a ragged length the 16-byte aligned, vector-multiple layout of
+// the vector path.  The others convert between the Mamba-2 token-major
+// tensors and the channel-major rows of the scan, for the general Mamba-2 path
 // (any head dim, up to 256 states, fp32 or bf16): a head of the Mamba-2
 // recurrence of the Mamba-2 cuTile news page ("Технические детали
 // оптимизации") is the selective scan of "Mamba CUDA 实现解析" eq (4)-(7)
@@ -17,6 +19,8 @@
 #pragma once
 
 #include <cstdint>
+
+#include "ss_device.cuh"
 
 namespace ss {
 
@@ -101,6 +105,57 @@ __global__ void ss_expand_heads(const float* __restrict__ A, const float* __rest
     if (i % N == 0) {
       if (D) D_out[c] = D[h];
       if (bias) bias_out[c] = bias[h];
+    }
+  }
+}
+
+// Rows of a ragged length L copied into rows of Lp >= L steps (a multiple of
+// the 16-byte vector) whose starts are 16-byte aligned, for the vector path:
+// steps past L get `fill`, or, when `neg_of` is given, minus its entry for the
+// row's channel (row % dim).  grid.y walks the rows, grid.x * block the
+// vectors of a row; each thread writes whole 16-byte vectors.
+template <typename T>
+__global__ void __launch_bounds__(256) ss_pad_rows(const T* __restrict__ in, T* __restrict__ out,
+                                                    int64_t rows, int64_t L, int64_t Lp,
+                                                    float fill, const float* __restrict__ neg_of,
+                                                    int64_t dim) {
+  constexpr int V = Elem<T>::kVec;
+  const int64_t nvec = Lp / V;
+  for (int64_t row = blockIdx.y; row < rows; row += gridDim.y) {
+    const T* src = in + row * L;
+    T* dst = out + row * Lp;
+    const T fv = Elem<T>::from_f32(neg_of ? -neg_of[row % dim] : fill);
+    for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < nvec;
+         v += (int64_t)gridDim.x * blockDim.x) {
+      Vec16<T> w;
+#pragma unroll
+      for (int e = 0; e < V; ++e) {
+        const int64_t t = v * V + e;
+        w.e[e] = t < L ? src[t] : fv;
+      }
+      stg_vec(dst + v * V, w);
+    }
+  }
+}
+
+// ... and the first L steps of each padded row back into rows of L (whole
+// 16-byte vectors read, elements written).
+template <typename T>
+__global__ void __launch_bounds__(256) ss_unpad_rows(const T* __restrict__ in, T* __restrict__ out,
+                                                      int64_t rows, int64_t L, int64_t Lp) {
+  constexpr int V = Elem<T>::kVec;
+  const int64_t nvec = (L + V - 1) / V;
+  for (int64_t row = blockIdx.y; row < rows; row += gridDim.y) {
+    const T* src = in + row * Lp;
+    T* dst = out + row * L;
+    for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < nvec;
+         v += (int64_t)gridDim.x * blockDim.x) {
+      const Vec16<T> w = ldg_vec(src + v * V);
+#pragma unroll
+      for (int e = 0; e < V; ++e) {
+        const int64_t t = v * V + e;
+        if (t < L) dst[t] = w.e[e];
+      }
     }
   }
 }

@@ -294,3 +294,41 @@ def test_full_size_workload_sampled(orc, key):
         assert_close(s_rows[i], ref[r][1], w.dtype, f"{w.name} row {r} state")
     # every output is finite
     assert torch.isfinite(y.float()).all()
+
+
+# Ragged rows of a size that takes the padded vector path (seqlen not a
+# multiple of the 16-byte vector, rows x steps >= 2^16): the rows are copied
+# into aligned, padded rows whose extra steps leave the state unchanged
+# (dt = 0 there), the vector path runs on them and y is copied back.
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("shape", [(4, 512, 16, 1023), (2, 300, 16, 509), (1, 256, 32, 777)])
+def test_ragged_rows_on_the_padded_vector_path(orc, dtype, shape):
+    b, d, n, L = shape
+    check(orc, ScanWorkload(f"ragged-b{b}-d{d}-n{n}-L{L}-{dtype}", b, d, n, L, dtype,
+                            seed=L + d))
+
+
+def _no_softplus_inputs(w, bias_value):
+    """dt = delta + bias > 0 without the softplus, with a bias present."""
+    inp = make_inputs(w)
+    bias = torch.full((w.dim,), bias_value, dtype=torch.float32)
+    delta = inp["delta"].float().abs() * 0.05 + 0.01
+    inp["delta"] = delta.to(inp["delta"].dtype)
+    inp["delta_bias"] = bias
+    return inp
+
+
+def test_ragged_rows_padded_without_softplus_fp32(orc):
+    """No softplus, fp32: the padding's delta is -bias, which cancels the bias
+    exactly, so the padded steps leave the state as it is."""
+    w = ScanWorkload("ragged-nosp-b2-d300-n16-L511-f32", 2, 300, 16, 511, "f32",
+                     softplus=False, seed=7)
+    check(orc, w, _no_softplus_inputs(w, 0.37))
+
+
+def test_ragged_rows_bf16_without_softplus_stay_scalar(orc):
+    """bf16 without softplus and with a bias cannot pad exactly (-0.37 is not a
+    bf16 value): the scalar path runs, and matches the oracle."""
+    w = ScanWorkload("ragged-nosp-b2-d300-n16-L511-bf16", 2, 300, 16, 511, "bf16",
+                     softplus=False, seed=8)
+    check(orc, w, _no_softplus_inputs(w, 0.37))
