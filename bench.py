@@ -411,16 +411,14 @@ def run_ours(args, world, rank, local):
                   if isinstance(v, torch.Tensor))
         d2h = y_host.numel() * y_host.element_size() + st_host.numel() * st_host.element_size()
 
+        # the C-ABI call on host buffers: it copies the rows in, scans and
+        # copies y and last_state out, overlapping copies and scan over
+        # segments of the sequence (ss_selective_scan_fwd_host)
         def e2e_step():
-            with torch.cuda.stream(stream):
-                for k, v in host.items():
-                    if isinstance(v, torch.Tensor):
-                        d[k].copy_(v, non_blocking=True)
-                ss.selective_scan_fwd(d["u"], d["delta"], d["A"], d["B"], d["C"], d["D"], d["z"],
-                                      d["delta_bias"], d["delta_softplus"], y=y, last_state=st,
-                                      stream=stream)
-                y_host.copy_(y, non_blocking=True)
-                st_host.copy_(st, non_blocking=True)
+            ss.selective_scan_fwd_host(host["u"], host["delta"], host["A"], host["B"],
+                                       host["C"], host["D"], host["z"], host["delta_bias"],
+                                       host["delta_softplus"], y=y_host, last_state=st_host,
+                                       stream=stream)
 
         for _ in range(3):
             e2e_step()

@@ -134,6 +134,37 @@ SS_API ss_status_t ss_selective_scan_fwd_h0(
     ss_dtype_t dtype, void* stream);
 
 /*
+ * ss_selective_scan_fwd_host -- the forward of ss_selective_scan_fwd_h0 on
+ * arrays in HOST memory: every array argument (u, delta, A, B, C, D, z,
+ * delta_bias, h0, y, last_state) is a host pointer, with the layouts,
+ * dtypes, NULL options and overlap rules of ss_selective_scan_fwd_h0.
+ * Page-locked (pinned) host memory lets the copies overlap the scan; pageable
+ * memory works, with staged copies.
+ *
+ * The work goes in pieces, two in flight: the inputs of piece k+1 are copied
+ * in on a stream of the call's own while piece k is scanned on `stream` and
+ * the outputs of piece k-1 are copied out on a third stream.  With batch > 1
+ * a piece is a slice of the batch (up to 8 slices; contiguous copies; each
+ * slice an independent scan, so the results are those of
+ * ss_selective_scan_fwd_h0 on that slice); a single sequence goes in
+ * segments of about 4096 steps (up to 8; strided 2-D copies), each scanned
+ * from the state the previous one left, which equals one call over the whole
+ * sequence within the fp32 arithmetic's tolerance (chaining through the
+ * state, as ss_selective_scan_fwd_h0 documents).  Device buffers for two
+ * pieces are allocated and freed on `stream` (stream-ordered).
+ *
+ * Behaviour: validated on the host (errors launch nothing and write
+ * nothing).  The call is synchronous: it returns once y and last_state are
+ * in host memory (SS_OK), or with the first error.
+ */
+SS_API ss_status_t ss_selective_scan_fwd_host(
+    const void* u, const void* delta, const float* A, const void* B, const void* C,
+    const float* D, const void* z, const float* delta_bias, int delta_softplus,
+    const float* h0, void* y, float* last_state,
+    int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
+    ss_dtype_t dtype, void* stream);
+
+/*
  * ss_selective_state_update -- one decode step (one token) of the selective
  * scan for every (batch, channel), with the state updated in place: the
  * token-by-token recurrent form that "从顺序到并行用PyTorch实现Blelloch算法加速Mamba

@@ -8,7 +8,7 @@ raise: there is no fallback implementation.
 Low-level names mirror the C ABI exactly (raw device pointers as ints):
     ss_selective_scan_fwd, ss_selective_scan_fwd_h0, ss_selective_state_update,
     ss_selective_scan_bwd, ss_selective_scan_bwd_h0, ss_selective_scan_fwd_pc,
-    ss_selective_scan_fwd_pc_h0, ss_mamba2_fwd, ss_mamba2_fwd_h0,
+    ss_selective_scan_fwd_pc_h0, ss_selective_scan_fwd_host, ss_mamba2_fwd, ss_mamba2_fwd_h0,
     ss_status_string, ss_selective_scan_check, ss_selective_scan_plan,
     ss_selective_scan_fwd_noalloc
 plus convenience wrappers for torch CUDA tensors:
@@ -32,9 +32,9 @@ __all__ = [
     "ss_selective_scan_fwd", "ss_status_string", "ss_selective_scan_check",
     "ss_selective_scan_plan", "ss_selective_scan_fwd_noalloc", "ss_selective_scan_fwd_h0",
     "ss_selective_state_update", "ss_selective_scan_bwd", "ss_selective_scan_bwd_h0",
-    "ss_selective_scan_fwd_pc", "ss_selective_scan_fwd_pc_h0",
+    "ss_selective_scan_fwd_pc", "ss_selective_scan_fwd_pc_h0", "ss_selective_scan_fwd_host",
     "ss_mamba2_fwd", "ss_mamba2_fwd_h0", "selective_scan_fwd", "test_hooks",
-    "selective_state_update", "selective_scan_bwd", "mamba2_fwd",
+    "selective_state_update", "selective_scan_bwd", "mamba2_fwd", "selective_scan_fwd_host",
 ]
 
 SS_F32, SS_BF16 = 0, 1
@@ -81,6 +81,8 @@ def _declare(lib):
     lib.ss_selective_scan_fwd_pc.argtypes = list(lib.ss_selective_scan_fwd.argtypes)
     lib.ss_selective_scan_fwd_pc_h0.restype = ctypes.c_int
     lib.ss_selective_scan_fwd_pc_h0.argtypes = list(lib.ss_selective_scan_fwd_h0.argtypes)
+    lib.ss_selective_scan_fwd_host.restype = ctypes.c_int
+    lib.ss_selective_scan_fwd_host.argtypes = list(lib.ss_selective_scan_fwd_h0.argtypes)
     lib.ss_selective_scan_bwd.restype = ctypes.c_int
     lib.ss_selective_scan_bwd.argtypes = [vp] * 8 + [ctypes.c_int] + [vp] * 10 + \
         [i64, i64, i64, i64, ctypes.c_int, vp]
@@ -199,6 +201,14 @@ def ss_selective_scan_fwd_pc_h0(u, delta, A, B, C, D, z, delta_bias, delta_softp
                                 last_state, batch, dim, dstate, seqlen, dtype, stream) -> int:
     """The per-channel forward started from state h0 (fp32 [batch, dim, dstate])."""
     return load_library().ss_selective_scan_fwd_pc_h0(
+        u, delta, A, B, C, D, z, delta_bias, int(delta_softplus), h0, y, last_state,
+        batch, dim, dstate, seqlen, int(dtype), stream)
+
+
+def ss_selective_scan_fwd_host(u, delta, A, B, C, D, z, delta_bias, delta_softplus, h0, y,
+                               last_state, batch, dim, dstate, seqlen, dtype, stream) -> int:
+    """The forward on host arrays (pointers are host addresses); synchronous."""
+    return load_library().ss_selective_scan_fwd_host(
         u, delta, A, B, C, D, z, delta_bias, int(delta_softplus), h0, y, last_state,
         batch, dim, dstate, seqlen, int(dtype), stream)
 
@@ -325,6 +335,43 @@ def selective_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None,
         what = ("_pc" if per_channel else "") + ("" if h0 is None else "_h0")
         raise SelectiveScanError(status, "ss_selective_scan_fwd" + what)
     return (y, last_state) if return_last_state else y
+
+
+def selective_scan_fwd_host(u, delta, A, B, C, D=None, z=None, delta_bias=None,
+                            delta_softplus: bool = True, h0=None, y=None, last_state=None,
+                            stream=None):
+    """The forward on CPU torch tensors (pinned for overlapped copies), through
+    ss_selective_scan_fwd_host: same layouts and dtypes as selective_scan_fwd;
+    returns (y, last_state) as CPU tensors once they are complete.  The copies
+    and the scan run on ``stream`` (default torch's current stream) and two
+    streams of the call's own."""
+    import torch
+
+    for name, t in (("u", u), ("delta", delta), ("A", A), ("B", B), ("C", C), ("D", D),
+                    ("z", z), ("delta_bias", delta_bias), ("h0", h0)):
+        if t is not None and (t.is_cuda or not t.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous CPU tensor")
+    dt = _io_dtype(u)
+    for name, t in (("delta", delta), ("B", B), ("C", C), ("z", z)):
+        if t is not None and t.dtype != u.dtype:
+            raise TypeError(f"{name} must have dtype {u.dtype}")
+    for name, t in (("A", A), ("D", D), ("delta_bias", delta_bias), ("h0", h0)):
+        if t is not None and t.dtype != torch.float32:
+            raise TypeError(f"{name} must be float32")
+    batch, dim, seqlen = u.shape
+    dstate = A.shape[1]
+    if y is None:
+        y = torch.empty(u.shape, dtype=u.dtype, pin_memory=u.is_pinned())
+    if last_state is None:
+        last_state = torch.empty((batch, dim, dstate), dtype=torch.float32,
+                                 pin_memory=u.is_pinned())
+    s = _stream(stream, torch.device("cuda", torch.cuda.current_device()))
+    status = ss_selective_scan_fwd_host(
+        _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias),
+        delta_softplus, _ptr(h0), _ptr(y), _ptr(last_state), batch, dim, dstate, seqlen, dt, s)
+    if status != SS_OK:
+        raise SelectiveScanError(status, "ss_selective_scan_fwd_host")
+    return y, last_state
 
 
 def selective_state_update(state, x, dt, A, B, C, D=None, z=None, dt_bias=None,

@@ -364,6 +364,8 @@ ss_status_t fwd_impl(const void* u, const void* delta, const float* A, const voi
                      ss_dtype_t dtype, void* stream);
 
 constexpr int64_t kPadMinElems = 1 << 16;  // rows x steps below which ragged calls stay scalar
+constexpr int64_t kHostPieces = 8;           // host-buffer calls: pieces (batch slices or segments)
+constexpr int64_t kHostSegmentSteps = 4096;  // ... and steps per segment of a single sequence
 
 // The forward of ragged rows through padded copies (see fwd_impl): u, delta,
 // z, B and C copied into rows of seqlen rounded up to the vector, in
@@ -574,6 +576,157 @@ SS_API ss_status_t ss_selective_scan_fwd_h0(
     ss_dtype_t dtype, void* stream) {
   return fwd_impl(u, delta, A, B, C, D, z, delta_bias, delta_softplus, h0, y, last_state,
                   batch, dim, dstate, seqlen, dtype, stream);
+}
+
+SS_API ss_status_t ss_selective_scan_fwd_host(
+    const void* u, const void* delta, const float* A, const void* B, const void* C,
+    const float* D, const void* z, const float* delta_bias, int delta_softplus,
+    const float* h0, void* y, float* last_state,
+    int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
+    ss_dtype_t dtype, void* stream) {
+  // ---- validation (host arrays): nothing is enqueued or written on error ----
+  if (dtype != SS_F32 && dtype != SS_BF16) return SS_ERR_UNSUPPORTED;
+  if (!u || !delta || !A || !B || !C || !y) return SS_ERR_INVALID_ARGUMENT;
+  if (batch <= 0 || dim <= 0 || dstate <= 0 || seqlen <= 0) return SS_ERR_INVALID_ARGUMENT;
+  if (dstate > 256) return SS_ERR_UNSUPPORTED;
+  const int64_t elt = dtype == SS_F32 ? 4 : 2;
+  Sizes sz;
+  if (!sizes_ok(batch, dim, dstate, seqlen, elt, &sz)) return SS_ERR_UNSUPPORTED;
+  const uintptr_t ea = (uintptr_t)elt;
+  if (!aligned(u, ea) || !aligned(delta, ea) || !aligned(B, ea) || !aligned(C, ea) ||
+      !aligned(y, ea) || (z && !aligned(z, ea)) || !aligned(A, 4) || (D && !aligned(D, 4)) ||
+      (delta_bias && !aligned(delta_bias, 4)) || (last_state && !aligned(last_state, 4)) ||
+      (h0 && !aligned(h0, 4)))
+    return SS_ERR_INVALID_ARGUMENT;
+  const void* ins[] = {u, delta, B, C, z, A, D, delta_bias, h0};
+  const int64_t in_bytes[] = {sz.x_bytes, sz.x_bytes, sz.bc_bytes, sz.bc_bytes,
+                              z ? sz.x_bytes : 0, sz.a_elems * 4, D ? dim * 4 : 0,
+                              delta_bias ? dim * 4 : 0, h0 ? sz.st_elems * 4 : 0};
+  for (int i = 0; i < 9; ++i) {
+    if (range_overlap(y, sz.x_bytes, ins[i], in_bytes[i])) return SS_ERR_INVALID_ARGUMENT;
+    const bool in_place = i == 8 && last_state == h0;
+    if (last_state && !in_place && range_overlap(last_state, sz.st_elems * 4, ins[i], in_bytes[i]))
+      return SS_ERR_INVALID_ARGUMENT;
+  }
+  if (last_state && range_overlap(last_state, sz.st_elems * 4, y, sz.x_bytes))
+    return SS_ERR_INVALID_ARGUMENT;
+
+  // ---- pieces, two in flight: slices of the batch (contiguous in host
+  // memory, independent problems), or, for one sequence, segments of time
+  // chained through the state (strided 2-D copies) ----
+  const int64_t L = seqlen, N = dstate;
+  const bool by_batch = batch > 1;
+  int64_t npieces, nb, seg;
+  if (by_batch) {
+    npieces = std::min<int64_t>(batch, kHostPieces);
+    nb = (batch + npieces - 1) / npieces;
+    npieces = (batch + nb - 1) / nb;
+    seg = L;
+  } else {
+    const int64_t n = std::max<int64_t>(1, std::min<int64_t>(kHostPieces, L / kHostSegmentSteps));
+    seg = round_up((L + n - 1) / n, 64);
+    npieces = (L + seg - 1) / seg;
+    nb = 1;
+  }
+  const int64_t xs = round_up(nb * dim * seg * elt, 256), bcs = round_up(nb * N * seg * elt, 256);
+  const int64_t ss_bytes = round_up(nb * dim * N * 4, 256);
+  const int64_t slot_bytes = (z ? 4 : 3) * xs + 2 * bcs + ss_bytes;
+  const int64_t par_bytes = round_up(sz.a_elems * 4, 256) + 2 * round_up(dim * 4, 256);
+  const int64_t total = 2 * slot_bytes + par_bytes;
+
+  cudaStream_t sc = static_cast<cudaStream_t>(stream), sh = nullptr, sd = nullptr;
+  cudaEvent_t ev[7] = {};  // allocated, inputs in x2, scanned x2, outputs out x2
+  void* base = nullptr;
+  ss_status_t status = SS_OK;
+  auto ok = [&](cudaError_t e) {
+    if (e != cudaSuccess && status == SS_OK) status = SS_ERR_CUDA;
+    return status == SS_OK;
+  };
+  (void)cudaGetLastError();
+  ok(cudaStreamCreateWithFlags(&sh, cudaStreamNonBlocking));
+  ok(cudaStreamCreateWithFlags(&sd, cudaStreamNonBlocking));
+  for (auto& e : ev) ok(cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
+  if (status == SS_OK && ok(cudaMallocAsync(&base, (size_t)total, sc))) {
+    char* q = static_cast<char*>(base);
+    char* slot[2][7];  // u, delta, y, B, C, z, state
+    for (int s = 0; s < 2; ++s) {
+      slot[s][0] = q; q += xs;
+      slot[s][1] = q; q += xs;
+      slot[s][2] = q; q += xs;
+      slot[s][3] = q; q += bcs;
+      slot[s][4] = q; q += bcs;
+      slot[s][5] = z ? q : nullptr; if (z) q += xs;
+      slot[s][6] = q; q += ss_bytes;
+    }
+    float* Ad = reinterpret_cast<float*>(q); q += round_up(sz.a_elems * 4, 256);
+    float* Dd = D ? reinterpret_cast<float*>(q) : nullptr; q += round_up(dim * 4, 256);
+    float* bd = delta_bias ? reinterpret_cast<float*>(q) : nullptr;
+    const cudaMemcpyKind h2d = cudaMemcpyHostToDevice, d2h = cudaMemcpyDeviceToHost;
+    ok(cudaMemcpyAsync(Ad, A, sz.a_elems * 4, h2d, sc));
+    if (D) ok(cudaMemcpyAsync(Dd, D, dim * 4, h2d, sc));
+    if (delta_bias) ok(cudaMemcpyAsync(bd, delta_bias, dim * 4, h2d, sc));
+    float* chain = reinterpret_cast<float*>(slot[0][6]);  // time segments: one state, chained
+    if (!by_batch) {
+      if (h0) ok(cudaMemcpyAsync(chain, h0, sz.st_elems * 4, h2d, sc));
+      else ok(cudaMemsetAsync(chain, 0, sz.st_elems * 4, sc));
+    }
+    ok(cudaEventRecord(ev[0], sc));
+    ok(cudaStreamWaitEvent(sh, ev[0], 0));
+    // rows of `rows` host rows of L steps from step t0, `len` steps each
+    auto copy_in = [&](void* dst, const void* src, int64_t row0, int64_t rows, int64_t t0,
+                       int64_t len) {
+      const char* from = static_cast<const char*>(src) + (row0 * L + t0) * elt;
+      if (len == L) return ok(cudaMemcpyAsync(dst, from, rows * L * elt, h2d, sh));
+      return ok(cudaMemcpy2DAsync(dst, len * elt, from, L * elt, len * elt, rows, h2d, sh));
+    };
+    for (int64_t k = 0; k < npieces && status == SS_OK; ++k) {
+      const int s = (int)(k & 1);
+      const int64_t b0 = by_batch ? k * nb : 0, pb = by_batch ? std::min(nb, batch - b0) : 1;
+      const int64_t t0 = by_batch ? 0 : k * seg, len = by_batch ? L : std::min(seg, L - t0);
+      const int64_t rows = pb * dim, bc_rows = pb * N;
+      float* state = by_batch ? reinterpret_cast<float*>(slot[s][6]) : chain;
+      // inputs of piece k (its slot's previous piece is read by then)
+      if (k >= 2) ok(cudaStreamWaitEvent(sh, ev[3 + s], 0));
+      copy_in(slot[s][0], u, b0 * dim, rows, t0, len);
+      copy_in(slot[s][1], delta, b0 * dim, rows, t0, len);
+      copy_in(slot[s][3], B, b0 * N, bc_rows, t0, len);
+      copy_in(slot[s][4], C, b0 * N, bc_rows, t0, len);
+      if (z) copy_in(slot[s][5], z, b0 * dim, rows, t0, len);
+      if (by_batch && h0) ok(cudaMemcpyAsync(state, h0 + b0 * dim * N, rows * N * 4, h2d, sh));
+      ok(cudaEventRecord(ev[1 + s], sh));
+      // the scan of piece k
+      ok(cudaStreamWaitEvent(sc, ev[1 + s], 0));
+      if (k >= 2) ok(cudaStreamWaitEvent(sc, ev[5 + s], 0));  // its outputs are copied out
+      if (status != SS_OK) break;
+      status = fwd_impl(slot[s][0], slot[s][1], Ad, slot[s][3], slot[s][4], Dd, slot[s][5], bd,
+                        delta_softplus, (by_batch && !h0) ? nullptr : state, slot[s][2],
+                        (by_batch && !last_state) ? nullptr : state, pb, dim, N, len, dtype, sc);
+      ok(cudaEventRecord(ev[3 + s], sc));
+      // outputs of piece k back into their place in the host arrays
+      ok(cudaStreamWaitEvent(sd, ev[3 + s], 0));
+      char* yto = static_cast<char*>(y) + (b0 * dim * L + t0) * elt;
+      if (len == L)
+        ok(cudaMemcpyAsync(yto, slot[s][2], rows * L * elt, d2h, sd));
+      else
+        ok(cudaMemcpy2DAsync(yto, L * elt, slot[s][2], len * elt, len * elt, rows, d2h, sd));
+      if (by_batch && last_state)
+        ok(cudaMemcpyAsync(last_state + b0 * dim * N, state, rows * N * 4, d2h, sd));
+      ok(cudaEventRecord(ev[5 + s], sd));
+    }
+    if (status == SS_OK && !by_batch && last_state)
+      ok(cudaMemcpyAsync(last_state, chain, sz.st_elems * 4, d2h, sc));
+    cudaEventRecord(ev[0], sd);
+    cudaStreamWaitEvent(sc, ev[0], 0);
+    cudaEventRecord(ev[1], sh);
+    cudaStreamWaitEvent(sc, ev[1], 0);
+    cudaFreeAsync(base, sc);
+  }
+  if (cudaStreamSynchronize(sc) != cudaSuccess && status == SS_OK) status = SS_ERR_CUDA;
+  if (sh) { cudaStreamSynchronize(sh); cudaStreamDestroy(sh); }
+  if (sd) { cudaStreamSynchronize(sd); cudaStreamDestroy(sd); }
+  for (auto& e : ev)
+    if (e) cudaEventDestroy(e);
+  return status;
 }
 
 SS_API ss_status_t ss_selective_state_update(

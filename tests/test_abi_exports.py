@@ -29,7 +29,8 @@ def test_header_declares_the_entry_points():
     assert declared_functions() == ["ss_mamba2_fwd", "ss_mamba2_fwd_h0", "ss_selective_scan_bwd",
                                     "ss_selective_scan_bwd_h0", "ss_selective_scan_check",
                                     "ss_selective_scan_fwd",
-                                    "ss_selective_scan_fwd_h0", "ss_selective_scan_fwd_noalloc",
+                                    "ss_selective_scan_fwd_h0", "ss_selective_scan_fwd_host",
+                                    "ss_selective_scan_fwd_noalloc",
                                     "ss_selective_scan_fwd_pc", "ss_selective_scan_fwd_pc_h0",
                                     "ss_selective_scan_plan", "ss_selective_state_update",
                                     "ss_status_string"]
