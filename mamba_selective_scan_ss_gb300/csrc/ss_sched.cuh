@@ -122,26 +122,40 @@ __device__ __forceinline__ unsigned look_back(const unsigned* flags, int64_t M, 
 __global__ void ss_set_ticket(unsigned* ticket, unsigned first) { *ticket = first; }
 #endif
 
-template <int TGS, int TPB>
+// fp32 I/O with two lanes per row pair streams u, delta and z through
+// per-warp segments (below); every other instantiation through per-lane slots.
+template <typename T, int TGS>
+constexpr bool kSegStream = TGS == 2 && sizeof(T) == 4;
+constexpr int kSegVecs = 4;   // vectors per segment: 64 bytes of each of 32 rows
+constexpr int kSegSlots = 4;  // segments in a warp's ring
+
+// WARP_ROWS: a warp's rows are the contiguous rows [32 w, 32 w + 32) of the
+// tile, lane l owning row 32 w + l (the segment stream copies a warp's rows as
+// one block); otherwise lane pair g owns rows g and g + TPB / TGS.
+template <int TGS, int TPB, bool WARP_ROWS = false>
 struct PairRows {
   static constexpr int kRowsPerCta = 2 * TPB / TGS;
+  static_assert(!WARP_ROWS || TGS == 2, "warp rows need two lanes per row pair");
   int64_t row[2];  // slot 0: own row; slot 1: the other row of the group
   int64_t d[2];
   int rc[2];       // row index inside the tile
   bool valid[2];
   int64_t b;
+  int64_t d0;      // first channel of the tile
   int q;           // lane in group
 
   __device__ __forceinline__ PairRows(int64_t tile, int64_t dim) {
     const int64_t dtiles = (dim + kRowsPerCta - 1) / kRowsPerCta;
     b = tile / dtiles;
     const int64_t base = (tile - b * dtiles) * kRowsPerCta;
+    d0 = base;
     const int g = threadIdx.x / TGS;
     q = threadIdx.x % TGS;
 #pragma unroll
     for (int s = 0; s < 2; ++s) {
       const int which = TGS == 1 ? s : (s == 0 ? q : 1 - q);
-      rc[s] = which * (TPB / TGS) + g;
+      rc[s] = WARP_ROWS ? (int)(threadIdx.x & ~31u) + 2 * ((int)(threadIdx.x & 31u) / 2) + which
+                        : which * (TPB / TGS) + g;
       const int64_t dd = base + rc[s];
       valid[s] = dd < dim;
       d[s] = valid[s] ? dd : dim - 1;
@@ -150,7 +164,7 @@ struct PairRows {
   }
 };
 
-template <typename T, int NT, int TGS, int TPB, int STAGES>
+template <typename T, int NT, int TGS, int TPB, int STAGES, bool SEG = kSegStream<T, TGS>>
 struct PipeSmem {
   static constexpr int kOwn = 2 / TGS;
   static constexpr int kRaw = kTileSteps + 16 / (int)sizeof(T);  // padded raw row
@@ -159,13 +173,39 @@ struct PipeSmem {
   float m[2][kTileSteps][NT];         // widened, transposed B, C tile
 };
 
+// Segment stream: per warp, a ring of kSegSlots segments; a segment holds
+// kSegVecs vectors of the warp's 32 rows for u, delta and z, each row 64
+// bytes whose 16-byte vectors are XOR-permuted by (row / 2) % 4, so that both
+// the copies (two rows per 8 lanes) and the reads (8 rows per 8 lanes, one
+// vector each) touch every bank once.
+template <typename T, int NT, int TGS, int TPB, int STAGES>
+struct PipeSmem<T, NT, TGS, TPB, STAGES, true> {
+  static constexpr int kRaw = kTileSteps + 16 / (int)sizeof(T);
+  uint4 xs[TPB / 32][kSegSlots][3][32][kSegVecs];
+  T raw[2][NT][kRaw];
+  float m[2][kTileSteps][NT];
+};
+
 // The kernel's pipeline buffers, declared in a function of their own rather
 // than at kernel scope (measured: 1-2.5% faster on every workload, the fp32
 // ones most; the placement of the CTA's shared variables is the only change).
-template <class S>
+// The segment-stream layout is larger than the 48 KB of static shared memory
+// and lives in dynamic shared memory (the launch passes its size).
+template <class S, bool DYN>
 __device__ __forceinline__ S& pipe_smem() {
-  __shared__ __align__(16) S sm;
-  return sm;
+  if constexpr (DYN) {
+    extern __shared__ __align__(16) unsigned char ss_dyn_smem[];
+    return *reinterpret_cast<S*>(ss_dyn_smem);
+  } else {
+    __shared__ __align__(16) S sm;
+    return sm;
+  }
+}
+
+// Dynamic shared memory of one ss_fwd_sched instantiation (0: static only).
+template <typename T, int NT, int TGS, int TPB, int STAGES>
+constexpr int fwd_sched_dyn_smem() {
+  return kSegStream<T, TGS> ? (int)sizeof(PipeSmem<T, NT, TGS, TPB, STAGES>) : 0;
 }
 
 // One pass over steps [t_begin, t_end) of a unit: AGG = false runs the
@@ -178,10 +218,20 @@ __device__ __forceinline__ S& pipe_smem() {
 // vector j+1 (its shared-memory reads, softplus and the dt/du exchange,
 // ~150 cycles of latency) is issued before the recurrence of vector j, so
 // that latency overlaps the recurrence instead of stalling it.
+//
+// u, delta and z reach shared memory one of two ways.  Per-lane slots: each
+// lane copies the next vectors of its own row (one 16-byte copy per row and
+// tensor, 32 rows per warp instruction).  Segment stream (fp32, two lanes per
+// row pair): every kSegVecs vectors the warp copies a whole segment of its 32
+// rows, 8 rows x 64 bytes per instruction, kSegSlots - 2 segments ahead, and
+// a __syncwarp hands it to the lanes.  The per-lane form made the sweep's
+// copies cost ~17% of its time (measured by leaving them out); the segments,
+// with the same instruction count, cut the fp32 sweep by 7-8%.
 template <typename T, int NT, int TGS, int TPB, int STAGES, bool AGG, bool HAS_Z, bool MULTI>
 __device__ __forceinline__ void scan_pass(const FwdParams& p,
                                           PipeSmem<T, NT, TGS, TPB, STAGES>& sm,
-                                          const PairRows<TGS, TPB>& rs, int64_t t_begin,
+                                          const PairRows<TGS, TPB, kSegStream<T, TGS>>& rs,
+                                          int64_t t_begin,
                                           int64_t t_end, f2 (&h)[2][NT / TGS / 2],
                                           const f2 (&A2)[2][NT / TGS / 2],
                                           const float (&bias)[2 / TGS],
@@ -197,6 +247,12 @@ __device__ __forceinline__ void scan_pass(const FwdParams& p,
   constexpr int CPR = kTileSteps * (int)sizeof(T) / 16;  // 16-byte chunks per state row
   constexpr int EPC = 16 / (int)sizeof(T);                // elements per 16-byte chunk
   static_assert(STAGES >= 3 && STAGES <= VPT + 1, "pipeline depth must fit in a tile");
+  constexpr bool SEG = kSegStream<T, TGS>;
+  constexpr int SV = kSegVecs, SR = kSegSlots;
+  // the raw B/C copies of a tile join the copy group of the first segment
+  // issued after the tile boundary, which is waited for (SR - 1) * SV vectors
+  // later: that must come before the next tile boundary
+  static_assert(!SEG || ((SR - 1) * SV <= VPT && SR >= 3), "segment ring too deep for the B/C tile");
 
   const int tid = threadIdx.x;
   const int64_t L = p.seqlen, N = p.dstate;
@@ -212,6 +268,7 @@ __device__ __forceinline__ void scan_pass(const FwdParams& p,
   const bool use_softplus = p.softplus != 0;
 
   auto issue_vec = [&](int64_t j) {
+    if constexpr (!SEG) {
     if (j < nvec) {
       const int slot = (int)(j % STAGES);
       const int64_t t = t_begin + j * V;
@@ -224,6 +281,41 @@ __device__ __forceinline__ void scan_pass(const FwdParams& p,
       }
     }
     cp_async_commit();
+    }
+  };
+  // segment stream: lane l copies vector l % SV of rows (32 i + l) / SV of the
+  // warp (i < SV); rows past dim read the last channel (never stored)
+  const int lane = tid & 31, wp = tid >> 5;
+  int64_t seg_row[SEG ? SV : 1];
+  if constexpr (SEG) {
+#pragma unroll
+    for (int i = 0; i < SV; ++i) {
+      const int64_t dd = rs.d0 + wp * 32 + (i * 32 + lane) / SV;
+      seg_row[i] = (rs.b * p.dim + (dd < p.dim ? dd : p.dim - 1)) * L;
+    }
+  }
+  auto seg_pos = [](int row, int c) { return c ^ ((row >> 1) & 3); };  // 16-byte slot of vector c
+  auto issue_seg = [&](int64_t sg) {
+    if constexpr (SEG) {
+      const int64_t v0 = sg * SV;
+      if (v0 < nvec) {
+        const int slot = (int)(sg % SR);
+        const int64_t t = t_begin + v0 * V;
+        const int c = lane % SV;
+#pragma unroll
+        for (int i = 0; i < SV; ++i) {
+          const int r = (i * 32 + lane) / SV;
+          if (v0 + c < nvec) {
+            const int64_t off = seg_row[i] + t + c * V;
+            const int pc = seg_pos(r, c);
+            cp_async16(&sm.xs[wp][slot][0][r][pc], ug + off);
+            cp_async16(&sm.xs[wp][slot][1][r][pc], dg + off);
+            if (GATE) cp_async16(&sm.xs[wp][slot][2][r][pc], zg + off);
+          }
+        }
+      }
+      cp_async_commit();
+    }
   };
   auto issue_tile = [&](int64_t t0) {
     if (t0 >= t_end) return;
@@ -249,13 +341,20 @@ __device__ __forceinline__ void scan_pass(const FwdParams& p,
   f2 up[OWN][VP], zp[OWN][VP];  // own u (skip) and z (gate)
   auto rowwork = [&](int64_t j, float (&dt_o)[2][V], float (&du_o)[2][V], f2 (&u_o)[OWN][VP],
                      f2 (&z_o)[OWN][VP]) {
-    const int slot = (int)(j % STAGES);
 #pragma unroll
     for (int o = 0; o < OWN; ++o) {
       f2 dp[VP];
-      to_pairs<T>(*reinterpret_cast<const uint4*>(&sm.x[slot][0][o][tid]), u_o[o]);
-      to_pairs<T>(*reinterpret_cast<const uint4*>(&sm.x[slot][1][o][tid]), dp);
-      if (GATE) to_pairs<T>(*reinterpret_cast<const uint4*>(&sm.x[slot][2][o][tid]), z_o[o]);
+      if constexpr (SEG) {
+        const int slot = (int)((j / SV) % SR), c = seg_pos(lane, (int)(j % SV));
+        to_pairs<T>(sm.xs[wp][slot][0][lane][c], u_o[o]);
+        to_pairs<T>(sm.xs[wp][slot][1][lane][c], dp);
+        if (GATE) to_pairs<T>(sm.xs[wp][slot][2][lane][c], z_o[o]);
+      } else {
+        const int slot = (int)(j % STAGES);
+        to_pairs<T>(*reinterpret_cast<const uint4*>(&sm.x[slot][0][o][tid]), u_o[o]);
+        to_pairs<T>(*reinterpret_cast<const uint4*>(&sm.x[slot][1][o][tid]), dp);
+        if (GATE) to_pairs<T>(*reinterpret_cast<const uint4*>(&sm.x[slot][2][o][tid]), z_o[o]);
+      }
 #pragma unroll
       for (int m = 0; m < VP; ++m) {
         const f2 x = add2(dp[m], splat(bias[o]));
@@ -277,17 +376,36 @@ __device__ __forceinline__ void scan_pass(const FwdParams& p,
   };
 
   issue_tile(t_begin);
+  if constexpr (SEG) {
 #pragma unroll
-  for (int s = 0; s < STAGES - 1; ++s) issue_vec(s);
-  cp_async_wait<STAGES - 2>();  // vector 0 landed
+    for (int sg = 0; sg < SR - 1; ++sg) issue_seg(sg);
+    cp_async_wait<SR - 2>();  // this lane's copies of segment 0 landed
+    __syncwarp();             // ... and every lane's
+  } else {
+#pragma unroll
+    for (int s = 0; s < STAGES - 1; ++s) issue_vec(s);
+    cp_async_wait<STAGES - 2>();  // vector 0 landed
+  }
   rowwork(0, dts, dus, up, zp);
 
   // unrolled by two so that the hand-over of the next vector's row work
   // (dts_n -> dts, ...) becomes register renaming instead of moves
 #pragma unroll 2
   for (int64_t j = 0; j < nvec; ++j) {
-    issue_vec(j + STAGES - 1);
-    cp_async_wait<STAGES - 2>();  // this lane's copies of vector j+1 (and older) landed
+    if constexpr (SEG) {
+      if ((j % SV) == SV - 1 && j + 1 < nvec) {
+        // vector j+1 opens segment ns: copy segment ns + SR - 2 into the slot of
+        // segment ns - 2 (every lane passed the last __syncwarp after reading
+        // it), then wait for segment ns and hand it to the lanes
+        const int64_t ns = (j + 1) / SV;
+        issue_seg(ns + SR - 2);
+        cp_async_wait<SR - 2>();
+        __syncwarp();
+      }
+    } else {
+      issue_vec(j + STAGES - 1);
+      cp_async_wait<STAGES - 2>();  // this lane's copies of vector j+1 (and older) landed
+    }
     const int jt = (int)(j % VPT) * V;
     if (jt == 0) {
       // tile boundary: widen + transpose the raw tile, then prefetch the next one
@@ -440,10 +558,11 @@ __global__ void __launch_bounds__(TPB) ss_fwd_sched(const FwdParams p) {
   constexpr int G = NT / TGS;
   constexpr int GP = G / 2;
   constexpr int OWN = 2 / TGS;
-  constexpr int RPC = PairRows<TGS, TPB>::kRowsPerCta;
+  constexpr bool SEG = kSegStream<T, TGS>;
+  constexpr int RPC = PairRows<TGS, TPB, SEG>::kRowsPerCta;
   static_assert(TGS == 1 || TGS == 2, "one or two lanes per row pair");
   static_assert(G % 4 == 0, "a lane holds a multiple of four states");
-  PipeSmem<T, NT, TGS, TPB, STAGES>& sm = pipe_smem<PipeSmem<T, NT, TGS, TPB, STAGES>>();
+  PipeSmem<T, NT, TGS, TPB, STAGES>& sm = pipe_smem<PipeSmem<T, NT, TGS, TPB, STAGES>, SEG>();
   __shared__ unsigned s_ticket, s_flag;
 
   const int tid = threadIdx.x;
@@ -460,7 +579,7 @@ __global__ void __launch_bounds__(TPB) ss_fwd_sched(const FwdParams p) {
     if (t >= units) break;
     const int k = (int)(t / M);
     const int64_t tile = t - (int64_t)k * M;
-    const PairRows<TGS, TPB> rs(tile, p.dim);
+    const PairRows<TGS, TPB, SEG> rs(tile, p.dim);
     const int nl0 = rs.q * G;
     const int64_t t_begin = (int64_t)k * p.chunk_len;
     const int64_t t_end = min(L, t_begin + p.chunk_len);
