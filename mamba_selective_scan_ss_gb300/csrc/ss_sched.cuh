@@ -194,7 +194,7 @@ struct PipeSmem<T, NT, TGS, TPB, STAGES, true> {
 template <class S, bool DYN>
 __device__ __forceinline__ S& pipe_smem() {
   if constexpr (DYN) {
-    extern __shared__ __align__(16) unsigned char ss_dyn_smem[];
+    extern __shared__ __align__(1024) unsigned char ss_dyn_smem[];
     return *reinterpret_cast<S*>(ss_dyn_smem);
   } else {
     __shared__ __align__(16) S sm;
