@@ -334,12 +334,22 @@ cudaError_t dispatch(const ss::FwdParams& p, const LaunchPlan& plan, cudaStream_
 }
 
 // The per-channel kernel for the given gate, vector-path and row-width choices.
+// One CTA per SM (registers), so a launch is ceil(CTAs / SMs) waves whose
+// length is set by the row work per CTA.  Rows of up to 32 lanes take CTAs of
+// 7 warps instead of 8 when that costs no extra wave: less work per wave for
+// the same count (measured on 8 x 5120 rows of 16 states: 5 waves either way,
+// 0.441 against 0.457 ms; 6 or 5 warps per CTA were slower, 0.493 / 0.560).
 template <typename T>
-void pc_launch(const ss::PcParams& p, bool has_z, bool vec, unsigned grid, cudaStream_t st) {
+void pc_launch(const ss::PcParams& p, bool has_z, bool vec, int sms, cudaStream_t st) {
   const bool wide = p.seg_shift > 5;
+  const int64_t threads = p.rows << p.seg_shift;
+  const int64_t nsm = std::max(sms, 1);
+  auto waves = [&](int64_t block) { return ((threads + block - 1) / block + nsm - 1) / nsm; };
+  const int block = (!wide && waves(224) <= waves(256)) ? 224 : 256;
+  const unsigned grid = (unsigned)((threads + block - 1) / block);
   auto go = [&](auto z, auto v, auto w) {
     ss::ss_fwd_pc<T, decltype(z)::value, decltype(v)::value, decltype(w)::value>
-        <<<grid, 256, 0, st>>>(p);
+        <<<grid, block, 0, st>>>(p);
   };
   using F = std::false_type;
   using U = std::true_type;
@@ -831,11 +841,25 @@ ss_status_t bwd_impl(const void* u, const void* delta, const float* A, const voi
   if (!sizes_ok(batch, dim, dstate, seqlen, elt, &sz)) return SS_ERR_UNSUPPORTED;
   const int groups = (int)((dstate + ss::kBwdLanes - 1) / ss::kBwdLanes);
   const int64_t npad = (int64_t)groups * ss::kBwdLanes;
-  const int64_t dtiles = (dim + ss::kBwdRows - 1) / ss::kBwdRows;
+  // rows per CTA: the main kernel runs in one wave of CTAs whose rows all take
+  // the same time, so the SM with the most rows sets the makespan; one state
+  // group takes 96-row CTAs when that lowers the most rows an SM holds (the
+  // Mamba-2.8B layer's 40960 rows: 3 x 96 = 288 against 5 x 64 = 320, measured
+  // 3.10 against 3.33 ms), else 64 (fewer rows than SMs x 64 fill more SMs
+  // with the smaller CTAs: the Mamba-130M layer's 3072 rows, 1.62 against 1.94 ms)
+  const int64_t nsm = std::max(1, sm_count());
+  auto most_rows = [&](int64_t r) {
+    const int64_t c = batch * ((dim + r - 1) / r);
+    return (c + nsm - 1) / nsm * r;
+  };
+  const int64_t bwd_rows =
+      (groups == 1 && most_rows(ss::kBwdRowsWide) < most_rows(ss::kBwdRows)) ? ss::kBwdRowsWide
+                                                                              : ss::kBwdRows;
+  const int64_t dtiles = (dim + bwd_rows - 1) / bwd_rows;
   const int64_t ctas = batch * dtiles;
   const int64_t nblk = (seqlen + ss::kBwdBlock - 1) / ss::kBwdBlock;
   int64_t ck_elems, bc_elems, row_elems = 0, tmp;
-  if (!mul_ok(ctas * ss::kBwdRows * ss::kBwdLanes, nblk, &ck_elems) ||
+  if (!mul_ok(ctas * bwd_rows * ss::kBwdLanes, nblk, &ck_elems) ||
       !mul_ok(ctas * 2 * npad, seqlen, &bc_elems) || !mul_ok(ck_elems + bc_elems, 4, &tmp) ||
       (groups > 1 && !mul_ok(3 * sz.rows, seqlen, &row_elems)) || ctas > INT_MAX)
     return SS_ERR_UNSUPPORTED;
@@ -906,29 +930,47 @@ ss_status_t bwd_impl(const void* u, const void* delta, const float* A, const voi
                    (const void*)ss::ss_bwd_main<__nv_bfloat16, true, true>,
                    (const void*)ss::ss_bwd_main<__nv_bfloat16, false, true>})
       cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    for (auto k : {(const void*)ss::ss_bwd_main<float, true, false, ss::kBwdRowsWide>,
+                   (const void*)ss::ss_bwd_main<float, false, false, ss::kBwdRowsWide>,
+                   (const void*)ss::ss_bwd_main<__nv_bfloat16, true, false, ss::kBwdRowsWide>,
+                   (const void*)ss::ss_bwd_main<__nv_bfloat16, false, false, ss::kBwdRowsWide>}) {
+      cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+      cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)sizeof(ss::BwdSmem<ss::kBwdRowsWide>));
+    }
     return true;
   }();
   (void)carveout;
   (void)cudaGetLastError();
   const unsigned grid = (unsigned)ctas;
+  constexpr int kR = ss::kBwdRows, kW = ss::kBwdRowsWide;
+  constexpr unsigned kWideSmem = sizeof(ss::BwdSmem<ss::kBwdRowsWide>);
   for (int g = 0; g < groups; ++g) {
     p.group = g;
     p.final_group = g == groups - 1;
-    if (groups == 1) {
+    if (groups == 1 && bwd_rows == kW) {
       if (dtype == SS_F32) {
-        if (z) ss::ss_bwd_main<float, true, false><<<grid, ss::kBwdThreads, 0, st>>>(p);
-        else ss::ss_bwd_main<float, false, false><<<grid, ss::kBwdThreads, 0, st>>>(p);
+        if (z) ss::ss_bwd_main<float, true, false, kW><<<grid, kW, kWideSmem, st>>>(p);
+        else ss::ss_bwd_main<float, false, false, kW><<<grid, kW, kWideSmem, st>>>(p);
       } else {
-        if (z) ss::ss_bwd_main<__nv_bfloat16, true, false><<<grid, ss::kBwdThreads, 0, st>>>(p);
-        else ss::ss_bwd_main<__nv_bfloat16, false, false><<<grid, ss::kBwdThreads, 0, st>>>(p);
+        if (z) ss::ss_bwd_main<__nv_bfloat16, true, false, kW><<<grid, kW, kWideSmem, st>>>(p);
+        else ss::ss_bwd_main<__nv_bfloat16, false, false, kW><<<grid, kW, kWideSmem, st>>>(p);
+      }
+    } else if (groups == 1) {
+      if (dtype == SS_F32) {
+        if (z) ss::ss_bwd_main<float, true, false><<<grid, kR, 0, st>>>(p);
+        else ss::ss_bwd_main<float, false, false><<<grid, kR, 0, st>>>(p);
+      } else {
+        if (z) ss::ss_bwd_main<__nv_bfloat16, true, false><<<grid, kR, 0, st>>>(p);
+        else ss::ss_bwd_main<__nv_bfloat16, false, false><<<grid, kR, 0, st>>>(p);
       }
     } else {
       if (dtype == SS_F32) {
-        if (z) ss::ss_bwd_main<float, true, true><<<grid, ss::kBwdThreads, 0, st>>>(p);
-        else ss::ss_bwd_main<float, false, true><<<grid, ss::kBwdThreads, 0, st>>>(p);
+        if (z) ss::ss_bwd_main<float, true, true><<<grid, kR, 0, st>>>(p);
+        else ss::ss_bwd_main<float, false, true><<<grid, kR, 0, st>>>(p);
       } else {
-        if (z) ss::ss_bwd_main<__nv_bfloat16, true, true><<<grid, ss::kBwdThreads, 0, st>>>(p);
-        else ss::ss_bwd_main<__nv_bfloat16, false, true><<<grid, ss::kBwdThreads, 0, st>>>(p);
+        if (z) ss::ss_bwd_main<__nv_bfloat16, true, true><<<grid, kR, 0, st>>>(p);
+        else ss::ss_bwd_main<__nv_bfloat16, false, true><<<grid, kR, 0, st>>>(p);
       }
     }
   }
@@ -1109,15 +1151,15 @@ SS_API ss_status_t ss_selective_scan_fwd_pc_h0(
   const int quads = (int)((dstate + 3) / 4);
   p.seg_shift = 0;
   while ((1 << p.seg_shift) < quads) ++p.seg_shift;
-  const int64_t blocks = ((p.rows << p.seg_shift) + 255) / 256;
+  const int64_t blocks = ((p.rows << p.seg_shift) + 223) / 224;  // the smaller CTA size
   if (blocks > INT_MAX) return SS_ERR_UNSUPPORTED;
   const bool vec = seqlen % (32 / elt) == 0 && aligned(u, 32) && aligned(delta, 32) &&
                    aligned(B, 32) && aligned(C, 32) && aligned(y, 16) && (!z || aligned(z, 32));
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   (void)cudaGetLastError();
-  const unsigned g = (unsigned)blocks;
-  if (dtype == SS_F32) pc_launch<float>(p, z != nullptr, vec, g, st);
-  else pc_launch<__nv_bfloat16>(p, z != nullptr, vec, g, st);
+  const int sms = sm_count();
+  if (dtype == SS_F32) pc_launch<float>(p, z != nullptr, vec, sms, st);
+  else pc_launch<__nv_bfloat16>(p, z != nullptr, vec, sms, st);
   return cudaGetLastError() == cudaSuccess ? SS_OK : SS_ERR_CUDA;
 }
 

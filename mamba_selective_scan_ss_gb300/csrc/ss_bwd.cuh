@@ -54,10 +54,18 @@
 namespace ss {
 
 constexpr int kBwdBlock = 8;       // steps per recomputed block (and checkpoint spacing)
-constexpr int kBwdRows = 64;       // rows per CTA (one thread each)
+constexpr int kBwdRows = 64;       // rows per CTA (one thread each); ...
+constexpr int kBwdRowsWide = 96;   // ... or 96 when the rows are many (see bwd_rows_per_cta)
 constexpr int kBwdLanes = 16;      // states per group (dstate <= 16)
-constexpr int kBwdThreads = kBwdRows;
 constexpr int kBwdMinBlocks = 5;  // resident CTAs per SM the register budget is sized for
+
+// Resident CTAs per SM each instantiation's register budget is sized for: 64-row
+// CTAs five (bf16, one state group) or four; 96-row CTAs three or two (the same
+// warps per scheduler).
+template <typename T, bool MULTI, int ROWS>
+constexpr int bwd_min_blocks() {
+  return (ROWS == kBwdRows ? kBwdMinBlocks : 3) - ((sizeof(T) == 2 && !MULTI) ? 0 : 1);
+}
 
 struct BwdParams {
   const void* u;
@@ -74,7 +82,7 @@ struct BwdParams {
   void* du;             // [b,d,L] dtype
   void* ddelta;         // [b,d,L] dtype
   void* dz;             // [b,d,L] dtype (z present)
-  float* ckpt;          // [ctas][nblk][16][64] states at the end of each block
+  float* ckpt;          // [ctas][nblk][16][rows per CTA] states at the end of each block
   float* part_bc;       // [ctas][2][npad][L] per-CTA sums of dB, dC
   float* part_a;        // [b][d][npad] per-row sums of dA
   float* part_dd;       // [b][d][2] per-row sums of dD, dbias
@@ -90,7 +98,7 @@ struct BwdParams {
   int npad;             // groups * 16: state stride of part_a and part_bc
   int final_group;      // 1: this launch completes the row sums and writes the row outputs
   int64_t batch, dim, dstate, seqlen;
-  int64_t dtiles;       // CTAs per batch row: ceil(dim / 64)
+  int64_t dtiles;       // CTAs per batch row: ceil(dim / rows per CTA)
   int64_t nblk;         // ceil(seqlen / kBwdBlock)
   int vec;              // rows 16-byte aligned: a block's row values load as 16-byte vectors
 };
@@ -193,15 +201,17 @@ __device__ __forceinline__ int red_at(int r, int group) { return r * kBwdTable +
 // B (and C) values of one block, kBwdBlock steps of every state, loaded one
 // block ahead by the CTA's threads together (element i of the block: tensor
 // i / (NT S), state (i / S) % NT, step i % S), as I/O-dtype bits.
-template <typename T, int TENSORS>
+template <typename T, int TENSORS, int THREADS>
 struct BcBlk {
-  static constexpr int kPer = TENSORS * kBwdLanes * kBwdBlock / kBwdThreads;
+  static constexpr int kTot = TENSORS * kBwdLanes * kBwdBlock;
+  static constexpr int kPer = (kTot + THREADS - 1) / THREADS;
   uint32_t w[kPer];
   __device__ __forceinline__ void load(const T* Bg, const T* Cg, int64_t L, int64_t N, int64_t t0,
                                        int cnt, int tid) {
 #pragma unroll
     for (int j = 0; j < kPer; ++j) {
-      const int i = tid + j * kBwdThreads;
+      const int i = tid + j * THREADS;
+      if (kTot % THREADS != 0 && i >= kTot) continue;
       const int m = i / (kBwdLanes * kBwdBlock), n = (i / kBwdBlock) % kBwdLanes,
                 st = i % kBwdBlock;
       const T* src = m == 0 ? Bg : Cg;
@@ -212,7 +222,8 @@ struct BcBlk {
   __device__ __forceinline__ void put(float (*bc)[kBwdBlock][kBwdLanes], int tid) const {
 #pragma unroll
     for (int j = 0; j < kPer; ++j) {
-      const int i = tid + j * kBwdThreads;
+      const int i = tid + j * THREADS;
+      if (kTot % THREADS != 0 && i >= kTot) continue;
       const int m = i / (kBwdLanes * kBwdBlock), n = (i / kBwdBlock) % kBwdLanes,
                 st = i % kBwdBlock;
       bc[m][st][n] = std::is_same<T, float>::value ? __uint_as_float(w[j]) : __uint_as_float(w[j] << 16);
@@ -232,19 +243,45 @@ __device__ __forceinline__ void block_dt(const RowBlk<T>& x, float bias, bool so
   }
 }
 
-template <typename T, bool HAS_Z, bool MULTI>
-__global__ void __launch_bounds__(kBwdThreads, (sizeof(T) == 2 && !MULTI) ? kBwdMinBlocks : kBwdMinBlocks - 1) ss_bwd_main(const BwdParams p) {
+// The kernel's shared buffers for CTAs of ROWS rows.
+template <int ROWS>
+struct BwdSmem {
+  float bc[2][2][kBwdBlock][kBwdLanes];                 // B, C of a block's steps (two buffers)
+  f2 hp[kBwdBlock][kBwdLanes / 2][ROWS];                // state before each step of the block
+  float red[ROWS * kBwdTable];                          // one step's dC, dB per row
+  float wpart[ROWS / 32][kBwdBlock][kBwdTable];         // the block's per-warp dC/dB sums
+};
+
+// 64-row CTAs keep their 44 KB in static shared memory; the 66 KB of 96-row CTAs
+// exceed the static limit and come as dynamic shared memory (the launch passes
+// sizeof(BwdSmem<96>)).
+template <int ROWS>
+__device__ __forceinline__ BwdSmem<ROWS>& bwd_smem() {
+  if constexpr (ROWS == kBwdRows) {
+    __shared__ __align__(16) BwdSmem<ROWS> sm;
+    return sm;
+  } else {
+    extern __shared__ __align__(1024) unsigned char bwd_dyn_smem[];
+    return *reinterpret_cast<BwdSmem<ROWS>*>(bwd_dyn_smem);
+  }
+}
+
+template <typename T, bool HAS_Z, bool MULTI, int ROWS = kBwdRows>
+__global__ void __launch_bounds__(ROWS, bwd_min_blocks<T, MULTI, ROWS>()) ss_bwd_main(const BwdParams p) {
+  static_assert(ROWS % 32 == 0, "whole warps of rows");
   constexpr int S = kBwdBlock, NT = kBwdLanes, NP = NT / 2;
-  __shared__ __align__(16) float bc[2][2][S][NT];      // B, C of a block's steps (two buffers)
-  __shared__ f2 hp[S][NP][kBwdRows];                   // state before each step of the block
-  __shared__ __align__(16) float red[kBwdRows * kBwdTable];  // one step's dC, dB per row
-  __shared__ float wpart[kBwdRows / 32][S][kBwdTable];  // the block's per-warp dC/dB sums
+  constexpr int kThreads = ROWS;
+  BwdSmem<ROWS>& sm = bwd_smem<ROWS>();
+  auto& bc = sm.bc;
+  auto& hp = sm.hp;
+  auto& red = sm.red;
+  auto& wpart = sm.wpart;
 
   const int tid = threadIdx.x;
   const int lane = tid & 31, warp = tid >> 5;
   const int64_t cta = blockIdx.x;
   const int64_t b = cta / p.dtiles;
-  const int64_t d = (cta - b * p.dtiles) * kBwdRows + tid;
+  const int64_t d = (cta - b * p.dtiles) * ROWS + tid;
   const bool valid = d < p.dim;
   const int64_t dc = valid ? d : p.dim - 1;
   const int64_t L = p.seqlen, N = p.dstate;
@@ -268,7 +305,7 @@ __global__ void __launch_bounds__(kBwdThreads, (sizeof(T) == 2 && !MULTI) ? kBwd
   const float bias = p.bias ? p.bias[dc] : 0.f;
   const float Dd = p.D ? p.D[dc] : 0.f;
   auto ck = [&](int64_t blk, int n) -> float& {
-    return p.ckpt[((cta * p.nblk + blk) * NT + n) * kBwdRows + tid];
+    return p.ckpt[((cta * p.nblk + blk) * NT + n) * ROWS + tid];
   };
   auto count = [&](int64_t blk) { return (int)min((int64_t)S, L - blk * S); };
   const bool vec = p.vec != 0;
@@ -280,7 +317,7 @@ __global__ void __launch_bounds__(kBwdThreads, (sizeof(T) == 2 && !MULTI) ? kBwd
 #pragma unroll
     for (int k = 0; k < NP; ++k) h[k] = pack(h0_of(2 * k), h0_of(2 * k + 1));
     RowBlk<T> xn, un;
-    BcBlk<T, 1> bn;
+    BcBlk<T, 1, kThreads> bn;
     xn.load(dg, 0, count(0), vec);
     un.load(ug, 0, count(0), vec);
     bn.load(Bg, Cg, L, NG, 0, count(0), tid);
@@ -334,7 +371,7 @@ __global__ void __launch_bounds__(kBwdThreads, (sizeof(T) == 2 && !MULTI) ? kBwd
   }
   float dD_acc = 0.f, dbias_acc = 0.f;
   RowBlk<T> xn{}, un{}, yn{}, zn{};
-  BcBlk<T, 2> bn;
+  BcBlk<T, 2, kThreads> bn;
   float hn[NT];  // checkpoint the next block's recompute starts from
   auto load_ckpt = [&](int64_t blk) {  // the state entering block blk
 #pragma unroll
@@ -510,12 +547,12 @@ __global__ void __launch_bounds__(kBwdThreads, (sizeof(T) == 2 && !MULTI) ? kBwd
     }
     // the block's dB/dC: the two warps' sums added, step by step
     __syncthreads();
-    for (int idx = tid; idx < S * kBwdTable; idx += kBwdThreads) {
+    for (int idx = tid; idx < S * kBwdTable; idx += kThreads) {
       const int st = idx / kBwdTable, k = idx - st * kBwdTable;
       if (st < cnt) {
         float v = 0.f;
 #pragma unroll
-        for (int w = 0; w < kBwdRows / 32; ++w) v += wpart[w][st][k];
+        for (int w = 0; w < ROWS / 32; ++w) v += wpart[w][st][k];
         const int m = k < NT ? 1 : 0, nn = k & (NT - 1);
         p.part_bc[((cta * 2 + m) * p.npad + ng0 + nn) * L + t0 + st] = v;
       }

@@ -101,7 +101,8 @@ struct PcStep {
   PcVec<T, VEC> u, x, z, b[4], c[4];
 };
 
-// grid = ceil(rows * 2^seg_shift / 256), block = 256.  VEC: seqlen a multiple
+// grid = ceil(rows * 2^seg_shift / block); block = 256 for WIDE (four rows of
+// 64 lanes), else any multiple of 32 up to 256.  VEC: seqlen a multiple
 // of kPcSteps and every input row 32-byte aligned (y 16-byte aligned).  WIDE:
 // 64 lanes per row (seg_shift 6, dstate up to 256).
 template <typename T, bool HAS_Z, bool VEC, bool WIDE>
