@@ -95,6 +95,16 @@ def test_backward_matches_oracle(orc, dtype, shape):
     run_case(orc, W(*shape, dtype=dtype, seed=71))
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("with_h0", [False, True])
+def test_backward_96_row_ctas(orc, dtype, with_h0):
+    """2 x 5120 rows: 160 CTAs of 64 rows would put two on some SMs of a 152-SM
+    GPU, 108 CTAs of 96 rows one on each, so the launch takes 96-row CTAs (the
+    last tile of each batch row 32 rows short, the last block of steps 4 short);
+    every gradient against the oracle."""
+    run_case(orc, W(2, 5120, 16, 100, dtype=dtype, seed=73), with_h0=with_h0, with_dlast=with_h0)
+
+
 @pytest.mark.parametrize("dstate", [1, 2, 4, 7, 8, 12, 16, 17, 24, 32, 33, 64])
 def test_backward_dstate(orc, dstate):
     """Up to 16 states in one group; above, groups of 16 whose row sums
