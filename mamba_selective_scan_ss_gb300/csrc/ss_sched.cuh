@@ -122,12 +122,17 @@ __device__ __forceinline__ unsigned look_back(const unsigned* flags, int64_t M, 
 __global__ void ss_set_ticket(unsigned* ticket, unsigned first) { *ticket = first; }
 #endif
 
-// fp32 I/O with two lanes per row pair streams u, delta and z through
-// per-warp segments (below); every other instantiation through per-lane slots.
+// Two lanes per row pair (8 or 16 states) stream u, delta and z through
+// per-warp segments (below); four states per row pair through per-lane slots.
 template <typename T, int TGS>
-constexpr bool kSegStream = TGS == 2 && sizeof(T) == 4;
-constexpr int kSegVecs = 4;   // vectors per segment: 64 bytes of each of 32 rows
-constexpr int kSegSlots = 4;  // segments in a warp's ring
+constexpr bool kSegStream = TGS == 2;
+// vectors per segment: fp32 4 (64 bytes of each of 32 rows), bf16 2 (32
+// bytes); segments in a warp's ring: 4.  (The bf16 tile of B/C holds 8
+// vectors, and a tile's raw copies ride in a segment's copy group, which bounds
+// (slots - 1) x vectors by the tile.)
+template <typename T>
+constexpr int kSegVecs = sizeof(T) == 4 ? 4 : 2;
+constexpr int kSegSlots = 4;
 
 // WARP_ROWS: a warp's rows are the contiguous rows [32 w, 32 w + 32) of the
 // tile, lane l owning row 32 w + l (the segment stream copies a warp's rows as
@@ -174,14 +179,14 @@ struct PipeSmem {
 };
 
 // Segment stream: per warp, a ring of kSegSlots segments; a segment holds
-// kSegVecs vectors of the warp's 32 rows for u, delta and z, each row 64
-// bytes whose 16-byte vectors are XOR-permuted by (row / 2) % 4, so that both
-// the copies (two rows per 8 lanes) and the reads (8 rows per 8 lanes, one
-// vector each) touch every bank once.
+// kSegVecs vectors of the warp's 32 rows for u, delta and z, each row 64 (fp32)
+// or 32 (bf16) bytes whose 16-byte vectors are XOR-permuted by (row / 2) % 4 or
+// (row / 4) % 2, so that both the copies (two or four rows per 8 lanes) and
+// the reads (8 rows per 8 lanes, one vector each) touch every bank once.
 template <typename T, int NT, int TGS, int TPB, int STAGES>
 struct PipeSmem<T, NT, TGS, TPB, STAGES, true> {
   static constexpr int kRaw = kTileSteps + 16 / (int)sizeof(T);
-  uint4 xs[TPB / 32][kSegSlots][3][32][kSegVecs];
+  uint4 xs[TPB / 32][kSegSlots][3][32][kSegVecs<T>];
   T raw[2][NT][kRaw];
   float m[2][kTileSteps][NT];
 };
@@ -221,12 +226,13 @@ constexpr int fwd_sched_dyn_smem() {
 //
 // u, delta and z reach shared memory one of two ways.  Per-lane slots: each
 // lane copies the next vectors of its own row (one 16-byte copy per row and
-// tensor, 32 rows per warp instruction).  Segment stream (fp32, two lanes per
-// row pair): every kSegVecs vectors the warp copies a whole segment of its 32
-// rows, 8 rows x 64 bytes per instruction, kSegSlots - 2 segments ahead, and
-// a __syncwarp hands it to the lanes.  The per-lane form made the sweep's
-// copies cost ~17% of its time (measured by leaving them out); the segments,
-// with the same instruction count, cut the fp32 sweep by 7-8%.
+// tensor, 32 rows per warp instruction).  Segment stream (two lanes per row
+// pair): every kSegVecs vectors the warp copies a whole segment of its 32
+// rows, 8 rows x 64 bytes (fp32) or 16 rows x 32 bytes (bf16) per
+// instruction, kSegSlots - 2 segments ahead, and a __syncwarp hands it to the
+// lanes.  The per-lane form made the fp32 sweep's copies cost ~17% of its time
+// (measured by leaving them out); the segments, with the same instruction
+// count, cut the fp32 sweep by 7-8% and the bf16 layers by about 2%.
 template <typename T, int NT, int TGS, int TPB, int STAGES, bool AGG, bool HAS_Z, bool MULTI>
 __device__ __forceinline__ void scan_pass(const FwdParams& p,
                                           PipeSmem<T, NT, TGS, TPB, STAGES>& sm,
@@ -248,7 +254,7 @@ __device__ __forceinline__ void scan_pass(const FwdParams& p,
   constexpr int EPC = 16 / (int)sizeof(T);                // elements per 16-byte chunk
   static_assert(STAGES >= 3 && STAGES <= VPT + 1, "pipeline depth must fit in a tile");
   constexpr bool SEG = kSegStream<T, TGS>;
-  constexpr int SV = kSegVecs, SR = kSegSlots;
+  constexpr int SV = kSegVecs<T>, SR = kSegSlots;
   // the raw B/C copies of a tile join the copy group of the first segment
   // issued after the tile boundary, which is waited for (SR - 1) * SV vectors
   // later: that must come before the next tile boundary
@@ -294,7 +300,9 @@ __device__ __forceinline__ void scan_pass(const FwdParams& p,
       seg_row[i] = (rs.b * p.dim + (dd < p.dim ? dd : p.dim - 1)) * L;
     }
   }
-  auto seg_pos = [](int row, int c) { return c ^ ((row >> 1) & 3); };  // 16-byte slot of vector c
+  auto seg_pos = [](int row, int c) {  // 16-byte slot of vector c in row's segment
+    return SV == 4 ? (c ^ ((row >> 1) & 3)) : (c ^ ((row >> 2) & 1));
+  };
   auto issue_seg = [&](int64_t sg) {
     if constexpr (SEG) {
       const int64_t v0 = sg * SV;
