@@ -46,7 +46,10 @@ def close(got, ref, dtype, what, slack=0.0):
 
 
 # Relative error per step of an fp32 state update with the approximate ex2:
-# 2^-22 for the exponential and 2^-23 for the products and sums, rounded up.
+# about 2^-22 for the exponential (the kernels' decays come from the MUFU
+# instruction ex2.approx.ftz.f32, accurate to about 22 bits over the argument
+# range a decay takes, plus the rounding of its fp32 argument dt * A * log2(e))
+# and 2^-23 for the products and sums, rounded up to one bound per step.
 STEP_EPS = 2.0 ** -21
 
 
