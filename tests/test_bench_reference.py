@@ -2,6 +2,7 @@
 --reference-seconds whatever --steps and --warmup are, because every step runs
 one sample sized from a single probe."""
 import json
+import re
 import subprocess
 import sys
 import time
@@ -35,10 +36,22 @@ def test_many_steps_stay_within_the_budget():
     assert wall < 120.0
 
 
+def _sample_size(line):
+    """(batch rows, channels) of the per-step sample the line reports."""
+    m = re.match(r"the first (\d+) of \d+ batch rows x the first (\d+) of \d+ channels",
+                 line["cpu_baseline"]["sample"])
+    assert m, line["cpu_baseline"]["sample"]
+    return int(m.group(1)), int(m.group(2))
+
+
 def test_sample_grows_with_the_budget():
-    """A larger budget per step takes a larger sample of the same workload."""
+    """A larger budget per step takes a larger sample of the same workload (a
+    tiny one: part of the batch rows of one channel)."""
     small, _ = _reference_line("--workload", "1", "--steps", "4", "--warmup", "0",
-                               "--reference-seconds", "0.05")
+                               "--reference-seconds", "1e-7")
     large, _ = _reference_line("--workload", "1", "--steps", "4", "--warmup", "0",
                                "--reference-seconds", "4")
-    assert large["ms_per_step"] > small["ms_per_step"]
+    nb_s, ch_s = _sample_size(small)
+    nb_l, ch_l = _sample_size(large)
+    assert (nb_s, ch_s) == (1, 1)
+    assert nb_l * ch_l > nb_s * ch_s
