@@ -24,6 +24,14 @@
  * Threading and lifetime: the library keeps no pointer after a call returns
  * and holds no global state besides a per-device error word (see
  * ss_selective_scan_check).  Calls on different streams may run concurrently.
+ *
+ * Devices: a process drives one GPU with this library.  The forward kernels
+ * for 8 or 16 states and the backward's 96-row kernels use more than 48 KB of
+ * dynamic shared memory, and the library raises their limit once per process,
+ * on the device current at its first call; a call that takes one of them on
+ * another device of the same process fails with SS_ERR_CUDA (nothing is
+ * launched, nothing written).  Run one process per GPU (as torchrun does).
+ * The Mamba-2 forward raises its limit per device.
  */
 #ifndef SS_SELECTIVE_SCAN_H_
 #define SS_SELECTIVE_SCAN_H_
